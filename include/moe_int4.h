@@ -1,0 +1,221 @@
+/*
+ * moe_int4.h -- C ABI of a GB300 (sm_103a) routed-MoE layer library.
+ *
+ * The library computes one GLM-5.2 (glm_moe_dsa) routed-MoE layer forward:
+ * a sigmoid router with correction bias choosing top-K of E experts with
+ * weights sigmoid(logit) * routed_scale, SwiGLU experts stored as packed int4
+ * with one fp32 scale per row, applied to activations quantised per row to
+ * int8, a batch-wide union of experts so each expert's weights are read once,
+ * and an always-on shared expert.
+ *
+ * Sources (page title, section):
+ *   reader.mx, "惊呆了！25GB 内存上运行 GLM 5.2 744B 模型":
+ *     §02 模型与硬件 (model config: hidden 6144, 256 experts, top-8, 1 shared
+ *         expert, moe_intermediate 2048, sigmoid scoring, routed_scaling_factor 2.5),
+ *     §04 手写的基础数学 (rmsnorm with double accumulation; siluf; layer order),
+ *     §06 从 FP8 到 int4 (per-row int4 packing and nibble layout),
+ *     §11 MoE 路由与专家执行 (router, expert union, SwiGLU and weighted add),
+ *     §12 AVX2 整数 kernel (per-row int8 activation quantiser, integer dot).
+ *   besthub.dev, "Running 744B MoE on 25GB RAM: Int4, Disk Streaming & MLA
+ *     Compression", §06, §11, §12 (the same steps summarised).
+ *
+ * Conventions for every call:
+ *   - Pointers are DEVICE pointers unless the parameter says "host".
+ *   - Every call is asynchronous on `stream` (0 = legacy default stream); it
+ *     only validates arguments on the host and enqueues kernels.  No call
+ *     allocates, frees or synchronises, except moe_layer_create / _destroy
+ *     and moe_layer_device_status (which synchronises `stream`).
+ *   - Return value: MOE_OK (0) or a negative MOE_ERR_* code.  On error nothing
+ *     was enqueued unless the code is MOE_ERR_CUDA (a launch failed); the text
+ *     of the last error on the calling thread is in moe_last_error().
+ *   - There is no CPU fallback: a missing GPU or a failed launch is an error.
+ *   - Non-finite inputs (NaN / Inf) are outside the contract; the kernels stay
+ *     memory-safe on them but the results are unspecified.
+ */
+#ifndef MOE_INT4_H
+#define MOE_INT4_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG (-1) /* NULL or misaligned pointer, bad handle, bad scalar */
+#define MOE_ERR_SHAPE (-2)       /* unsupported or mismatched sizes, n_tokens > max_tokens */
+#define MOE_ERR_CUDA (-3)        /* a CUDA call or kernel launch failed */
+#define MOE_ERR_NOMEM (-4)       /* device allocation failed (create only) */
+#define MOE_ERR_DEVICE (-5)      /* a kernel flagged an inconsistency (moe_layer_device_status) */
+
+/* Library version, (major << 16) | minor. */
+int moe_version(void);
+
+/* Text of the last error returned on the calling thread ("" if none).  The
+ * string is owned by the library and valid until the next call on the thread. */
+const char *moe_last_error(void);
+
+/*
+ * Per-row int4 packing of a weight matrix.
+ * reader.mx article §06 (C packer / Python converter); besthub.dev §06.
+ *   w     [O, I] fp32, row-major (any alignment)
+ *   q4    [O, (I+1)/2] uint8 out: byte j of row o holds element 2j in its low
+ *         nibble and element 2j+1 in its high nibble, each stored as value+8;
+ *         an odd I pads the last high nibble with 8 (value 0)
+ *   scale [O] fp32 out: s = max(amax_row / 7, 1e-8)
+ * value = nearest integer of w/s (IEEE division, ties to even), clamped to
+ * [-8, 7].  Byte-exact with the packer described on the pages.
+ * Errors: INVALID_ARG for NULL pointers, SHAPE for O < 0, I < 0 or O*I >= 2^62.
+ */
+int moe_pack_int4(const float *w, uint8_t *q4, float *scale, int64_t O, int64_t I,
+                  cudaStream_t stream);
+
+/*
+ * Per-token int8 activation quantiser.
+ * reader.mx article §12 (qrow_i8); besthub.dev §12.
+ *   x  [n_tokens, D] fp32 row-major;  xq [n_tokens, D] int8 out (natural
+ *   element order);  sx [n_tokens] fp32 out.
+ * s = max(amax_row / 127, 1e-12); inv = 1/s; xq = nearest integer of x*inv
+ * (ties to even).  Bit-exact with the quantiser described on the pages.
+ * Errors: INVALID_ARG for NULL pointers, SHAPE for n_tokens < 0 or D < 1.
+ */
+int moe_quant_act_int8(const float *x, int8_t *xq, float *sx, int n_tokens, int D,
+                       cudaStream_t stream);
+
+/*
+ * Sigmoid router with correction bias and greedy top-K.
+ * reader.mx article §11 (sigmoid(logit)+bias selects, the weight is the plain
+ * sigmoid); §02 config (scoring_func sigmoid, routed_scaling_factor 2.5).
+ *   x    [n_tokens, D] fp32 (the fp32 post-norm activations, not int8)
+ *   Wr   [E, D] fp32 router weight, out-major;  bias [E] fp32
+ *   idx  [n_tokens, K] int32 out, in selection order (descending
+ *        sigmoid(logit)+bias; an exact tie goes to the lower expert index)
+ *   w    [n_tokens, K] fp32 out: sigmoid(logit[idx]) * routed_scale (not
+ *        renormalised)
+ * Logits are accumulated in fp32 (order differs from a sequential loop by
+ * rounding only).  1 <= K <= 16, K <= E <= 512, D % 4 == 0, x and Wr 16-byte
+ * aligned.  Errors: INVALID_ARG, SHAPE.
+ */
+int moe_router_topk(const float *x, const float *Wr, const float *bias, int n_tokens, int D,
+                    int E, int K, float routed_scale, int32_t *idx, float *w,
+                    cudaStream_t stream);
+
+/* Layer description (host struct, copied by create). */
+typedef struct {
+    int D;              /* hidden size (6144 for GLM-5.2); D % 32 == 0, D <= 8192 */
+    int I;              /* expert intermediate size (2048); I % 32 == 0, I <= 8192 */
+    int E;              /* routed experts (256); 1 <= E <= 512 */
+    int K;              /* experts per token (8); 1 <= K <= min(E, 16) */
+    int n_shared;       /* 0 or 1 always-on shared experts, same I as routed */
+    float routed_scale; /* routed_scaling_factor (2.5) */
+    int max_tokens;     /* largest n_tokens any forward will pass; >= 1 */
+} MoeLayerDesc;
+
+/* One expert's packed weights (device pointers, as moe_pack_int4 writes them):
+ * gate_q/up_q [I, D/2] uint8, gate_s/up_s [I] fp32, down_q [D, I/2] uint8,
+ * down_s [D] fp32.  Every pointer 16-byte aligned. */
+typedef struct {
+    const uint8_t *gate_q, *up_q, *down_q;
+    const float *gate_s, *up_s, *down_s;
+} MoeExpertW;
+
+/*
+ * Create a layer handle.
+ *   desc     host: layer sizes;  Wr [E, D] fp32, bias [E] fp32 (device)
+ *   experts  host array of E + n_shared entries; entry E is the shared expert
+ *   handle_out host: receives the handle
+ * Ownership: Wr, bias and every expert buffer stay owned by the caller and
+ * must outlive the handle (they are borrowed, never copied or freed).  The
+ * handle owns a device workspace sized for desc->max_tokens (about
+ * max_tokens * (K+1) * (4*I + 4*D) bytes plus small tables) and a device copy
+ * of the expert pointer table.  Uses the current CUDA device.
+ * Errors: INVALID_ARG, SHAPE, NOMEM, CUDA.
+ */
+int moe_layer_create(const MoeLayerDesc *desc, const float *Wr, const float *bias,
+                     const MoeExpertW *experts, void **handle_out);
+
+/* Release a handle and its workspace (synchronises the device first).
+ * NULL is accepted.  Errors: CUDA. */
+int moe_layer_destroy(void *handle);
+
+/*
+ * One routed-MoE layer forward.
+ * reader.mx article §11 and §12; besthub.dev §11, §12.
+ *   x   [n_tokens, D] fp32;  out [n_tokens, D] fp32 out (may not alias x)
+ * out[t] = sum_k w[t,k] * y_k(t) + y_shared(t), summed in slot order, where
+ * y_e(t) = down_e( hq ) * scales, h = silu(gate_e(xq)) * up_e(xq) requantised
+ * per row to int8, and every dot product is an exact int32 accumulation of
+ * int4 weights with int8 activations; scales are applied as
+ * ((float)acc * s_act) * s_row.  The workspace makes one handle usable by one
+ * stream at a time.  0 <= n_tokens <= max_tokens.  The launch sequence has no
+ * host synchronisation and may be captured in a CUDA graph.
+ * Errors: INVALID_ARG, SHAPE, CUDA.
+ */
+int moe_layer_forward(void *handle, const float *x, int n_tokens, float *out,
+                      cudaStream_t stream);
+
+/*
+ * Residual MoE block of a layer stack: x <- x + MoE(RMSNorm(x)).
+ * reader.mx article §04 (rmsnorm: mean of squares in double, r = 1/sqrtf(ms/D
+ * + eps), x*r*w; layer order norm -> MoE -> residual add).
+ *   x_inout [n_tokens, D] fp32, updated in place;  norm_w [D] fp32;  eps > 0.
+ * Errors: INVALID_ARG, SHAPE, CUDA.
+ */
+int moe_block_forward(void *handle, float *x_inout, const float *norm_w, float eps,
+                      int n_tokens, cudaStream_t stream);
+
+/* Intermediates of one forward, for parity checks.  Every pointer is a device
+ * pointer and may be NULL (not written).  S = K + n_shared; slot s < K is the
+ * s-th selected expert, slot K the shared expert. */
+typedef struct {
+    int32_t *idx;      /* [T, K] */
+    float *w;          /* [T, K] */
+    int8_t *xq;        /* [T, D] natural order */
+    float *sx;         /* [T] */
+    int32_t *gate_acc; /* [T, S, I] int32 gate dot products */
+    int32_t *up_acc;   /* [T, S, I] */
+    int8_t *hq;        /* [T, S, I] requantised h, natural order */
+    float *sh;         /* [T, S] */
+    int32_t *down_acc; /* [T, S, D] */
+    int32_t *union_experts; /* [E + 1] routed union (ascending id) then the shared id E */
+    int32_t *n_union;  /* [1] entries written to union_experts */
+} MoeDebugOut;
+
+/*
+ * Same as moe_layer_forward and also writes the requested intermediates.
+ * `out` may be NULL.  Errors: as moe_layer_forward.
+ */
+int moe_layer_debug(void *handle, const float *x, int n_tokens, float *out,
+                    const MoeDebugOut *dbg_host, cudaStream_t stream);
+
+/*
+ * Synchronise `stream`, then read and clear the handle's device error word
+ * (set by a kernel that met an input outside the contract, e.g. a token with
+ * no finite selection score).  *status_out (host) receives 0 or the flag bits.
+ * Returns MOE_OK, or MOE_ERR_DEVICE when a flag was set.
+ */
+int moe_layer_device_status(void *handle, cudaStream_t stream, int *status_out);
+
+/* Kernel identifiers for moe_layer_set_probe. */
+#define MOE_PROBE_NONE 0
+#define MOE_PROBE_GATE_UP 1
+#define MOE_PROBE_DOWN 2
+#define MOE_PROBE_ROUTER 3
+
+/*
+ * Timing probe: while set, every forward records `begin` on its stream just
+ * before the kernel `which` and `end` just after it (as external event-record
+ * nodes under stream capture).  which = MOE_PROBE_NONE clears it.  The events
+ * are owned by the caller.  Errors: INVALID_ARG.
+ */
+int moe_layer_set_probe(void *handle, int which, cudaEvent_t begin, cudaEvent_t end);
+
+/* Bytes of device workspace a handle with this description owns (host). */
+int moe_layer_workspace_bytes(const MoeLayerDesc *desc, size_t *bytes_out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_INT4_H */

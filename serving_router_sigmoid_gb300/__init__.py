@@ -1,0 +1,218 @@
+"""Thin Python binding of libmoe_int4.so, the GB300 routed-MoE layer library.
+
+Argument marshalling only: every function passes device pointers of torch
+tensors (and the current CUDA stream) to the C ABI declared in
+include/moe_int4.h and raises on a non-zero status.  Every step of the layer
+runs in the library's CUDA kernels; there is no CPU path.  Importing the
+package fails loudly when the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_int4.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = -1
+MOE_ERR_SHAPE = -2
+MOE_ERR_CUDA = -3
+MOE_ERR_NOMEM = -4
+MOE_ERR_DEVICE = -5
+MOE_PROBE_NONE, MOE_PROBE_GATE_UP, MOE_PROBE_DOWN, MOE_PROBE_ROUTER = 0, 1, 2, 3
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with "
+                      "`python -c 'import __graft_entry__ as g; g.build()'`")
+
+
+class MoeLayerDesc(ctypes.Structure):
+    _fields_ = [("D", ctypes.c_int), ("I", ctypes.c_int), ("E", ctypes.c_int), ("K", ctypes.c_int),
+                ("n_shared", ctypes.c_int), ("routed_scale", ctypes.c_float), ("max_tokens", ctypes.c_int)]
+
+
+class MoeExpertW(ctypes.Structure):
+    _fields_ = [("gate_q", ctypes.c_void_p), ("up_q", ctypes.c_void_p), ("down_q", ctypes.c_void_p),
+                ("gate_s", ctypes.c_void_p), ("up_s", ctypes.c_void_p), ("down_s", ctypes.c_void_p)]
+
+
+class MoeDebugOut(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("idx", "w", "xq", "sx", "gate_acc", "up_acc", "hq", "sh", "down_acc", "union_experts",
+                 "n_union")]
+
+
+_lib = ctypes.CDLL(LIB_PATH)
+_vp, _i64, _ci, _cf = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+_SIGS = {
+    "moe_version": ([], _ci),
+    "moe_last_error": ([], ctypes.c_char_p),
+    "moe_pack_int4": ([_vp, _vp, _vp, _i64, _i64, _vp], _ci),
+    "moe_quant_act_int8": ([_vp, _vp, _vp, _ci, _ci, _vp], _ci),
+    "moe_router_topk": ([_vp, _vp, _vp, _ci, _ci, _ci, _ci, _cf, _vp, _vp, _vp], _ci),
+    "moe_layer_create": ([ctypes.POINTER(MoeLayerDesc), _vp, _vp, ctypes.POINTER(MoeExpertW),
+                          ctypes.POINTER(_vp)], _ci),
+    "moe_layer_destroy": ([_vp], _ci),
+    "moe_layer_forward": ([_vp, _vp, _ci, _vp, _vp], _ci),
+    "moe_block_forward": ([_vp, _vp, _vp, _cf, _ci, _vp], _ci),
+    "moe_layer_debug": ([_vp, _vp, _ci, _vp, ctypes.POINTER(MoeDebugOut), _vp], _ci),
+    "moe_layer_device_status": ([_vp, _vp, ctypes.POINTER(_ci)], _ci),
+    "moe_layer_set_probe": ([_vp, _ci, _vp, _vp], _ci),
+    "moe_layer_workspace_bytes": ([ctypes.POINTER(MoeLayerDesc), ctypes.POINTER(ctypes.c_size_t)], _ci),
+}
+for _name, (_args, _res) in _SIGS.items():
+    _f = getattr(_lib, _name)
+    _f.argtypes = _args
+    _f.restype = _res
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[{code}] {msg}")
+        self.code = code
+
+
+def _check(rc: int) -> None:
+    if rc != MOE_OK:
+        raise MoeError(rc, _lib.moe_last_error().decode(errors="replace"))
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor (the library has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def version() -> int:
+    return int(_lib.moe_version())
+
+
+def library():
+    """The ctypes handle of libmoe_int4.so."""
+    return _lib
+
+
+def moe_pack_int4(w, q4, scale, stream=None):
+    O, I = w.shape
+    _check(_lib.moe_pack_int4(_ptr(w), _ptr(q4), _ptr(scale), O, I, _stream(stream)))
+
+
+def moe_quant_act_int8(x, xq, sx, stream=None):
+    T, D = x.shape
+    _check(_lib.moe_quant_act_int8(_ptr(x), _ptr(xq), _ptr(sx), T, D, _stream(stream)))
+
+
+def moe_router_topk(x, Wr, bias, K, routed_scale, idx, w, stream=None):
+    T, D = x.shape
+    E = Wr.shape[0]
+    _check(_lib.moe_router_topk(_ptr(x), _ptr(Wr), _ptr(bias), T, D, E, K, float(routed_scale),
+                                _ptr(idx), _ptr(w), _stream(stream)))
+
+
+def pack_int4(w, stream=None):
+    """Allocating convenience wrapper: w [O, I] fp32 (cuda) -> (q4, scale)."""
+    O, I = w.shape
+    q4 = torch.empty((O, (I + 1) // 2), dtype=torch.uint8, device=w.device)
+    s = torch.empty(O, dtype=torch.float32, device=w.device)
+    moe_pack_int4(w, q4, s, stream)
+    return q4, s
+
+
+class MoeLayer:
+    """Owns a library handle; borrows (and keeps alive) the weight tensors.
+
+    experts: list of E + n_shared tuples (gate_q, gate_s, up_q, up_s, down_q, down_s)
+    of CUDA tensors as moe_pack_int4 writes them; entry E is the shared expert.
+    """
+
+    def __init__(self, D, I, E, K, n_shared, routed_scale, max_tokens, Wr, bias, experts):
+        self.D, self.I, self.E, self.K, self.n_shared = D, I, E, K, n_shared
+        self.S = K + n_shared
+        self.max_tokens = max_tokens
+        self._keep = (Wr, bias, list(experts))
+        desc = MoeLayerDesc(D, I, E, K, n_shared, float(routed_scale), max_tokens)
+        arr = (MoeExpertW * (E + n_shared))()
+        for e, (gq, gs, uq, us, dq, ds) in enumerate(experts):
+            arr[e] = MoeExpertW(_ptr(gq), _ptr(uq), _ptr(dq), _ptr(gs), _ptr(us), _ptr(ds))
+        h = ctypes.c_void_p()
+        _check(_lib.moe_layer_create(ctypes.byref(desc), _ptr(Wr), _ptr(bias), arr, ctypes.byref(h)))
+        self.handle = h
+
+    def close(self):
+        if getattr(self, "handle", None) is not None and self.handle.value:
+            _check(_lib.moe_layer_destroy(self.handle))
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def moe_layer_forward(self, x, out, stream=None):
+        _check(_lib.moe_layer_forward(self.handle, _ptr(x), x.shape[0], _ptr(out), _stream(stream)))
+
+    def forward(self, x, stream=None):
+        out = torch.empty_like(x)
+        self.moe_layer_forward(x, out, stream)
+        return out
+
+    def moe_block_forward(self, x_inout, norm_w, eps, stream=None):
+        _check(_lib.moe_block_forward(self.handle, _ptr(x_inout), _ptr(norm_w), float(eps), x_inout.shape[0],
+                                      _stream(stream)))
+
+    def moe_layer_debug(self, x, out=None, stream=None, **want):
+        """Runs a forward and returns the requested intermediates as tensors.
+        want: any of idx, w, xq, sx, gate_acc, up_acc, hq, sh, down_acc, union (True to request)."""
+        T, dev = x.shape[0], x.device
+        S = self.S
+        shapes = dict(idx=((T, self.K), torch.int32), w=((T, self.K), torch.float32),
+                      xq=((T, self.D), torch.int8), sx=((T,), torch.float32),
+                      gate_acc=((T, S, self.I), torch.int32), up_acc=((T, S, self.I), torch.int32),
+                      hq=((T, S, self.I), torch.int8), sh=((T, S), torch.float32),
+                      down_acc=((T, S, self.D), torch.int32))
+        res = {}
+        for k, (shp, dt) in shapes.items():
+            if want.get(k):
+                res[k] = torch.full(shp, -1, dtype=dt, device=dev) if dt != torch.float32 else \
+                    torch.full(shp, float("nan"), dtype=dt, device=dev)
+        if want.get("union"):
+            res["union_experts"] = torch.full((self.E + 1,), -1, dtype=torch.int32, device=dev)
+            res["n_union"] = torch.zeros(1, dtype=torch.int32, device=dev)
+        d = MoeDebugOut(*[_ptr(res.get(n)) for n, _ in MoeDebugOut._fields_])
+        _check(_lib.moe_layer_debug(self.handle, _ptr(x), T, _ptr(out), ctypes.byref(d), _stream(stream)))
+        return res
+
+    def device_status(self, stream=None) -> int:
+        v = ctypes.c_int(0)
+        rc = _lib.moe_layer_device_status(self.handle, _stream(stream), ctypes.byref(v))
+        if rc not in (MOE_OK, MOE_ERR_DEVICE):
+            _check(rc)
+        return int(v.value)
+
+    def set_probe(self, which, begin=None, end=None):
+        _check(_lib.moe_layer_set_probe(self.handle, int(which),
+                                        ctypes.c_void_p(begin.cuda_event if begin is not None else 0),
+                                        ctypes.c_void_p(end.cuda_event if end is not None else 0)))
+
+
+def workspace_bytes(D, I, E, K, n_shared, max_tokens, routed_scale=2.5) -> int:
+    desc = MoeLayerDesc(D, I, E, K, n_shared, float(routed_scale), max_tokens)
+    n = ctypes.c_size_t(0)
+    _check(_lib.moe_layer_workspace_bytes(ctypes.byref(desc), ctypes.byref(n)))
+    return int(n.value)

@@ -1,0 +1,131 @@
+// common.cuh -- shared device helpers and internal structures of the
+// routed-MoE layer library (sm_103a).  Internal: not part of the C ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/moe_int4.h"
+
+namespace moe {
+
+constexpr int kMaxE = 512;        // routed experts per layer
+constexpr int kMaxK = 16;         // experts per token
+constexpr int kSmallT = 16;       // token count served by the fused small-batch router
+constexpr int kMaxDim = 8192;     // D and I upper bound (GEMV chunks per lane <= 8)
+
+// Device error word bits (moe_layer_device_status).
+constexpr int kErrNoSelection = 1;   // a token had no finite selection score left
+constexpr int kErrRouteCount = 2;    // routing table inconsistent
+
+struct DevExpert {
+    const uint8_t *gq, *uq, *dq;
+    const float *gs, *us, *ds;
+};
+
+// Routing tables built on the device for one forward.  Union entry u covers
+// rows [ubeg[u], ubeg[u+1]) of `rows`; the shared expert (if any) is the last
+// entry with id E.
+struct RouteMeta {
+    int n_union;
+    int n_gu_items;
+    int n_dn_items;
+    int counter;  // last-CTA counter of the small-batch router (reset by that CTA)
+    int uexp[kMaxE + 1];
+    int ubeg[kMaxE + 2];
+};
+
+struct DebugPtrs {
+    int8_t *xq;
+    int32_t *gate_acc, *up_acc;
+    int8_t *hq;
+    float *sh;
+    int32_t *down_acc;
+};
+
+// ------------------------------------------------------------------ helpers
+
+__device__ __forceinline__ float warp_sum_f(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ int warp_sum_i(int v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max_f(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Block-wide max of non-negative floats; every thread gets the result.
+// `red` must hold blockDim.x/32 floats.
+__device__ __forceinline__ float block_max_nonneg(float v, float *red) {
+    v = warp_max_f(v);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float r = lane < nw ? red[lane] : 0.f;
+    r = warp_max_f(r);
+    return r;
+}
+
+__device__ __forceinline__ int block_sum_i(int v, int *red) {
+    v = warp_sum_i(v);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    int r = lane < nw ? red[lane] : 0;
+    r = warp_sum_i(r);
+    return r;
+}
+
+// Streaming 16-byte load of read-once weights: no L1 allocation.
+__device__ __forceinline__ int4 ld_stream16(const void *p) {
+    int4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.s32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// 16-byte load through L2 only (data written earlier in the same grid by other CTAs).
+__device__ __forceinline__ float4 ld_cg_f4(const float *p) { return __ldcg(reinterpret_cast<const float4 *>(p)); }
+
+// Per-row int8 quantisation scale: s = max(amax/127, 1e-12), inv = 1/s, both
+// IEEE-rounded (reader.mx article §12, qrow_i8).
+__device__ __forceinline__ void act_scale(float amax, float &s, float &inv) {
+    s = __fdiv_rn(amax, 127.f);
+    if (s < 1e-12f) s = 1e-12f;
+    inv = __fdiv_rn(1.f, s);
+}
+
+__device__ __forceinline__ int quant_i8(float v, float inv) { return __float2int_rn(__fmul_rn(v, inv)); }
+
+// Byte position of element i (0..7) of an 8-group in the even/odd lane
+// layout used by the int4 GEMV kernels: [x0 x2 x4 x6 | x1 x3 x5 x7].  With
+// that layout the low nibbles of a packed weight word (elements 0,2,4,6) meet
+// the first activation word and the high nibbles the second.
+__device__ __forceinline__ int perm8(int i) { return (i & 1) ? 4 + (i >> 1) : (i >> 1); }
+
+// Sum over the 8 nibble-offset products of one packed weight word against the
+// permuted activations: returns acc + sum_i nibble_i * x_i (nibbles unsigned,
+// 0..15); the caller subtracts 8 * sum(x) once per row.
+__device__ __forceinline__ int dot_word(uint32_t w, int xe, int xo, int acc) {
+    const int lo = static_cast<int>(w & 0x0F0F0F0Fu);
+    const int hi = static_cast<int>((w >> 4) & 0x0F0F0F0Fu);
+    acc = __dp4a(lo, xe, acc);
+    acc = __dp4a(hi, xo, acc);
+    return acc;
+}
+
+__device__ __forceinline__ float silu_f(float g) { return __fdiv_rn(g, __fadd_rn(1.f, expf(-g))); }
+
+}  // namespace moe

@@ -1,0 +1,56 @@
+// layer_args.cuh -- kernel argument block shared by the layer kernels and the
+// host launch code.  Internal.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+struct LayerArgs {
+    int D, I, E, K, S, n_shared, T;
+    float routed_scale;
+    const float *x;      // [T, D] fp32 layer input (post-norm activations)
+    const float *Wr;     // [E, D]
+    const float *bias;   // [E]
+    const DevExpert *experts;  // [E + n_shared]
+    int8_t *xq;          // [Tmax, D] int8, even/odd permuted 8-groups
+    float *sx;           // [Tmax]
+    int32_t *xsum;       // [Tmax] sum of xq over the row
+    float *logits;       // [kSmallT, E]
+    int32_t *idx;        // [Tmax, K]
+    float *wts;          // [Tmax, K]
+    int32_t *rows;       // [Tmax * S] entry ids (t*S + slot) grouped by union expert
+    RouteMeta *meta;
+    float *h;            // [Tmax * S, I] fp32 SwiGLU output, by grouped row
+    uint32_t *hamax;     // [Tmax * S] bits of max|h| per grouped row
+    float *part;         // [Tmax * S, D] expert outputs y by entry id
+    int32_t *dn_cnt;     // [nb_dn] arrival counters of the fused reduce
+    float *out;          // [T, D]
+    const float *resid;  // [T, D] or null: out = resid + MoE
+    int32_t *err;
+    int nb_gu, rpi_gu;   // gate/up: row blocks per expert, rows per block
+    int nb_dn, rpi_dn;   // down: row blocks per expert, rows per block
+    DebugPtrs dbg;
+};
+
+// Host launchers (defined in the .cu files).
+cudaError_t launch_router_small(const LayerArgs &a, cudaStream_t s);
+cudaError_t launch_quant_perm(const LayerArgs &a, cudaStream_t s);
+cudaError_t launch_router_tile(const float *x, const float *Wr, const float *bias, int T, int D,
+                               int E, int K, float scale, int32_t *idx, float *w, int32_t *err,
+                               cudaStream_t s);
+cudaError_t launch_permute(const LayerArgs &a, cudaStream_t s);
+cudaError_t launch_gateup(const LayerArgs &a, int mch, int grid, cudaStream_t s);
+cudaError_t launch_down(const LayerArgs &a, int mch, int grid, bool fused_reduce, cudaStream_t s);
+cudaError_t launch_reduce(const LayerArgs &a, cudaStream_t s);
+cudaError_t launch_rmsnorm(const float *x, const float *w, float eps, float *out, int T, int D,
+                           cudaStream_t s);
+cudaError_t launch_quant_natural(const float *x, int8_t *xq, float *sx, int T, int D,
+                                 cudaStream_t s);
+cudaError_t launch_pack_int4(const float *w, uint8_t *q4, float *scale, int64_t O, int64_t I,
+                             cudaStream_t s);
+// Occupancy-derived grid sizes and kernel attributes (call once per device).
+cudaError_t prepare_expert_kernels(int D, int I, int num_sms, int grid_gu[4], int grid_dn[4]);
+int mch_index(int mch);
+
+}  // namespace moe

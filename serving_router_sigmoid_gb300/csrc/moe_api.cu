@@ -1,0 +1,398 @@
+// moe_api.cu -- the C ABI of the routed-MoE layer library: argument
+// validation, the handle with its device workspace, and the launch sequence of
+// one layer forward.  Every compute step runs in this library's kernels.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "layer_args.cuh"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t ce, const char *what) {
+    return fail(MOE_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(ce), cudaGetErrorName(ce));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr uint32_t kMagic = 0x4d6f4534u;  // handle tag
+
+struct Handle {
+    uint32_t magic;
+    int device;
+    MoeLayerDesc d;
+    int S;
+    const float *Wr, *bias;
+    moe::DevExpert *experts;  // device table [E + n_shared]
+    // workspace
+    void *ws;
+    size_t ws_bytes;
+    int8_t *xq;
+    float *sx;
+    int32_t *xsum;
+    float *logits;
+    int32_t *idx;
+    float *wts;
+    int32_t *rows;
+    moe::RouteMeta *meta;
+    float *h;
+    uint32_t *hamax;
+    float *part;
+    int32_t *dn_cnt;
+    int32_t *err;
+    float *xnorm;  // [Tmax, D] RMSNorm output of moe_block_forward
+    int nb_gu, rpi_gu, nb_dn, rpi_dn;
+    int grid_gu[4], grid_dn[4];
+    int probe_which;
+    cudaEvent_t probe_begin, probe_end;
+};
+
+constexpr int kRpiGu = 16;  // gate/up rows per item: 2 per warp
+constexpr int kRpiDn = 32;  // down rows per item: 4 per warp
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Workspace layout; returns the total and fills offsets when h != nullptr.
+size_t layout(const MoeLayerDesc &d, Handle *h) {
+    const size_t T = (size_t)d.max_tokens, S = (size_t)d.K + d.n_shared;
+    const size_t D = d.D, I = d.I, E = d.E, K = d.K;
+    const size_t nb_dn = (D + kRpiDn - 1) / kRpiDn;
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
+    const size_t o_xq = take(T * D);
+    const size_t o_sx = take(4 * T);
+    const size_t o_xsum = take(4 * T);
+    const size_t o_logits = take(4 * moe::kSmallT * E);
+    const size_t o_idx = take(4 * T * K);
+    const size_t o_wts = take(4 * T * K);
+    const size_t o_rows = take(4 * T * S);
+    const size_t o_meta = take(sizeof(moe::RouteMeta));
+    const size_t o_h = take(4 * T * S * I);
+    const size_t o_hamax = take(4 * T * S);
+    const size_t o_part = take(4 * T * S * D);
+    const size_t o_cnt = take(4 * nb_dn);
+    const size_t o_err = take(4);
+    const size_t o_xn = take(4 * T * D);
+    if (h) {
+        char *b = static_cast<char *>(h->ws);
+        h->xq = reinterpret_cast<int8_t *>(b + o_xq);
+        h->sx = reinterpret_cast<float *>(b + o_sx);
+        h->xsum = reinterpret_cast<int32_t *>(b + o_xsum);
+        h->logits = reinterpret_cast<float *>(b + o_logits);
+        h->idx = reinterpret_cast<int32_t *>(b + o_idx);
+        h->wts = reinterpret_cast<float *>(b + o_wts);
+        h->rows = reinterpret_cast<int32_t *>(b + o_rows);
+        h->meta = reinterpret_cast<moe::RouteMeta *>(b + o_meta);
+        h->h = reinterpret_cast<float *>(b + o_h);
+        h->hamax = reinterpret_cast<uint32_t *>(b + o_hamax);
+        h->part = reinterpret_cast<float *>(b + o_part);
+        h->dn_cnt = reinterpret_cast<int32_t *>(b + o_cnt);
+        h->err = reinterpret_cast<int32_t *>(b + o_err);
+        h->xnorm = reinterpret_cast<float *>(b + o_xn);
+    }
+    return off;
+}
+
+int check_desc(const MoeLayerDesc *d) {
+    if (!d) return fail(MOE_ERR_INVALID_ARG, "desc is NULL");
+    if (d->D < 32 || d->D > moe::kMaxDim || d->D % 32)
+        return fail(MOE_ERR_SHAPE, "D=%d: need 32 <= D <= %d and D %% 32 == 0", d->D, moe::kMaxDim);
+    if (d->I < 32 || d->I > moe::kMaxDim || d->I % 32)
+        return fail(MOE_ERR_SHAPE, "I=%d: need 32 <= I <= %d and I %% 32 == 0", d->I, moe::kMaxDim);
+    if (d->E < 1 || d->E > moe::kMaxE) return fail(MOE_ERR_SHAPE, "E=%d: need 1 <= E <= %d", d->E, moe::kMaxE);
+    if (d->K < 1 || d->K > moe::kMaxK || d->K > d->E)
+        return fail(MOE_ERR_SHAPE, "K=%d: need 1 <= K <= min(E, %d)", d->K, moe::kMaxK);
+    if (d->n_shared < 0 || d->n_shared > 1) return fail(MOE_ERR_SHAPE, "n_shared=%d: need 0 or 1", d->n_shared);
+    if (d->max_tokens < 1 || d->max_tokens > (1 << 20))
+        return fail(MOE_ERR_SHAPE, "max_tokens=%d: need 1 <= max_tokens <= 2^20", d->max_tokens);
+    if (!(d->routed_scale == d->routed_scale)) return fail(MOE_ERR_INVALID_ARG, "routed_scale is NaN");
+    return MOE_OK;
+}
+
+Handle *as_handle(void *p) {
+    Handle *h = static_cast<Handle *>(p);
+    if (!h || h->magic != kMagic) return nullptr;
+    return h;
+}
+
+cudaError_t record(cudaEvent_t ev, cudaStream_t s) {
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    cudaError_t ce = cudaStreamIsCapturing(s, &st);
+    if (ce != cudaSuccess) return ce;
+    if (st == cudaStreamCaptureStatusActive) return cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+    return cudaEventRecord(ev, s);
+}
+
+// The launch sequence of one forward.  x is the layer input (already
+// normalised for a block), out/resid as in LayerArgs.
+int run_layer(Handle *h, const float *x, int T, float *out, const float *resid, const moe::DebugPtrs &dbg,
+              cudaStream_t s) {
+    moe::LayerArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.D = h->d.D; a.I = h->d.I; a.E = h->d.E; a.K = h->d.K; a.S = h->S; a.n_shared = h->d.n_shared; a.T = T;
+    a.routed_scale = h->d.routed_scale;
+    a.x = x; a.Wr = h->Wr; a.bias = h->bias; a.experts = h->experts;
+    a.xq = h->xq; a.sx = h->sx; a.xsum = h->xsum; a.logits = h->logits; a.idx = h->idx; a.wts = h->wts;
+    a.rows = h->rows; a.meta = h->meta; a.h = h->h; a.hamax = h->hamax; a.part = h->part; a.dn_cnt = h->dn_cnt;
+    a.out = out; a.resid = resid; a.err = h->err;
+    a.nb_gu = h->nb_gu; a.rpi_gu = h->rpi_gu; a.nb_dn = h->nb_dn; a.rpi_dn = h->rpi_dn;
+    a.dbg = dbg;
+    const int mch = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8;
+    const int mi = moe::mch_index(mch);
+    const bool small = T <= moe::kSmallT;
+    cudaError_t ce;
+
+    if (h->probe_which == MOE_PROBE_ROUTER && (ce = record(h->probe_begin, s)) != cudaSuccess)
+        return cuda_fail(ce, "probe record");
+    if (small) {
+        if ((ce = moe::launch_router_small(a, s)) != cudaSuccess) return cuda_fail(ce, "router_small launch");
+    } else {
+        if ((ce = moe::launch_quant_perm(a, s)) != cudaSuccess) return cuda_fail(ce, "quant launch");
+        if ((ce = moe::launch_router_tile(x, h->Wr, h->bias, T, a.D, a.E, a.K, a.routed_scale, h->idx, h->wts,
+                                          h->err, s)) != cudaSuccess)
+            return cuda_fail(ce, "router_tile launch");
+        if ((ce = moe::launch_permute(a, s)) != cudaSuccess) return cuda_fail(ce, "permute launch");
+    }
+    if (h->probe_which == MOE_PROBE_ROUTER && (ce = record(h->probe_end, s)) != cudaSuccess)
+        return cuda_fail(ce, "probe record");
+
+    if (h->probe_which == MOE_PROBE_GATE_UP && (ce = record(h->probe_begin, s)) != cudaSuccess)
+        return cuda_fail(ce, "probe record");
+    if ((ce = moe::launch_gateup(a, mch, h->grid_gu[mi], s)) != cudaSuccess) return cuda_fail(ce, "gateup launch");
+    if (h->probe_which == MOE_PROBE_GATE_UP && (ce = record(h->probe_end, s)) != cudaSuccess)
+        return cuda_fail(ce, "probe record");
+
+    if (h->probe_which == MOE_PROBE_DOWN && (ce = record(h->probe_begin, s)) != cudaSuccess)
+        return cuda_fail(ce, "probe record");
+    if ((ce = moe::launch_down(a, mch, h->grid_dn[mi], small, s)) != cudaSuccess) return cuda_fail(ce, "down launch");
+    if (!small && (ce = moe::launch_reduce(a, s)) != cudaSuccess) return cuda_fail(ce, "reduce launch");
+    if (h->probe_which == MOE_PROBE_DOWN && (ce = record(h->probe_end, s)) != cudaSuccess)
+        return cuda_fail(ce, "probe record");
+    return MOE_OK;
+}
+
+int check_forward(Handle *h, const float *x, int T, const float *out) {
+    if (!h) return fail(MOE_ERR_INVALID_ARG, "invalid handle");
+    if (T < 0 || T > h->d.max_tokens)
+        return fail(MOE_ERR_SHAPE, "n_tokens=%d outside [0, max_tokens=%d]", T, h->d.max_tokens);
+    if (T == 0) return MOE_OK;
+    if (!x || !out) return fail(MOE_ERR_INVALID_ARG, "x or out is NULL");
+    if (!aligned16(x) || !aligned16(out)) return fail(MOE_ERR_INVALID_ARG, "x and out must be 16-byte aligned");
+    int dev = -1;
+    cudaError_t ce = cudaGetDevice(&dev);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cudaGetDevice");
+    if (dev != h->device) return fail(MOE_ERR_INVALID_ARG, "current device %d is not the handle's device %d", dev, h->device);
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_version(void) { return (1 << 16) | 0; }
+
+const char *moe_last_error(void) { return g_err; }
+
+int moe_pack_int4(const float *w, uint8_t *q4, float *scale, int64_t O, int64_t I, cudaStream_t stream) {
+    if (O < 0 || I < 0) return fail(MOE_ERR_SHAPE, "O=%lld I=%lld must be >= 0", (long long)O, (long long)I);
+    if (O == 0) return MOE_OK;
+    if (I > 0 && O > ((int64_t)1 << 62) / I) return fail(MOE_ERR_SHAPE, "O*I too large");
+    if (!w || !q4 || !scale) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+    cudaError_t ce = moe::launch_pack_int4(w, q4, scale, O, I, stream);
+    return ce == cudaSuccess ? MOE_OK : cuda_fail(ce, "pack_int4 launch");
+}
+
+int moe_quant_act_int8(const float *x, int8_t *xq, float *sx, int n_tokens, int D, cudaStream_t stream) {
+    if (n_tokens < 0 || D < 1) return fail(MOE_ERR_SHAPE, "n_tokens=%d D=%d", n_tokens, D);
+    if (n_tokens == 0) return MOE_OK;
+    if (!x || !xq || !sx) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+    cudaError_t ce = moe::launch_quant_natural(x, xq, sx, n_tokens, D, stream);
+    return ce == cudaSuccess ? MOE_OK : cuda_fail(ce, "quant launch");
+}
+
+int moe_router_topk(const float *x, const float *Wr, const float *bias, int n_tokens, int D, int E, int K,
+                    float routed_scale, int32_t *idx, float *w, cudaStream_t stream) {
+    if (n_tokens < 0 || D < 4 || D % 4 || E < 1 || E > moe::kMaxE || K < 1 || K > moe::kMaxK || K > E)
+        return fail(MOE_ERR_SHAPE, "n_tokens=%d D=%d E=%d K=%d", n_tokens, D, E, K);
+    if (n_tokens == 0) return MOE_OK;
+    if (!x || !Wr || !bias || !idx || !w) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned16(x) || !aligned16(Wr)) return fail(MOE_ERR_INVALID_ARG, "x and Wr must be 16-byte aligned");
+    cudaError_t ce = moe::launch_router_tile(x, Wr, bias, n_tokens, D, E, K, routed_scale, idx, w, nullptr, stream);
+    return ce == cudaSuccess ? MOE_OK : cuda_fail(ce, "router launch");
+}
+
+int moe_layer_workspace_bytes(const MoeLayerDesc *desc, size_t *bytes_out) {
+    int rc = check_desc(desc);
+    if (rc) return rc;
+    if (!bytes_out) return fail(MOE_ERR_INVALID_ARG, "bytes_out is NULL");
+    *bytes_out = layout(*desc, nullptr);
+    return MOE_OK;
+}
+
+int moe_layer_create(const MoeLayerDesc *desc, const float *Wr, const float *bias, const MoeExpertW *experts,
+                     void **handle_out) {
+    int rc = check_desc(desc);
+    if (rc) return rc;
+    if (!Wr || !bias || !experts || !handle_out) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned16(Wr)) return fail(MOE_ERR_INVALID_ARG, "Wr must be 16-byte aligned");
+    const int ne = desc->E + desc->n_shared;
+    for (int e = 0; e < ne; ++e) {
+        const MoeExpertW &x = experts[e];
+        if (!x.gate_q || !x.up_q || !x.down_q || !x.gate_s || !x.up_s || !x.down_s)
+            return fail(MOE_ERR_INVALID_ARG, "expert %d has a NULL pointer", e);
+        if (!aligned16(x.gate_q) || !aligned16(x.up_q) || !aligned16(x.down_q))
+            return fail(MOE_ERR_INVALID_ARG, "expert %d weights must be 16-byte aligned", e);
+    }
+    *handle_out = nullptr;
+    Handle *h = new (std::nothrow) Handle();
+    if (!h) return fail(MOE_ERR_NOMEM, "host allocation failed");
+    std::memset(h, 0, sizeof *h);
+    h->d = *desc;
+    h->S = desc->K + desc->n_shared;
+    h->Wr = Wr;
+    h->bias = bias;
+    h->rpi_gu = kRpiGu;
+    h->nb_gu = (desc->I + kRpiGu - 1) / kRpiGu;
+    h->rpi_dn = kRpiDn;
+    h->nb_dn = (desc->D + kRpiDn - 1) / kRpiDn;
+    cudaError_t ce;
+    int nsm = 0;
+    if ((ce = cudaGetDevice(&h->device)) != cudaSuccess ||
+        (ce = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, h->device)) != cudaSuccess) {
+        delete h;
+        return cuda_fail(ce, "device query");
+    }
+    if ((ce = moe::prepare_expert_kernels(desc->D, desc->I, nsm, h->grid_gu, h->grid_dn)) != cudaSuccess) {
+        delete h;
+        return cuda_fail(ce, "kernel attributes");
+    }
+    h->ws_bytes = layout(*desc, nullptr);
+    if ((ce = cudaMalloc(&h->ws, h->ws_bytes)) != cudaSuccess) {
+        cudaGetLastError();
+        delete h;
+        return fail(MOE_ERR_NOMEM, "workspace of %zu bytes: %s", h->ws_bytes, cudaGetErrorString(ce));
+    }
+    layout(*desc, h);
+    if ((ce = cudaMalloc(&h->experts, sizeof(moe::DevExpert) * ne)) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(h->ws);
+        delete h;
+        return fail(MOE_ERR_NOMEM, "expert table: %s", cudaGetErrorString(ce));
+    }
+    moe::DevExpert *tab = new (std::nothrow) moe::DevExpert[ne];
+    if (!tab) {
+        cudaFree(h->ws);
+        cudaFree(h->experts);
+        delete h;
+        return fail(MOE_ERR_NOMEM, "host allocation failed");
+    }
+    for (int e = 0; e < ne; ++e)
+        tab[e] = moe::DevExpert{experts[e].gate_q, experts[e].up_q, experts[e].down_q,
+                                experts[e].gate_s, experts[e].up_s, experts[e].down_s};
+    ce = cudaMemcpy(h->experts, tab, sizeof(moe::DevExpert) * ne, cudaMemcpyHostToDevice);
+    delete[] tab;
+    if (ce == cudaSuccess) ce = cudaMemset(h->ws, 0, h->ws_bytes);
+    if (ce == cudaSuccess) ce = cudaDeviceSynchronize();
+    if (ce != cudaSuccess) {
+        cudaFree(h->ws);
+        cudaFree(h->experts);
+        delete h;
+        return cuda_fail(ce, "handle initialisation");
+    }
+    h->magic = kMagic;
+    *handle_out = h;
+    return MOE_OK;
+}
+
+int moe_layer_destroy(void *handle) {
+    if (!handle) return MOE_OK;
+    Handle *h = as_handle(handle);
+    if (!h) return fail(MOE_ERR_INVALID_ARG, "invalid handle");
+    cudaError_t ce = cudaDeviceSynchronize();
+    cudaFree(h->ws);
+    cudaFree(h->experts);
+    h->magic = 0;
+    delete h;
+    return ce == cudaSuccess ? MOE_OK : cuda_fail(ce, "destroy");
+}
+
+int moe_layer_forward(void *handle, const float *x, int n_tokens, float *out, cudaStream_t stream) {
+    Handle *h = as_handle(handle);
+    int rc = check_forward(h, x, n_tokens, out);
+    if (rc || n_tokens == 0) return rc;
+    if (x == out) return fail(MOE_ERR_INVALID_ARG, "out may not alias x");
+    return run_layer(h, x, n_tokens, out, nullptr, moe::DebugPtrs{}, stream);
+}
+
+int moe_block_forward(void *handle, float *x_inout, const float *norm_w, float eps, int n_tokens,
+                      cudaStream_t stream) {
+    Handle *h = as_handle(handle);
+    int rc = check_forward(h, x_inout, n_tokens, x_inout);
+    if (rc || n_tokens == 0) return rc;
+    if (!norm_w) return fail(MOE_ERR_INVALID_ARG, "norm_w is NULL");
+    if (!(eps >= 0.f)) return fail(MOE_ERR_INVALID_ARG, "eps must be >= 0");
+    cudaError_t ce = moe::launch_rmsnorm(x_inout, norm_w, eps, h->xnorm, n_tokens, h->d.D, stream);
+    if (ce != cudaSuccess) return cuda_fail(ce, "rmsnorm launch");
+    return run_layer(h, h->xnorm, n_tokens, x_inout, x_inout, moe::DebugPtrs{}, stream);
+}
+
+int moe_layer_debug(void *handle, const float *x, int n_tokens, float *out, const MoeDebugOut *dbg,
+                    cudaStream_t stream) {
+    Handle *h = as_handle(handle);
+    if (!h) return fail(MOE_ERR_INVALID_ARG, "invalid handle");
+    if (!dbg) return fail(MOE_ERR_INVALID_ARG, "dbg is NULL");
+    float *o = out ? out : h->xnorm;  // scratch output when the caller does not want it
+    int rc = check_forward(h, x, n_tokens, o);
+    if (rc || n_tokens == 0) return rc;
+    moe::DebugPtrs p{dbg->xq, dbg->gate_acc, dbg->up_acc, dbg->hq, dbg->sh, dbg->down_acc};
+    rc = run_layer(h, x, n_tokens, o, nullptr, p, stream);
+    if (rc) return rc;
+    cudaError_t ce = cudaSuccess;
+    const size_t TK = (size_t)n_tokens * h->d.K;
+    if (dbg->idx && ce == cudaSuccess) ce = cudaMemcpyAsync(dbg->idx, h->idx, 4 * TK, cudaMemcpyDeviceToDevice, stream);
+    if (dbg->w && ce == cudaSuccess) ce = cudaMemcpyAsync(dbg->w, h->wts, 4 * TK, cudaMemcpyDeviceToDevice, stream);
+    if (dbg->sx && ce == cudaSuccess)
+        ce = cudaMemcpyAsync(dbg->sx, h->sx, 4 * (size_t)n_tokens, cudaMemcpyDeviceToDevice, stream);
+    if (dbg->union_experts && ce == cudaSuccess)
+        ce = cudaMemcpyAsync(dbg->union_experts, h->meta->uexp, 4 * (size_t)(h->d.E + 1), cudaMemcpyDeviceToDevice,
+                             stream);
+    if (dbg->n_union && ce == cudaSuccess)
+        ce = cudaMemcpyAsync(dbg->n_union, &h->meta->n_union, 4, cudaMemcpyDeviceToDevice, stream);
+    return ce == cudaSuccess ? MOE_OK : cuda_fail(ce, "debug copies");
+}
+
+int moe_layer_device_status(void *handle, cudaStream_t stream, int *status_out) {
+    Handle *h = as_handle(handle);
+    if (!h || !status_out) return fail(MOE_ERR_INVALID_ARG, "invalid handle or NULL status_out");
+    int v = 0;
+    cudaError_t ce = cudaStreamSynchronize(stream);
+    if (ce == cudaSuccess) ce = cudaMemcpy(&v, h->err, 4, cudaMemcpyDeviceToHost);
+    if (ce == cudaSuccess) ce = cudaMemset(h->err, 0, 4);
+    if (ce != cudaSuccess) return cuda_fail(ce, "device status");
+    *status_out = v;
+    return v ? fail(MOE_ERR_DEVICE, "device error flags 0x%x", v) : MOE_OK;
+}
+
+int moe_layer_set_probe(void *handle, int which, cudaEvent_t begin, cudaEvent_t end) {
+    Handle *h = as_handle(handle);
+    if (!h) return fail(MOE_ERR_INVALID_ARG, "invalid handle");
+    if (which < MOE_PROBE_NONE || which > MOE_PROBE_ROUTER) return fail(MOE_ERR_INVALID_ARG, "bad probe id %d", which);
+    if (which != MOE_PROBE_NONE && (!begin || !end)) return fail(MOE_ERR_INVALID_ARG, "NULL event");
+    h->probe_which = which;
+    h->probe_begin = begin;
+    h->probe_end = end;
+    return MOE_OK;
+}
+
+}  // extern "C"
