@@ -1,0 +1,529 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 routed-MoE layer (GLM-5.2 sigmoid router, int4 experts).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+One step = one pass of the whole layer (router, activation quantiser, expert
+union, fused gate/up, down + ordered reduction) over one batch of synthetic
+input.  The default workload is the GLM-5.2-shaped layer at decode batch 1
+(hidden 6144, 256 experts top-8, intermediate 2048, 1 shared expert, int4
+per-row weights).  Eight independently seeded layer weight sets (4.86 GB each)
+stay resident and the steps cycle through them, so every step streams weights
+that are not in L2 (1.2 GB of other weights pass between two uses of a set).
+
+`value` is tokens/s with inputs already in HBM, timed with CUDA events over
+exactly K steps (CUDA-graph replays), max over ranks.  `e2e` is the same
+metric through the C ABI with x copied in from pinned host memory and the
+output copied back every step.  `roofline` reports the dominant kernel
+(fused gate/up) against the measured HBM copy bandwidth.  `cpu_baseline` is
+the plain CPU oracle timed on a bounded sample of the same workload.
+
+--impl reference times that oracle as the reference arm (rank 0 only).
+Multi-GPU (torchrun): independent replicas, one per GPU, no collective on the
+data path; weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s and achieved HBM GB/s vs ~8 TB/s (decode), int8 TOPS (prefill)"
+UNIT = "tokens/s"
+WORKLOADS = {
+    # name: (synth config, residual block stack?)
+    "glm_moe_layer_decode_b1": ("glm_decode_b1", False),
+    "glm_moe_layer_verify_b8": ("glm_verify_b8", False),
+    "glm_moe_layer_prefill_2048": ("glm_prefill_2048", False),
+    "glm_moe_stack8_decode_b1": ("glm_stack8_b1", True),
+    "glm_moe_stack8_decode_b8": ("glm_stack8_b8", True),
+}
+DEFAULT_WORKLOAD = "glm_moe_layer_decode_b1"
+HOT_KERNEL = "fused int4 gate/up + SiLU*up (gateup_kernel)"
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=200)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    p.add_argument("--layers", type=int, default=8, help="resident layer weight sets cycled by the steps")
+    p.add_argument("--light", action="store_true",
+                   help="profiling only: 17 physical experts aliased over the 257 table entries")
+    p.add_argument("--no-graph", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU oracle sample budget")
+    p.add_argument("--ref-seconds", type=float, default=150.0, help="reference arm time box")
+    p.add_argument("--probe", choices=["gateup", "down", "router"], default="gateup",
+                   help="kernel timed live by the roofline probe (the roofline figure is the gate/up kernel's)")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def env_rank():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def layer_bytes_per_expert(cfg):
+    import synth
+    return synth.expert_bytes(cfg)
+
+
+def gateup_bytes_per_expert(cfg):
+    return 2 * (cfg.I * (cfg.D // 2) + cfg.I * 4)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled in the background."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev_index):
+        self.proc = None
+        self.path = None
+        self.t_on = self.t_off = None
+        self.bus = None
+        try:
+            import torch
+            props = torch.cuda.get_device_properties(dev_index)
+            bus, dv = getattr(props, "pci_bus_id", None), getattr(props, "pci_device_id", None)
+            if bus is not None and dv is not None:
+                self.bus = f"{bus:02x}:{dv:02x}.0"
+        except Exception:
+            self.bus = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu=pci.bus_id,{self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "50", "-f", self.path]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark_on(self):
+        self.t_on = time.time()
+
+    def mark_off(self):
+        self.t_off = time.time()
+
+    def stop(self):
+        time.sleep(0.15)
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) >= 9 and (self.bus is None or parts[0].lower().endswith(self.bus)):
+                        rows.append(parts)
+            os.unlink(self.path)
+        except Exception:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        loaded = [s for s in sm if mx and s >= 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows),
+                "samples_loaded": len(loaded)}
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------ layer set-up
+
+def build_layers(cfg, n_layers, light, dev, rank_seed=0):
+    """n_layers resident GLM-shaped layers, weights drawn on the GPU from the
+    seeded generator and packed by the library's own int4 packer."""
+    import torch
+    import serving_router_sigmoid_gb300 as moe
+    import synth
+    layers, keep = [], []
+    for l in range(n_layers):
+        lid = l + 1000 * rank_seed
+        Wr = synth.router_weight(cfg, lid).to(dev)
+        bias = synth.router_bias(cfg, lid).to(dev)
+        phys = {}
+        n_phys = 16 if light else cfg.E
+        for e in list(range(n_phys)) + [cfg.E]:
+            g, u, d = synth.expert_fp32(cfg, e, lid, dev)
+            gq, gs = moe.pack_int4(g)
+            uq, us = moe.pack_int4(u)
+            dq, ds = moe.pack_int4(d)
+            phys[e] = (gq, gs, uq, us, dq, ds)
+            del g, u, d
+        table = [phys[e if e < n_phys or e == cfg.E else e % n_phys] for e in range(cfg.E)] + [phys[cfg.E]]
+        layers.append(moe.MoeLayer(cfg.D, cfg.I, cfg.E, cfg.K, cfg.n_shared, cfg.routed_scale, max(cfg.T, 1),
+                                   Wr, bias, table))
+        keep.append((Wr, bias, phys))
+    torch.cuda.synchronize()
+    return layers, keep
+
+
+def union_sizes(layers, xs):
+    """(distinct routed experts + shared) per layer for its input, via the debug entry."""
+    import torch
+    sizes = []
+    for layer, x in zip(layers, xs):
+        d = layer.moe_layer_debug(x, union=True)
+        torch.cuda.synchronize()
+        sizes.append(int(d["n_union"].item()))
+    return sizes
+
+
+# ----------------------------------------------------------------- our arm
+
+def run_ours(args, cfg, stack, rank, world, local):
+    import torch
+    import serving_router_sigmoid_gb300 as moe
+    import synth
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    n_layers = 8 if stack else max(1, args.layers)
+    t_setup = time.time()
+    layers, keep = build_layers(cfg, n_layers, args.light, dev, rank_seed=rank)
+    T = cfg.T
+    s = torch.cuda.Stream(device=dev)
+    norm_w = synth.norm_weight(cfg, dev)
+    # inputs: one token batch per layer set (single layer), or a pool of batches (stack)
+    xs = [synth.x_rows(cfg, T, "cpu", "bench-x", l + 100 * rank).to(dev) for l in range(n_layers)]
+    outs = [torch.empty_like(x) for x in xs]
+    xwork = torch.empty((T, cfg.D), device=dev)
+
+    def step_fn(i):
+        if stack:
+            xwork.copy_(xs[i % n_layers])
+            for layer in layers:
+                layer.moe_block_forward(xwork, norm_w, cfg.eps)
+        else:
+            layers[i % n_layers].moe_layer_forward(xs[i % n_layers], outs[i % n_layers])
+
+    # one graph per layer set (single layer) or two alternating graphs (stack),
+    # each with its own probe events so a step's probe is read while the next
+    # step runs
+    n_graph = 2 if stack else n_layers
+    probes = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_graph)]
+    use_graph = not args.no_graph
+    graphs = []
+    with torch.cuda.stream(s):
+        for i in range(n_graph):  # eager warm-up of every code path
+            step_fn(i)
+        torch.cuda.synchronize()
+        probe_id = {"gateup": moe.MOE_PROBE_GATE_UP, "down": moe.MOE_PROBE_DOWN,
+                    "router": moe.MOE_PROBE_ROUTER}[args.probe]
+        if not stack:
+            for l, layer in enumerate(layers):
+                layer.set_probe(probe_id, *probes[l])
+        if use_graph:
+            for i in range(n_graph):
+                if stack:
+                    layers[0].set_probe(probe_id, *probes[i])
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=s):
+                    step_fn(i)
+                graphs.append(g)
+        elif stack:
+            layers[0].set_probe(probe_id, *probes[0])
+            n_graph = 1
+        torch.cuda.synchronize()
+
+    def launch(i):
+        if use_graph:
+            graphs[i % n_graph].replay()
+        else:
+            step_fn(i)
+
+    kernels_per_forward = (3 if T <= 16 else 6) + (1 if stack else 0)
+    launches_per_step = kernels_per_forward * (len(layers) if stack else 1)
+    setup_s = time.time() - t_setup
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    # warm-up: at least W steps and at least ~0.5 s of work so clocks ramp up
+    w_done = 0
+    t0 = time.time()
+    with torch.cuda.stream(s):
+        while w_done < args.warmup or time.time() - t0 < 0.5:
+            launch(w_done)
+            w_done += 1
+            if w_done % 64 == 0:
+                s.synchronize()
+        s.synchronize()
+
+    K = args.steps
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    probe_ms = []
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.mark_on()
+    with torch.cuda.stream(s):
+        ev0.record(s)
+        for i in range(K):
+            launch(w_done + i)
+            if i >= 1:
+                b, e = probes[(w_done + i - 1) % n_graph]
+                e.synchronize()
+                probe_ms.append(b.elapsed_time(e))
+        ev1.record(s)
+    torch.cuda.synchronize()
+    b, e = probes[(w_done + K - 1) % n_graph]
+    probe_ms.append(b.elapsed_time(e))
+    clocks.mark_off()
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    clk = clocks.stop()
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    tokens = T * K * world
+    value = tokens / (elapsed_ms / 1e3)
+    ms_per_step = elapsed_ms / K
+
+    # algorithmic bytes of the dominant kernel and of a whole step
+    u1 = union_sizes(layers, xs if not stack else [xs[0]] * len(layers))
+    u1_mean = sum(u1) / len(u1)
+    gu_bytes = u1_mean * gateup_bytes_per_expert(cfg) + T * cfg.D + T * cfg.S * cfg.I * 4
+    step_bytes_layer = u1_mean * layer_bytes_per_expert(cfg) + cfg.E * cfg.D * 4 + cfg.E * 4 + 2 * T * cfg.D * 4
+    step_bytes = step_bytes_layer * (len(layers) if stack else 1)
+    peak, peak_kind = measured_peak()
+    probe_avg_ms = sum(probe_ms) / len(probe_ms)
+    achieved = gu_bytes / (probe_avg_ms / 1e3) / 1e9
+
+    # end to end through the C ABI: pinned host x -> device, forward, out -> pinned host
+    e2e = None
+    if not args.no_e2e:
+        Ke = max(16, min(K, 2000))
+        xh = [x.cpu().pin_memory() for x in xs]
+        oh = torch.empty((T, cfg.D), dtype=torch.float32).pin_memory()
+        xd = torch.empty((T, cfg.D), device=dev)
+        od = torch.empty((T, cfg.D), device=dev)
+        for lyr in layers:
+            lyr.set_probe(moe.MOE_PROBE_NONE)
+
+        def e2e_step(i):
+            xd.copy_(xh[i % n_layers], non_blocking=True)
+            if stack:
+                for lyr in layers:
+                    lyr.moe_block_forward(xd, norm_w, cfg.eps)
+                oh.copy_(xd, non_blocking=True)
+            else:
+                layers[i % n_layers].moe_layer_forward(xd, od)
+                oh.copy_(od, non_blocking=True)
+
+        with torch.cuda.stream(s):
+            for i in range(min(64, Ke)):
+                e2e_step(i)
+            s.synchronize()
+            if world > 1:
+                torch.distributed.barrier()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(s)
+            for i in range(Ke):
+                e2e_step(i)
+            a1.record(s)
+            s.synchronize()
+        e_ms = a0.elapsed_time(a1)
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": T * Ke * world / (e_ms / 1e3), "unit": UNIT, "steps": Ke,
+               "h2d_bytes_per_step": T * cfg.D * 4, "d2h_bytes_per_step": T * cfg.D * 4,
+               "api": "moe_block_forward" if stack else "moe_layer_forward", "graph": False}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(cfg, stack, args.cpu_seconds, dev)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": w_done,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int4 weights x int8 activations -> int32, fp32 scales", "data": "synthetic",
+        "config": {"workload": args.workload, "hidden": cfg.D, "moe_intermediate": cfg.I, "experts": cfg.E,
+                   "top_k": cfg.K, "shared_experts": cfg.n_shared, "tokens_per_step": T,
+                   "layers_per_step": len(layers) if stack else 1, "layer_sets_cycled": n_layers,
+                   "routed_scale": cfg.routed_scale, "zipf_skew": cfg.skew,
+                   "experts_streamed_per_layer": u1_mean, "cuda_graph": use_graph, "light": args.light,
+                   "l2": ("inputs larger than L2: the steps cycle %d resident layer weight sets "
+                          "(%.2f GB between reuses of a set)" % (n_layers, (n_layers - 1) * step_bytes_layer / 1e9))
+                   if n_layers > 1 or T > 1 else "single set",
+                   "parallelism": f"replicas x{world}"},
+        "hbm_gbs_step": step_bytes / (ms_per_step / 1e3) / 1e9,
+        "roofline": {"bound": "hbm", "kernel": HOT_KERNEL if args.probe == "gateup" else args.probe, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
+                     "algorithmic_bytes_per_launch": gu_bytes, "avg_launch_ms": probe_avg_ms,
+                     "launches_timed": len(probe_ms)},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+        "setup_s": round(setup_s, 1),
+    }
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    for lyr in layers:
+        lyr.close()
+    return line if rank == 0 else None
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def _oracle_layer_for(cfg, x_np, layer_id, dev):
+    import oracle
+    import synth
+    Wr = synth.router_weight(cfg, layer_id).numpy()
+    b = synth.router_bias(cfg, layer_id).numpy()
+    idx, _, _ = oracle.router(x_np, Wr, b, cfg.K, cfg.routed_scale)
+    need = sorted(set(idx.reshape(-1).tolist()) | {cfg.E})
+    ex = {}
+    for e in need:
+        g, u, d = synth.expert_fp32(cfg, e, layer_id, dev)
+        ex[e] = oracle.pack_expert(g.cpu().numpy(), u.cpu().numpy(), d.cpu().numpy())
+    return oracle.Layer(cfg.D, cfg.I, cfg.E, cfg.K, cfg.n_shared, cfg.routed_scale, Wr, b, ex)
+
+
+def cpu_baseline(cfg, stack, budget_s, dev="cpu", max_reps=None):
+    """The oracle as it stands on this host's cores, on a bounded sample: a few
+    tokens of the workload (through all 8 layers for the stack) repeated until
+    the budget is used.  Returns the cpu_baseline object."""
+    import synth
+    import oracle
+    T_s = 1 if not stack else 1
+    x = synth.x_rows(cfg, max(1, T_s), "cpu", "cpu-sample").numpy()
+    n_l = 8 if stack else 1
+    Ls = [_oracle_layer_for(cfg, x, l, dev) for l in range(n_l)]
+    w = synth.norm_weight(cfg).numpy()
+    reps, t0 = 0, time.time()
+    while True:
+        if stack:
+            y = x.copy()
+            for L in Ls:
+                y = L.block_forward(y, w, cfg.eps)
+        else:
+            Ls[0].forward(x)
+        reps += 1
+        el = time.time() - t0
+        if el >= budget_s or (max_reps and reps >= max_reps):
+            break
+    return {"value": reps * x.shape[0] / el, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{reps} forward(s) of {x.shape[0]} token through {n_l} GLM-shaped layer(s) "
+                      f"({'residual block stack' if stack else 'one MoE layer'}), plain C oracle, "
+                      f"{el:.1f} s wall"}
+
+
+def run_reference(args, cfg, stack, rank):
+    if rank != 0:
+        return None
+    import oracle
+    import synth
+    dev = "cuda" if _has_cuda() else "cpu"
+    x = synth.x_rows(cfg, 1, "cpu", "cpu-sample").numpy()
+    n_l = 8 if stack else 1
+    Ls = [_oracle_layer_for(cfg, x, l, dev) for l in range(n_l)]
+    w = synth.norm_weight(cfg).numpy()
+
+    def one():
+        if stack:
+            y = x.copy()
+            for L in Ls:
+                y = L.block_forward(y, w, cfg.eps)
+        else:
+            Ls[0].forward(x)
+
+    for _ in range(min(args.warmup, 3)):
+        one()
+    t0 = time.time()
+    done = 0
+    while done < args.steps and time.time() - t0 < args.ref_seconds:
+        one()
+        done += 1
+    el = time.time() - t0
+    value = done / el
+    sample = (f"{done} of {args.steps} steps timed (time box {args.ref_seconds:.0f} s); each step 1 token "
+              f"through {n_l} GLM-shaped layer(s) of the plain C oracle; warm-up {min(args.warmup, 3)}")
+    cpu = {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle", "sample": sample}
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * el / max(done, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int4 weights x int8 activations -> int32, fp32 scales",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "hidden": cfg.D, "moe_intermediate": cfg.I, "experts": cfg.E,
+                       "top_k": cfg.K, "shared_experts": cfg.n_shared, "tokens_per_step": 1,
+                       "layers_per_step": n_l},
+            "cpu_baseline": cpu,
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def _has_cuda():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+def main():
+    args = parse_args()
+    rank, world, local = env_rank()
+    import synth
+    cfg = synth.CONFIGS[WORKLOADS[args.workload][0]]
+    stack = WORKLOADS[args.workload][1]
+    if args.impl == "reference":
+        line = run_reference(args, cfg, stack, rank)
+    else:
+        if world != args.gpus:
+            print(f"warning: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
+        line = run_ours(args, cfg, stack, rank, world, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -206,6 +206,9 @@ class MoeLayer:
         return int(v.value)
 
     def set_probe(self, which, begin=None, end=None):
+        for ev in (begin, end):  # torch creates the CUDA event at its first record
+            if ev is not None and not ev.cuda_event:
+                ev.record()
         _check(_lib.moe_layer_set_probe(self.handle, int(which),
                                         ctypes.c_void_p(begin.cuda_event if begin is not None else 0),
                                         ctypes.c_void_p(end.cuda_event if end is not None else 0)))

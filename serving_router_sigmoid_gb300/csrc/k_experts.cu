@@ -289,30 +289,44 @@ __global__ void __launch_bounds__(256) down_kernel(LayerArgs a) {
 // ---------------------------------------------------------------- reduce
 
 // out[t] = (resid[t] +) sum_k w[t,k] * y[t,k] + y[t,shared], slots in order.
+// Every slot's value is loaded before the first add (K <= kMaxK).
 __global__ void __launch_bounds__(256) reduce_kernel(LayerArgs a) {
     const int t = blockIdx.y;
     const int o = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
     if (o >= a.D) return;
     const int K = a.K, S = a.S, D = a.D;
     const float *pt = a.part + (size_t)t * S * D + o;
+    float4 y[kMaxK + 1];
+    float wk[kMaxK];
+#pragma unroll
+    for (int k = 0; k <= kMaxK; ++k) {
+        if (k < S) y[k] = *reinterpret_cast<const float4 *>(pt + (size_t)k * D);
+        if (k < K && k < kMaxK) wk[k] = a.wts[t * K + k];
+    }
+    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (a.resid) r = *reinterpret_cast<const float4 *>(a.resid + (size_t)t * D + o);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = 0; k < K; ++k) {
-        const float wk = a.wts[t * K + k];
-        const float4 y = *reinterpret_cast<const float4 *>(pt + (size_t)k * D);
-        acc.x = __fadd_rn(acc.x, __fmul_rn(wk, y.x));
-        acc.y = __fadd_rn(acc.y, __fmul_rn(wk, y.y));
-        acc.z = __fadd_rn(acc.z, __fmul_rn(wk, y.z));
-        acc.w = __fadd_rn(acc.w, __fmul_rn(wk, y.w));
+#pragma unroll
+    for (int k = 0; k < kMaxK; ++k) {
+        if (k < K) {
+            acc.x = __fadd_rn(acc.x, __fmul_rn(wk[k], y[k].x));
+            acc.y = __fadd_rn(acc.y, __fmul_rn(wk[k], y[k].y));
+            acc.z = __fadd_rn(acc.z, __fmul_rn(wk[k], y[k].z));
+            acc.w = __fadd_rn(acc.w, __fmul_rn(wk[k], y[k].w));
+        }
     }
     if (a.n_shared) {
-        const float4 y = *reinterpret_cast<const float4 *>(pt + (size_t)K * D);
-        acc.x = __fadd_rn(acc.x, y.x);
-        acc.y = __fadd_rn(acc.y, y.y);
-        acc.z = __fadd_rn(acc.z, y.z);
-        acc.w = __fadd_rn(acc.w, y.w);
+#pragma unroll
+        for (int k = 0; k <= kMaxK; ++k) {
+            if (k == K) {
+                acc.x = __fadd_rn(acc.x, y[k].x);
+                acc.y = __fadd_rn(acc.y, y[k].y);
+                acc.z = __fadd_rn(acc.z, y[k].z);
+                acc.w = __fadd_rn(acc.w, y[k].w);
+            }
+        }
     }
     if (a.resid) {
-        const float4 r = *reinterpret_cast<const float4 *>(a.resid + (size_t)t * D + o);
         acc.x = __fadd_rn(r.x, acc.x);
         acc.y = __fadd_rn(r.y, acc.y);
         acc.z = __fadd_rn(r.z, acc.z);

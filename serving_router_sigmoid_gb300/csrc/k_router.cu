@@ -52,25 +52,40 @@ __device__ int block_excl_scan(const int *in, int *out, int n, int *wtot) {
 
 // ---------------------------------------------------------------- quantiser
 
-// One token row, whole block: writes the even/odd permuted int8 row, its
-// scale and the sum of its codes (used by the offset-nibble dot product).
-// D % 8 == 0 and 16-byte aligned rows.
+// One token row, whole block (256 threads): writes the even/odd permuted int8
+// row, its scale and the sum of its codes (used by the offset-nibble dot
+// product).  D % 8 == 0, D <= 8192, 16-byte aligned rows.  Each thread owns up
+// to four 8-element groups, loaded once into registers before any use.
 __device__ void quant_token_perm(const float *__restrict__ xrow, int D, int8_t *__restrict__ xq_row,
                                  float *sx_out, int32_t *xsum_out, int8_t *nat_row) {
     __shared__ float red_f[32];
     __shared__ int red_i[32];
-    float amax = 0.f;
-    for (int i = threadIdx.x * 4; i < D; i += blockDim.x * 4) {
-        const float4 v = __ldg(reinterpret_cast<const float4 *>(xrow + i));
-        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    constexpr int G = kMaxDim / (8 * 256);
+    const int ng = D >> 3;
+    float4 v[2 * G];
+#pragma unroll
+    for (int k = 0; k < G; ++k) {
+        const int g = threadIdx.x + 256 * k;
+        if (g < ng) {
+            v[2 * k] = __ldg(reinterpret_cast<const float4 *>(xrow + 8 * g));
+            v[2 * k + 1] = __ldg(reinterpret_cast<const float4 *>(xrow + 8 * g + 4));
+        } else {
+            v[2 * k] = v[2 * k + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     }
+    float amax = 0.f;
+#pragma unroll
+    for (int k = 0; k < 2 * G; ++k)
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[k].x), fabsf(v[k].y)), fmaxf(fabsf(v[k].z), fabsf(v[k].w))));
     amax = block_max_nonneg(amax, red_f);
     float s, inv;
     act_scale(amax, s, inv);
     int sum = 0;
-    for (int g = threadIdx.x; g < (D >> 3); g += blockDim.x) {
-        const float4 a = __ldg(reinterpret_cast<const float4 *>(xrow + 8 * g));
-        const float4 b = __ldg(reinterpret_cast<const float4 *>(xrow + 8 * g + 4));
+#pragma unroll
+    for (int k = 0; k < G; ++k) {
+        const int g = threadIdx.x + 256 * k;
+        if (g >= ng) continue;
+        const float4 a = v[2 * k], b = v[2 * k + 1];
         const int q0 = quant_i8(a.x, inv), q1 = quant_i8(a.y, inv), q2 = quant_i8(a.z, inv),
                   q3 = quant_i8(a.w, inv), q4 = quant_i8(b.x, inv), q5 = quant_i8(b.y, inv),
                   q6 = quant_i8(b.z, inv), q7 = quant_i8(b.w, inv);
@@ -119,51 +134,60 @@ __device__ __forceinline__ void score(float logit, float b, float &p, float &c) 
     c = __fadd_rn(p, b);
 }
 
+// Order-preserving map of a float onto uint32 (for non-NaN values): larger
+// float <=> larger key, equal floats <=> equal keys.
+__device__ __forceinline__ uint32_t order_key(float v) {
+    const uint32_t u = __float_as_uint(v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 // Greedy top-K of one token by one warp.  Lane l holds experts l + 32 j.
 // Each round takes the largest c among the experts not yet taken; an exact
 // tie goes to the lower expert index (the pages' strict '>' ascending scan).
+// A round is one warp max over the order keys and one warp min over the
+// indices of the lanes that hold that key.  NaN scores never win.
 template <int EPL>
 __device__ void select_topk(const float (&c)[EPL], const float (&p)[EPL], int E, int K, float scale,
                             int32_t *idx_out, float *w_out, int *s_idx_out, int32_t *err) {
     const int lane = threadIdx.x & 31;
+    uint32_t key[EPL];
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) key[j] = (lane + 32 * j < E && !(c[j] != c[j])) ? order_key(c[j]) : 0u;
     uint32_t taken = 0;
     for (int k = 0; k < K; ++k) {
-        float bv = -INFINITY, bp = 0.f;
-        int bi = INT_MAX;
+        // lane-local best: largest key, lowest index on a tie (ascending j)
+        uint32_t bk = 0;
+        int bj = -1;
 #pragma unroll
-        for (int j = 0; j < EPL; ++j) {
-            if (!((taken >> j) & 1u) && lane + 32 * j < E && c[j] > bv) {
-                bv = c[j];
-                bi = lane + 32 * j;
-                bp = p[j];
+        for (int j = 0; j < EPL; ++j)
+            if (!((taken >> j) & 1u) && key[j] > bk) {
+                bk = key[j];
+                bj = j;
             }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            const float op = __shfl_xor_sync(0xffffffffu, bp, o);
-            if (ov > bv || (ov == bv && oi < bi)) {
-                bv = ov;
-                bi = oi;
-                bp = op;
-            }
-        }
-        if (bi == INT_MAX) {
-            // no finite score left (non-finite input): take the lowest free
-            // index with weight 0 and flag the device error word
+        const uint32_t wk = __reduce_max_sync(0xffffffffu, bk);
+        int bi;
+        if (wk == 0u) {
+            // no finite score left (non-finite input): lowest free index, weight 0
             int cand = INT_MAX;
 #pragma unroll
             for (int j = EPL - 1; j >= 0; --j)
                 if (!((taken >> j) & 1u) && lane + 32 * j < E) cand = lane + 32 * j;
             bi = __reduce_min_sync(0xffffffffu, cand);
-            bp = 0.f;
             if (lane == 0 && err) atomicOr(err, kErrNoSelection);
+        } else {
+            bi = __reduce_min_sync(0xffffffffu, (bk == wk && bj >= 0) ? lane + 32 * bj : INT_MAX);
         }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        const int owner = bi & 31, oj = bi >> 5;
+        float pv = 0.f;
+#pragma unroll
+        for (int j = 0; j < EPL; ++j)
+            if (j == oj) pv = p[j];
+        pv = __shfl_sync(0xffffffffu, pv, owner);
+        if (wk == 0u) pv = 0.f;
+        if (lane == owner) taken |= 1u << oj;
         if (lane == 0) {
             idx_out[k] = bi;
-            w_out[k] = __fmul_rn(bp, scale);
+            w_out[k] = __fmul_rn(pv, scale);
             if (s_idx_out) s_idx_out[k] = bi;
         }
     }
@@ -171,51 +195,53 @@ __device__ void select_topk(const float (&c)[EPL], const float (&p)[EPL], int E,
 
 // ------------------------------------------------------- routing tables
 
-// Builds the union tables of a batch from its T*K selections (in shared
-// memory, (token, slot) order).  Block-level; E <= 2*blockDim.x.
+// Builds the union tables of a batch from its n = T*K selections (shared
+// memory, (token, slot) order), n <= blockDim.x.  Thread i ranks selection i
+// by (expert, i): that rank is its row in the expert-grouped order (stable:
+// rows of one expert keep (token, slot) order).  The first selection of each
+// expert also ranks its expert among the distinct ones, which gives the
+// union position (ascending expert id) and the expert's first row.
 __device__ void build_routing_small(const LayerArgs &a, const int *s_idx, int T) {
-    __shared__ int cnt[kMaxE], off[kMaxE], flg[kMaxE], upos[kMaxE], wtot[33];
-    const int E = a.E, K = a.K, S = a.S, n = T * K, tid = threadIdx.x, lane = tid & 31;
-    for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
-    __syncthreads();
-    for (int i = tid; i < n; i += blockDim.x) atomicAdd(&cnt[s_idx[i]], 1);
-    __syncthreads();
-    for (int e = tid; e < E; e += blockDim.x) flg[e] = cnt[e] > 0;
-    __syncthreads();
-    block_excl_scan(cnt, off, E, wtot);
-    const int n_routed = block_excl_scan(flg, upos, E, wtot);
-    for (int e = tid; e < E; e += blockDim.x)
-        if (cnt[e] > 0) {
-            a.meta->uexp[upos[e]] = e;
-            a.meta->ubeg[upos[e]] = off[e];
+    __shared__ int s_first[kSmallT * kMaxK];
+    __shared__ int s_nu;
+    const int K = a.K, S = a.S, n = T * K, tid = threadIdx.x;
+    int e = -1, less = 0;
+    bool first = true;
+    if (tid < n) {
+        e = s_idx[tid];
+        for (int j = 0; j < n; ++j) {
+            const int ej = s_idx[j];
+            less += ej < e;
+            if (ej == e && j < tid) {
+                ++less;
+                first = false;
+            }
         }
+        a.rows[less] = (tid / K) * S + (tid % K);
+        s_first[tid] = first;
+    }
+    if (tid == 0) s_nu = 0;
+    __syncthreads();
+    if (tid < n && first) {
+        int upos = 0;
+        for (int j = 0; j < n; ++j) upos += s_first[j] && s_idx[j] < e;
+        a.meta->uexp[upos] = e;
+        a.meta->ubeg[upos] = less;
+        atomicAdd(&s_nu, 1);
+    }
+    __syncthreads();
     if (tid == 0) {
+        const int n_routed = s_nu;
         int nu = n_routed;
         a.meta->ubeg[n_routed] = n;
         if (a.n_shared) {
-            a.meta->uexp[n_routed] = E;
+            a.meta->uexp[n_routed] = a.E;
             a.meta->ubeg[n_routed + 1] = n + T;
             nu += 1;
         }
         a.meta->n_union = nu;
         a.meta->n_gu_items = nu * a.nb_gu;
         a.meta->n_dn_items = nu * a.nb_dn;
-    }
-    __syncthreads();
-    // stable placement: entries of one expert keep (token, slot) order
-    if (tid < 32) {
-        const unsigned lt = (1u << lane) - 1u;
-        for (int g = 0; g < n; g += 32) {
-            const int i = g + lane;
-            const bool v = i < n;
-            const int e = v ? s_idx[i] : -1;
-            const unsigned m = __match_any_sync(0xffffffffu, e);
-            const int rank = __popc(m & lt);
-            if (v) a.rows[off[e] + rank] = (i / K) * S + (i % K);
-            __syncwarp();
-            if (v && rank == 0) off[e] += __popc(m);
-            __syncwarp();
-        }
     }
     if (a.n_shared)
         for (int t = tid; t < T; t += blockDim.x) a.rows[n + t] = t * S + K;
@@ -224,12 +250,11 @@ __device__ void build_routing_small(const LayerArgs &a, const int *s_idx, int T)
 // --------------------------------------------------- small-batch router
 
 // T <= kSmallT.  CTAs [0, ceil(E/2)) compute the logits of two experts each
-// (four warps per expert, each a quarter of every 512-wide chunk of D);
+// (four warps per expert, each a quarter of D);
 // CTAs [ceil(E/2), ceil(E/2)+T) quantise one token each.  The last CTA to
 // finish (arrival counter, no waiting) runs top-K and builds the union.
 template <int EPL>
 __global__ void __launch_bounds__(256) router_small_kernel(LayerArgs a) {
-    __shared__ __align__(16) float xs[kSmallT * 512];
     __shared__ float red[8][kSmallT];
     __shared__ int s_idx[kSmallT * kMaxK];
     __shared__ int s_last;
@@ -244,42 +269,33 @@ __global__ void __launch_bounds__(256) router_small_kernel(LayerArgs a) {
         if (t == 0)
             for (int i = tid; i < T * a.S; i += blockDim.x) a.hamax[i] = 0u;
     } else {
+        // warp = (expert, quarter of D); all of the warp's router weights are
+        // loaded before any use so the CTA has its whole 2 x 24 KB in flight
         const int e = blockIdx.x * 2 + (warp >> 2), q = warp & 3;
-        float acc[kSmallT];
+        const int L4 = D >> 4;  // float4 per quarter row
+        float4 w[16];
 #pragma unroll
-        for (int t = 0; t < kSmallT; ++t) acc[t] = 0.f;
-        for (int d0 = 0; d0 < D; d0 += 512) {
-            const int nf4 = min(512, D - d0) >> 2;
-            __syncthreads();
-            for (int i = tid; i < T * nf4; i += blockDim.x) {
-                const int t = i / nf4, j = i - t * nf4;
-                reinterpret_cast<float4 *>(xs)[t * 128 + j] =
-                    __ldg(reinterpret_cast<const float4 *>(a.x + (size_t)t * D + d0) + j);
-            }
-            __syncthreads();
-            const int j = q * 32 + lane;
-            if (e < E && j < nf4) {
-                const float4 w = __ldg(reinterpret_cast<const float4 *>(a.Wr + (size_t)e * D + d0) + j);
+        for (int j = 0; j < 16; ++j) {
+            const int c = j * 32 + lane;
+            w[j] = (e < E && c < L4) ? __ldg(reinterpret_cast<const float4 *>(a.Wr + (size_t)e * D) + q * L4 + c)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        for (int t = 0; t < T; ++t) {
+            const float4 *xr = reinterpret_cast<const float4 *>(a.x + (size_t)t * D) + q * L4;
+            float v = 0.f;
 #pragma unroll
-                for (int t = 0; t < kSmallT; ++t) {
-                    if (t < T) {
-                        const float4 xv = reinterpret_cast<const float4 *>(xs)[t * 128 + j];
-                        float v = acc[t];
-                        v = fmaf(w.x, xv.x, v);
-                        v = fmaf(w.y, xv.y, v);
-                        v = fmaf(w.z, xv.z, v);
-                        v = fmaf(w.w, xv.w, v);
-                        acc[t] = v;
-                    }
+            for (int j = 0; j < 16; ++j) {
+                const int c = j * 32 + lane;
+                if (c < L4) {
+                    const float4 xv = __ldg(xr + c);
+                    v = fmaf(w[j].x, xv.x, v);
+                    v = fmaf(w[j].y, xv.y, v);
+                    v = fmaf(w[j].z, xv.z, v);
+                    v = fmaf(w[j].w, xv.w, v);
                 }
             }
-        }
-#pragma unroll
-        for (int t = 0; t < kSmallT; ++t) {
-            if (t < T) {
-                const float v = warp_sum_f(acc[t]);
-                if (lane == 0) red[warp][t] = v;
-            }
+            v = warp_sum_f(v);
+            if (lane == 0) red[warp][t] = v;
         }
         __syncthreads();
         if (tid < 2 * kSmallT) {
@@ -288,12 +304,13 @@ __global__ void __launch_bounds__(256) router_small_kernel(LayerArgs a) {
                 const int w0 = which * 4;
                 const float l = ((red[w0][t] + red[w0 + 1][t]) + red[w0 + 2][t]) + red[w0 + 3][t];
                 a.logits[t * E + e2] = l;
+                __threadfence();  // the writer makes its logit visible before the arrival
             }
         }
     }
 
-    // arrival: the last CTA finishes the routing
-    __threadfence();
+    // arrival: the last CTA finishes the routing (the quantiser CTAs' outputs
+    // are read by later kernels only, so they need no fence here)
     __syncthreads();
     if (tid == 0) s_last = (atomicAdd(&a.meta->counter, 1) == (int)gridDim.x - 1);
     __syncthreads();

@@ -49,6 +49,9 @@ cudaError_t launch_quant_natural(const float *x, int8_t *xq, float *sx, int T, i
                                  cudaStream_t s);
 cudaError_t launch_pack_int4(const float *w, uint8_t *q4, float *scale, int64_t O, int64_t I,
                              cudaStream_t s);
+cudaError_t launch_gateup_stream(const LayerArgs &a, int grid, cudaStream_t s);
+cudaError_t launch_down_stream(const LayerArgs &a, int grid, cudaStream_t s);
+bool stream_supported(int D, int I);
 // Occupancy-derived grid sizes and kernel attributes (call once per device).
 cudaError_t prepare_expert_kernels(int D, int I, int num_sms, int grid_gu[4], int grid_dn[4]);
 int mch_index(int mch);

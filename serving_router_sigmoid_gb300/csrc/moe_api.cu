@@ -54,6 +54,8 @@ struct Handle {
     float *xnorm;  // [Tmax, D] RMSNorm output of moe_block_forward
     int nb_gu, rpi_gu, nb_dn, rpi_dn;
     int grid_gu[4], grid_dn[4];
+    int num_sms;
+    bool stream_ok;  // shapes and alignment the streaming kernels cover
     int probe_which;
     cudaEvent_t probe_begin, probe_end;
 };
@@ -67,7 +69,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 size_t layout(const MoeLayerDesc &d, Handle *h) {
     const size_t T = (size_t)d.max_tokens, S = (size_t)d.K + d.n_shared;
     const size_t D = d.D, I = d.I, E = d.E, K = d.K;
-    const size_t nb_dn = (D + kRpiDn - 1) / kRpiDn;
+    const size_t nb_dn = (D + 15) / 16;  // arrival counters: enough for 16-row tiles
     size_t off = 0;
     auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
     const size_t o_xq = take(T * D);
@@ -167,16 +169,22 @@ int run_layer(Handle *h, const float *x, int T, float *out, const float *resid, 
     if (h->probe_which == MOE_PROBE_ROUTER && (ce = record(h->probe_end, s)) != cudaSuccess)
         return cuda_fail(ce, "probe record");
 
+    // decode-sized batches stream the experts through TMA-fed tensor-core
+    // tiles; larger batches (and shapes the tiles do not cover) use the
+    // row-per-warp dp4a kernels
+    const bool stream = small && h->stream_ok;
     if (h->probe_which == MOE_PROBE_GATE_UP && (ce = record(h->probe_begin, s)) != cudaSuccess)
         return cuda_fail(ce, "probe record");
-    if ((ce = moe::launch_gateup(a, mch, h->grid_gu[mi], s)) != cudaSuccess) return cuda_fail(ce, "gateup launch");
+    ce = stream ? moe::launch_gateup_stream(a, h->num_sms, s) : moe::launch_gateup(a, mch, h->grid_gu[mi], s);
+    if (ce != cudaSuccess) return cuda_fail(ce, "gateup launch");
     if (h->probe_which == MOE_PROBE_GATE_UP && (ce = record(h->probe_end, s)) != cudaSuccess)
         return cuda_fail(ce, "probe record");
 
     if (h->probe_which == MOE_PROBE_DOWN && (ce = record(h->probe_begin, s)) != cudaSuccess)
         return cuda_fail(ce, "probe record");
-    if ((ce = moe::launch_down(a, mch, h->grid_dn[mi], small, s)) != cudaSuccess) return cuda_fail(ce, "down launch");
-    if (!small && (ce = moe::launch_reduce(a, s)) != cudaSuccess) return cuda_fail(ce, "reduce launch");
+    ce = stream ? moe::launch_down_stream(a, h->num_sms, s) : moe::launch_down(a, mch, h->grid_dn[mi], small, s);
+    if (ce != cudaSuccess) return cuda_fail(ce, "down launch");
+    if ((stream || !small) && (ce = moe::launch_reduce(a, s)) != cudaSuccess) return cuda_fail(ce, "reduce launch");
     if (h->probe_which == MOE_PROBE_DOWN && (ce = record(h->probe_end, s)) != cudaSuccess)
         return cuda_fail(ce, "probe record");
     return MOE_OK;
@@ -273,6 +281,8 @@ int moe_layer_create(const MoeLayerDesc *desc, const float *Wr, const float *bia
         delete h;
         return cuda_fail(ce, "device query");
     }
+    h->num_sms = nsm;
+    h->stream_ok = moe::stream_supported(desc->D, desc->I);
     if ((ce = moe::prepare_expert_kernels(desc->D, desc->I, nsm, h->grid_gu, h->grid_dn)) != cudaSuccess) {
         delete h;
         return cuda_fail(ce, "kernel attributes");
