@@ -215,6 +215,35 @@ int moe_layer_set_probe(void *handle, int which, cudaEvent_t begin, cudaEvent_t 
 /* Bytes of device workspace a handle with this description owns (host). */
 int moe_layer_workspace_bytes(const MoeLayerDesc *desc, size_t *bytes_out);
 
+/*
+ * Allocation-free variant of moe_layer_forward.  The pages have no
+ * counterpart: this entry point exists for callers that must not allocate
+ * device memory -- e.g. a host framework or plugin host whose allocator owns
+ * every byte of the GPU, a runtime with a fixed, pre-planned memory budget, or
+ * a latency-critical loop where cudaMalloc (which can synchronise the device)
+ * is not allowed.  It takes no handle and calls no cudaMalloc, cudaFree or
+ * other allocating routine.
+ *   desc        host: layer sizes (max_tokens is ignored)
+ *   Wr, bias    device: as for moe_layer_create
+ *   experts_dev DEVICE array of E + n_shared MoeExpertW (entry E = shared
+ *               expert), owned by the caller, 16-byte aligned
+ *   x, out      device [n_tokens, D] fp32, 16-byte aligned, out != x
+ * The workspace is one static device array of 8 MiB (every GPU that loads the
+ * library holds it until the process exits), which bounds the batch: a batch
+ * whose workspace does not fit (for the GLM-5.2 layer, more than ~26 tokens)
+ * is rejected with MOE_ERR_SHAPE and a message naming the limit.
+ * The first call on a device, with that device current, resolves the array's
+ * device address (cudaGetSymbolAddress) and reads the SM count; make that first
+ * call before any stream capture.  Every call shares the one array and keeps
+ * the previous call's contents (the routing tables, counters and error word are
+ * cleared at the start of each call): calls that overlap on the GPU -- on two
+ * streams, or two threads, at once -- race and must not be issued.
+ * Errors: INVALID_ARG, SHAPE, CUDA.
+ */
+int moe_layer_forward_static(const MoeLayerDesc *desc, const float *Wr, const float *bias,
+                             const MoeExpertW *experts_dev, const float *x, int n_tokens, float *out,
+                             cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

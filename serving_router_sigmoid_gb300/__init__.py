@@ -62,6 +62,7 @@ _SIGS = {
     "moe_layer_device_status": ([_vp, _vp, ctypes.POINTER(_ci)], _ci),
     "moe_layer_set_probe": ([_vp, _ci, _vp, _vp], _ci),
     "moe_layer_workspace_bytes": ([ctypes.POINTER(MoeLayerDesc), ctypes.POINTER(ctypes.c_size_t)], _ci),
+    "moe_layer_forward_static": ([ctypes.POINTER(MoeLayerDesc), _vp, _vp, _vp, _vp, _ci, _vp, _vp], _ci),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -219,3 +220,19 @@ def workspace_bytes(D, I, E, K, n_shared, max_tokens, routed_scale=2.5) -> int:
     n = ctypes.c_size_t(0)
     _check(_lib.moe_layer_workspace_bytes(ctypes.byref(desc), ctypes.byref(n)))
     return int(n.value)
+
+
+def expert_table_device(experts, device):
+    """Device copy of a MoeExpertW array (entry E = shared expert) for
+    moe_layer_forward_static; experts as for MoeLayer."""
+    arr = (MoeExpertW * len(experts))()
+    for e, (gq, gs, uq, us, dq, ds) in enumerate(experts):
+        arr[e] = MoeExpertW(_ptr(gq), _ptr(uq), _ptr(dq), _ptr(gs), _ptr(us), _ptr(ds))
+    return torch.frombuffer(bytearray(bytes(arr)), dtype=torch.uint8).to(device)
+
+
+def moe_layer_forward_static(D, I, E, K, n_shared, routed_scale, Wr, bias, experts_dev, x, out, stream=None):
+    """The allocation-free forward: experts_dev from expert_table_device."""
+    desc = MoeLayerDesc(D, I, E, K, n_shared, float(routed_scale), max(1, x.shape[0]))
+    _check(_lib.moe_layer_forward_static(ctypes.byref(desc), _ptr(Wr), _ptr(bias), _ptr(experts_dev), _ptr(x),
+                                         x.shape[0], _ptr(out), _stream(stream)))

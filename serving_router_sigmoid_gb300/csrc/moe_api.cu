@@ -4,6 +4,8 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <functional>
+#include <mutex>
 #include <new>
 
 #include "layer_args.cuh"
@@ -406,3 +408,90 @@ int moe_layer_set_probe(void *handle, int which, cudaEvent_t begin, cudaEvent_t 
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free forward.  The workspace of this entry point is a file-scope
+// device array instead of cudaMalloc'ed memory; every GPU that loads the
+// library holds it until the process exits.  Host code cannot pass the
+// array's name to a kernel (on the host it only stands for the symbol), so
+// its device address is looked up once per device with cudaGetSymbolAddress.
+namespace {
+
+constexpr size_t kStaticScratchBytes = (size_t)8 << 20;  // 8 MiB
+__device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+struct StaticDeviceState {
+    std::once_flag once;
+    cudaError_t status;
+    void *scratch;  // device address of g_static_scratch on this device
+    int num_sms;
+};
+StaticDeviceState g_static_dev[kMaxDevices];
+
+// Once per device, with that device current: resolve the scratch address and
+// the launch shapes.  No allocation happens here.
+void static_setup(StaticDeviceState *st, int dev) {
+    st->status = cudaGetSymbolAddress(&st->scratch, g_static_scratch);
+    if (st->status == cudaSuccess)
+        st->status = cudaDeviceGetAttribute(&st->num_sms, cudaDevAttrMultiProcessorCount, dev);
+}
+
+}  // namespace
+
+extern "C" int moe_layer_forward_static(const MoeLayerDesc *desc, const float *Wr, const float *bias,
+                                        const MoeExpertW *experts_dev, const float *x, int n_tokens, float *out,
+                                        cudaStream_t stream) {
+    int rc = check_desc(desc);
+    if (rc) return rc;
+    if (n_tokens < 0) return fail(MOE_ERR_SHAPE, "n_tokens=%d must be >= 0", n_tokens);
+    if (n_tokens == 0) return MOE_OK;
+    MoeLayerDesc d = *desc;
+    d.max_tokens = n_tokens;
+    const size_t need = layout(d, nullptr);
+    if (need > kStaticScratchBytes)
+        return fail(MOE_ERR_SHAPE,
+                    "n_tokens=%d needs %zu bytes of workspace; the static workspace holds %zu bytes "
+                    "(use moe_layer_create/moe_layer_forward for larger batches)",
+                    n_tokens, need, kStaticScratchBytes);
+    if (!Wr || !bias || !experts_dev || !x || !out) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned16(Wr) || !aligned16(x) || !aligned16(out) || !aligned16(experts_dev))
+        return fail(MOE_ERR_INVALID_ARG, "Wr, x, out and experts_dev must be 16-byte aligned");
+    if (x == out) return fail(MOE_ERR_INVALID_ARG, "out may not alias x");
+    int dev = -1;
+    cudaError_t ce = cudaGetDevice(&dev);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(MOE_ERR_INVALID_ARG, "device %d out of range", dev);
+    StaticDeviceState &st = g_static_dev[dev];
+    std::call_once(st.once, static_setup, &st, dev);
+    if (st.status != cudaSuccess) return cuda_fail(st.status, "static workspace set-up");
+
+    // a handle that lives on the stack and points into the static workspace
+    Handle h;
+    std::memset(&h, 0, sizeof h);
+    h.magic = kMagic;
+    h.device = dev;
+    h.d = d;
+    h.S = d.K + d.n_shared;
+    h.Wr = Wr;
+    h.bias = bias;
+    h.experts = reinterpret_cast<moe::DevExpert *>(const_cast<MoeExpertW *>(experts_dev));
+    h.ws = st.scratch;
+    h.ws_bytes = need;
+    layout(d, &h);
+    h.rpi_gu = kRpiGu;
+    h.nb_gu = (d.I + kRpiGu - 1) / kRpiGu;
+    h.rpi_dn = kRpiDn;
+    h.nb_dn = (d.D + kRpiDn - 1) / kRpiDn;
+    h.num_sms = st.num_sms;
+    h.stream_ok = moe::stream_supported(d.D, d.I);
+    if ((ce = moe::prepare_expert_kernels(d.D, d.I, st.num_sms, h.grid_gu, h.grid_dn)) != cudaSuccess)
+        return cuda_fail(ce, "kernel attributes");
+    // the arrival counters, routing tables and error word must start at zero;
+    // everything else is written before it is read
+    if ((ce = cudaMemsetAsync(h.meta, 0, sizeof(moe::RouteMeta), stream)) != cudaSuccess ||
+        (ce = cudaMemsetAsync(h.dn_cnt, 0, 4 * (size_t)((d.D + 15) / 16), stream)) != cudaSuccess ||
+        (ce = cudaMemsetAsync(h.err, 0, 4, stream)) != cudaSuccess)
+        return cuda_fail(ce, "static workspace clear");
+    return run_layer(&h, x, n_tokens, out, nullptr, moe::DebugPtrs{}, stream);
+}
