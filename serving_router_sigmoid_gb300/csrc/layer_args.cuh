@@ -24,6 +24,9 @@ struct LayerArgs {
     float *h;            // [Tmax * S, I] fp32 SwiGLU output, by grouped row
     uint32_t *hamax;     // [Tmax * S] bits of max|h| per grouped row
     float *part;         // [Tmax * S, D] expert outputs y by entry id
+    int8_t *hq;          // [Tmax * S, I] requantised h (even/odd layout), by grouped row
+    int32_t *hsum;       // [Tmax * S] code sums of hq rows
+    float *shq;          // [Tmax * S] scales of hq rows
     int32_t *dn_cnt;     // [nb_dn] arrival counters of the fused reduce
     float *out;          // [T, D]
     const float *resid;  // [T, D] or null: out = resid + MoE
@@ -52,6 +55,10 @@ cudaError_t launch_pack_int4(const float *w, uint8_t *q4, float *scale, int64_t 
 cudaError_t launch_gateup_stream(const LayerArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_down_stream(const LayerArgs &a, int grid, cudaStream_t s);
 bool stream_supported(int D, int I);
+cudaError_t launch_grouped_gateup(const LayerArgs &a, int num_sms, cudaStream_t s);
+cudaError_t launch_requant_h(const LayerArgs &a, cudaStream_t s);
+cudaError_t launch_grouped_down(const LayerArgs &a, int num_sms, cudaStream_t s);
+bool grouped_supported(int D, int I);
 // Occupancy-derived grid sizes and kernel attributes (call once per device).
 cudaError_t prepare_expert_kernels(int D, int I, int num_sms, int grid_gu[4], int grid_dn[4]);
 int mch_index(int mch);

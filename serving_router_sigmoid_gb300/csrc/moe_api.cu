@@ -51,6 +51,9 @@ struct Handle {
     float *h;
     uint32_t *hamax;
     float *part;
+    int8_t *hq;
+    int32_t *hsum;
+    float *shq;
     int32_t *dn_cnt;
     int32_t *err;
     float *xnorm;  // [Tmax, D] RMSNorm output of moe_block_forward
@@ -85,6 +88,9 @@ size_t layout(const MoeLayerDesc &d, Handle *h) {
     const size_t o_h = take(4 * T * S * I);
     const size_t o_hamax = take(4 * T * S);
     const size_t o_part = take(4 * T * S * D);
+    const size_t o_hq = take(T * S * I);
+    const size_t o_hsum = take(4 * T * S);
+    const size_t o_shq = take(4 * T * S);
     const size_t o_cnt = take(4 * nb_dn);
     const size_t o_err = take(4);
     const size_t o_xn = take(4 * T * D);
@@ -101,6 +107,9 @@ size_t layout(const MoeLayerDesc &d, Handle *h) {
         h->h = reinterpret_cast<float *>(b + o_h);
         h->hamax = reinterpret_cast<uint32_t *>(b + o_hamax);
         h->part = reinterpret_cast<float *>(b + o_part);
+        h->hq = reinterpret_cast<int8_t *>(b + o_hq);
+        h->hsum = reinterpret_cast<int32_t *>(b + o_hsum);
+        h->shq = reinterpret_cast<float *>(b + o_shq);
         h->dn_cnt = reinterpret_cast<int32_t *>(b + o_cnt);
         h->err = reinterpret_cast<int32_t *>(b + o_err);
         h->xnorm = reinterpret_cast<float *>(b + o_xn);
@@ -149,6 +158,7 @@ int run_layer(Handle *h, const float *x, int T, float *out, const float *resid, 
     a.x = x; a.Wr = h->Wr; a.bias = h->bias; a.experts = h->experts;
     a.xq = h->xq; a.sx = h->sx; a.xsum = h->xsum; a.logits = h->logits; a.idx = h->idx; a.wts = h->wts;
     a.rows = h->rows; a.meta = h->meta; a.h = h->h; a.hamax = h->hamax; a.part = h->part; a.dn_cnt = h->dn_cnt;
+    a.hq = h->hq; a.hsum = h->hsum; a.shq = h->shq;
     a.out = out; a.resid = resid; a.err = h->err;
     a.nb_gu = h->nb_gu; a.rpi_gu = h->rpi_gu; a.nb_dn = h->nb_dn; a.rpi_dn = h->rpi_dn;
     a.dbg = dbg;
@@ -171,9 +181,26 @@ int run_layer(Handle *h, const float *x, int T, float *out, const float *resid, 
     if (h->probe_which == MOE_PROBE_ROUTER && (ce = record(h->probe_end, s)) != cudaSuccess)
         return cuda_fail(ce, "probe record");
 
-    // decode-sized batches stream the experts through TMA-fed tensor-core
-    // tiles; larger batches (and shapes the tiles do not cover) use the
-    // row-per-warp dp4a kernels
+    // larger batches with tile-aligned shapes: tensor-core grouped GEMMs
+    if (!small && moe::grouped_supported(a.D, a.I)) {
+        if (h->probe_which == MOE_PROBE_GATE_UP && (ce = record(h->probe_begin, s)) != cudaSuccess)
+            return cuda_fail(ce, "probe record");
+        if ((ce = moe::launch_grouped_gateup(a, h->num_sms, s)) != cudaSuccess) return cuda_fail(ce, "gateup launch");
+        if (h->probe_which == MOE_PROBE_GATE_UP && (ce = record(h->probe_end, s)) != cudaSuccess)
+            return cuda_fail(ce, "probe record");
+        if (h->probe_which == MOE_PROBE_DOWN && (ce = record(h->probe_begin, s)) != cudaSuccess)
+            return cuda_fail(ce, "probe record");
+        if ((ce = moe::launch_requant_h(a, s)) != cudaSuccess) return cuda_fail(ce, "requant launch");
+        if ((ce = moe::launch_grouped_down(a, h->num_sms, s)) != cudaSuccess) return cuda_fail(ce, "down launch");
+        if ((ce = moe::launch_reduce(a, s)) != cudaSuccess) return cuda_fail(ce, "reduce launch");
+        if (h->probe_which == MOE_PROBE_DOWN && (ce = record(h->probe_end, s)) != cudaSuccess)
+            return cuda_fail(ce, "probe record");
+        return MOE_OK;
+    }
+
+    // decode-sized batches stream the experts through register-pipelined
+    // warps; shapes the grouped tiles do not cover use the row-per-warp dp4a
+    // kernels
     const bool stream = small && h->stream_ok;
     if (h->probe_which == MOE_PROBE_GATE_UP && (ce = record(h->probe_begin, s)) != cudaSuccess)
         return cuda_fail(ce, "probe record");
