@@ -15,8 +15,10 @@ that are not in L2 (1.2 GB of other weights pass between two uses of a set).
 `value` is tokens/s with inputs already in HBM, timed with CUDA events over
 exactly K steps (CUDA-graph replays), max over ranks.  `e2e` is the same
 metric through the C ABI with x copied in from pinned host memory and the
-output copied back every step.  `roofline` reports the dominant kernel
-(fused gate/up) against the measured HBM copy bandwidth.  `cpu_baseline` is
+output copied back every step.  `roofline` reports the dominant kernel: the
+fused gate/up weight stream against the measured HBM copy bandwidth at decode
+sizes, the gate/up grouped GEMM against the measured dense tensor rate at
+prefill sizes.  `cpu_baseline` is
 the plain CPU oracle timed on a bounded sample of the same workload.
 
 --impl reference times that oracle as the reference arm (rank 0 only).
@@ -48,7 +50,16 @@ WORKLOADS = {
     "glm_moe_stack8_decode_b8": ("glm_stack8_b8", True),
 }
 DEFAULT_WORKLOAD = "glm_moe_layer_decode_b1"
-HOT_KERNEL = "fused int4 gate/up + SiLU*up (gateup_kernel)"
+# Dominant kernel per path: decode batches (<= 16 tokens) stream the weights
+# (HBM-bound); larger batches run the grouped GEMM (tensor-pipe bound).
+HOT_KERNEL_DECODE = "stream_kernel<0> (fused int4 gate/up, SiLU*up, max abs h)"
+HOT_KERNEL_PREFILL = "grouped_gemm_kernel<0> (int4 x int8 gate/up GEMM, SiLU*up, max abs h)"
+# DRAM bytes (read + write) per launch of the dominant kernel from one ncu
+# capture of the current kernel source, or None.  Keyed by workload.
+TRAFFIC = {
+    # profiles/grouped_gemm_prefill_2048.md: 1.99 GB read + 0.14 GB written
+    "glm_moe_layer_prefill_2048": 2.131e9,
+}
 
 
 def parse_args():
@@ -160,14 +171,16 @@ class ClockSampler:
                 "samples_loaded": len(loaded)}
 
 
-def measured_peak():
+def measured_peak(kind="hbm_gbs"):
+    """A peak from MEASURED_PEAKS.json, else the profiling fallback."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    fallback = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
     try:
         with open(path) as f:
             j = json.load(f)
-        return float(j["hbm_gbs"]), "measured"
+        return float(j[kind]), "measured"
     except Exception:
-        return 6800.0, "fallback"
+        return fallback[kind], "fallback"
 
 
 # ------------------------------------------------------------ layer set-up
@@ -333,9 +346,31 @@ def run_ours(args, cfg, stack, rank, world, local):
     gu_bytes = u1_mean * gateup_bytes_per_expert(cfg) + T * cfg.D + T * cfg.S * cfg.I * 4
     step_bytes_layer = u1_mean * layer_bytes_per_expert(cfg) + cfg.E * cfg.D * 4 + cfg.E * 4 + 2 * T * cfg.D * 4
     step_bytes = step_bytes_layer * (len(layers) if stack else 1)
-    peak, peak_kind = measured_peak()
     probe_avg_ms = sum(probe_ms) / len(probe_ms)
-    achieved = gu_bytes / (probe_avg_ms / 1e3) / 1e9
+    grouped = T > 16
+    if args.probe != "gateup":
+        roof = {"bound": "hbm", "kernel": args.probe, "achieved": None, "peak": None, "unit": "GB/s",
+                "frac": None, "traffic": None, "avg_launch_ms": probe_avg_ms, "launches_timed": len(probe_ms)}
+    elif not grouped:
+        peak, peak_kind = measured_peak("hbm_gbs")
+        achieved = gu_bytes / (probe_avg_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": HOT_KERNEL_DECODE, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_kind": peak_kind + " HBM copy bandwidth",
+                "traffic": TRAFFIC.get(args.workload), "algorithmic_bytes_per_launch": gu_bytes,
+                "avg_launch_ms": probe_avg_ms, "launches_timed": len(probe_ms)}
+    else:
+        # int8 ops of the gate/up GEMM: every routed (token, expert) pair and
+        # every token through the shared expert, 2 ops per multiply-add
+        rows = T * cfg.K + T * cfg.n_shared
+        ops = 2.0 * rows * (2 * cfg.I) * cfg.D
+        peak, peak_kind = measured_peak("bf16_tflops_sustained")
+        achieved = ops / (probe_avg_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "kernel": HOT_KERNEL_PREFILL, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_kind": peak_kind + " dense bf16 (sustained); sm_103a has no int8 tcgen05 kind, so the "
+                             "densest tensor rate for these operands is the 16-bit one",
+                "traffic": TRAFFIC.get(args.workload), "algorithmic_ops_per_launch": ops,
+                "avg_launch_ms": probe_avg_ms, "launches_timed": len(probe_ms)}
 
     # end to end through the C ABI: pinned host x -> device, forward, out -> pinned host
     e2e = None
@@ -384,7 +419,8 @@ def run_ours(args, cfg, stack, rank, world, local):
         cpu = cpu_baseline(cfg, stack, args.cpu_seconds, dev)
 
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": w_done,
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "warmup_steps_run": w_done,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int4 weights x int8 activations -> int32, fp32 scales", "data": "synthetic",
         "config": {"workload": args.workload, "hidden": cfg.D, "moe_intermediate": cfg.I, "experts": cfg.E,
@@ -397,10 +433,7 @@ def run_ours(args, cfg, stack, rank, world, local):
                    if n_layers > 1 or T > 1 else "single set",
                    "parallelism": f"replicas x{world}"},
         "hbm_gbs_step": step_bytes / (ms_per_step / 1e3) / 1e9,
-        "roofline": {"bound": "hbm", "kernel": HOT_KERNEL if args.probe == "gateup" else args.probe, "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
-                     "algorithmic_bytes_per_launch": gu_bytes, "avg_launch_ms": probe_avg_ms,
-                     "launches_timed": len(probe_ms)},
+        "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,
