@@ -53,6 +53,7 @@ DEFAULT_WORKLOAD = "glm_moe_layer_decode_b1"
 # Dominant kernel per path: decode batches (<= 16 tokens) stream the weights
 # (HBM-bound); larger batches run the grouped GEMM (tensor-pipe bound).
 HOT_KERNEL_DECODE = "stream_kernel<0> (fused int4 gate/up, SiLU*up, max abs h)"
+HOT_KERNEL_SINGLE = "decode_layer_kernel (the whole layer as one persistent kernel)"
 HOT_KERNEL_PREFILL = "grouped_gemm_kernel<0> (int4 x int8 gate/up GEMM, SiLU*up, max abs h)"
 # DRAM bytes (read + write) per launch of the dominant kernel from one ncu
 # capture of the current kernel source, or None.  Keyed by workload.
@@ -77,6 +78,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU oracle sample budget")
     p.add_argument("--ref-seconds", type=float, default=150.0, help="reference arm time box")
+    p.add_argument("--four-kernel", action="store_true",
+                   help="decode batches: run the four-kernel launch plan instead of the single persistent kernel")
     p.add_argument("--probe", choices=["gateup", "down", "router"], default="gateup",
                    help="kernel timed live by the roofline probe (the roofline figure is the gate/up kernel's)")
     return p.parse_args()
@@ -240,6 +243,11 @@ def run_ours(args, cfg, stack, rank, world, local):
     t_setup = time.time()
     layers, keep = build_layers(cfg, n_layers, args.light, dev, rank_seed=rank)
     T = cfg.T
+    for lyr in layers:
+        if args.four_kernel:
+            lyr.set_option(moe.MOE_OPT_DECODE_SINGLE_KERNEL, 0)
+    single = (T <= 16 and not args.four_kernel
+              and layers[0].get_option(moe.MOE_OPT_DECODE_SINGLE_KERNEL_AVAILABLE) == 1)
     s = torch.cuda.Stream(device=dev)
     norm_w = synth.norm_weight(cfg, dev)
     # inputs: one token batch per layer set (single layer), or a pool of batches (stack)
@@ -290,7 +298,7 @@ def run_ours(args, cfg, stack, rank, world, local):
         else:
             step_fn(i)
 
-    kernels_per_forward = (3 if T <= 16 else 6) + (1 if stack else 0)
+    kernels_per_forward = (1 if single else 4 if T <= 16 else 7) + (1 if stack else 0)
     launches_per_step = kernels_per_forward * (len(layers) if stack else 1)
     setup_s = time.time() - t_setup
 
@@ -348,7 +356,15 @@ def run_ours(args, cfg, stack, rank, world, local):
     step_bytes = step_bytes_layer * (len(layers) if stack else 1)
     probe_avg_ms = sum(probe_ms) / len(probe_ms)
     grouped = T > 16
-    if args.probe != "gateup":
+    if single:
+        # one kernel is the whole layer: its algorithmic bytes are the step's
+        peak, peak_kind = measured_peak("hbm_gbs")
+        achieved = step_bytes_layer / (probe_avg_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": HOT_KERNEL_SINGLE, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_kind": peak_kind + " HBM copy bandwidth",
+                "traffic": TRAFFIC.get(args.workload), "algorithmic_bytes_per_launch": step_bytes_layer,
+                "avg_launch_ms": probe_avg_ms, "launches_timed": len(probe_ms)}
+    elif args.probe != "gateup":
         roof = {"bound": "hbm", "kernel": args.probe, "achieved": None, "peak": None, "unit": "GB/s",
                 "frac": None, "traffic": None, "avg_launch_ms": probe_avg_ms, "launches_timed": len(probe_ms)}
     elif not grouped:
@@ -428,6 +444,7 @@ def run_ours(args, cfg, stack, rank, world, local):
                    "layers_per_step": len(layers) if stack else 1, "layer_sets_cycled": n_layers,
                    "routed_scale": cfg.routed_scale, "zipf_skew": cfg.skew,
                    "experts_streamed_per_layer": u1_mean, "cuda_graph": use_graph, "light": args.light,
+                   "decode_plan": ("single persistent kernel" if single else "four kernels") if T <= 16 else None,
                    "l2": ("inputs larger than L2: the steps cycle %d resident layer weight sets "
                           "(%.2f GB between reuses of a set)" % (n_layers, (n_layers - 1) * step_bytes_layer / 1e9))
                    if n_layers > 1 or T > 1 else "single set",

@@ -193,7 +193,8 @@ int moe_layer_debug(void *handle, const float *x, int n_tokens, float *out,
 /*
  * Synchronise `stream`, then read and clear the handle's device error word
  * (set by a kernel that met an input outside the contract, e.g. a token with
- * no finite selection score).  *status_out (host) receives 0 or the flag bits.
+ * no finite selection score, or a wait of the persistent decode kernel that
+ * ran out of time, bit 16; the handle's arrival counters are then cleared).  *status_out (host) receives 0 or the flag bits.
  * Returns MOE_OK, or MOE_ERR_DEVICE when a flag was set.
  */
 int moe_layer_device_status(void *handle, cudaStream_t stream, int *status_out);
@@ -207,10 +208,43 @@ int moe_layer_device_status(void *handle, cudaStream_t stream, int *status_out);
 /*
  * Timing probe: while set, every forward records `begin` on its stream just
  * before the kernel `which` and `end` just after it (as external event-record
- * nodes under stream capture).  which = MOE_PROBE_NONE clears it.  The events
- * are owned by the caller.  Errors: INVALID_ARG.
+ * nodes under stream capture).  which = MOE_PROBE_NONE clears it.  When a
+ * decode-sized batch runs as the single persistent kernel (see
+ * MOE_OPT_DECODE_SINGLE_KERNEL) every probe id brackets that kernel.  The
+ * events are owned by the caller.  Errors: INVALID_ARG.
  */
 int moe_layer_set_probe(void *handle, int which, cudaEvent_t begin, cudaEvent_t end);
+
+/* Options of a handle (moe_layer_set_option / moe_layer_get_option). */
+/* 1 (default): batches of 1..16 tokens run the whole layer as one persistent
+ * kernel (cooperative launch, every CTA resident; its phases hand over through
+ * arrival counters with bounded waits); 0: as a sequence of four kernels
+ * (router + quantiser + union, gate/up, down, ordered reduce).  Both give
+ * bit-identical outputs.  The single kernel needs cooperative launch support,
+ * I <= 2048 and D <= 8192; otherwise the four-kernel sequence runs. */
+#define MOE_OPT_DECODE_SINGLE_KERNEL 1
+/* read-only: 1 when the single-kernel path can run for this handle */
+#define MOE_OPT_DECODE_SINGLE_KERNEL_AVAILABLE 2
+
+/*
+ * Set / read a handle option (host).  Not part of the pages' interface: these
+ * select between two equivalent launch plans of the same computation.
+ * Errors: INVALID_ARG (bad handle, unknown option, value out of range).
+ */
+int moe_layer_set_option(void *handle, int option, int value);
+int moe_layer_get_option(void *handle, int option, int *value_out);
+
+/*
+ * Phase trace of the persistent decode kernel (a tracing aid; the pages have
+ * no counterpart).  While set, every launch of that kernel writes, for CTA b,
+ * 10 %globaltimer stamps (ns) to stamps_dev[10*b .. 10*b+9] as long as
+ * 10*(b+1) <= n_stamps: kernel start, router/quantiser roles done, quantised
+ * tokens in, shared expert gate/up done, all logits in, top-K + union done,
+ * routed gate/up done, gate/up barrier passed, down rows done, end.
+ * stamps_dev: device, 8-byte aligned, owned by the caller; NULL / 0 clears.
+ * Errors: INVALID_ARG.
+ */
+int moe_layer_set_trace(void *handle, uint64_t *stamps_dev, int n_stamps);
 
 /* Bytes of device workspace a handle with this description owns (host). */
 int moe_layer_workspace_bytes(const MoeLayerDesc *desc, size_t *bytes_out);

@@ -23,6 +23,7 @@ MOE_ERR_CUDA = -3
 MOE_ERR_NOMEM = -4
 MOE_ERR_DEVICE = -5
 MOE_PROBE_NONE, MOE_PROBE_GATE_UP, MOE_PROBE_DOWN, MOE_PROBE_ROUTER = 0, 1, 2, 3
+MOE_OPT_DECODE_SINGLE_KERNEL, MOE_OPT_DECODE_SINGLE_KERNEL_AVAILABLE = 1, 2
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it with "
@@ -61,6 +62,9 @@ _SIGS = {
     "moe_layer_debug": ([_vp, _vp, _ci, _vp, ctypes.POINTER(MoeDebugOut), _vp], _ci),
     "moe_layer_device_status": ([_vp, _vp, ctypes.POINTER(_ci)], _ci),
     "moe_layer_set_probe": ([_vp, _ci, _vp, _vp], _ci),
+    "moe_layer_set_option": ([_vp, _ci, _ci], _ci),
+    "moe_layer_set_trace": ([_vp, _vp, _ci], _ci),
+    "moe_layer_get_option": ([_vp, _ci, ctypes.POINTER(_ci)], _ci),
     "moe_layer_workspace_bytes": ([ctypes.POINTER(MoeLayerDesc), ctypes.POINTER(ctypes.c_size_t)], _ci),
     "moe_layer_forward_static": ([ctypes.POINTER(MoeLayerDesc), _vp, _vp, _vp, _vp, _ci, _vp, _vp], _ci),
 }
@@ -205,6 +209,25 @@ class MoeLayer:
         if rc not in (MOE_OK, MOE_ERR_DEVICE):
             _check(rc)
         return int(v.value)
+
+    def set_option(self, option, value):
+        _check(_lib.moe_layer_set_option(self.handle, int(option), int(value)))
+
+    def get_option(self, option) -> int:
+        v = ctypes.c_int(0)
+        _check(_lib.moe_layer_get_option(self.handle, int(option), ctypes.byref(v)))
+        return int(v.value)
+
+    def set_trace(self, stamps=None):
+        """stamps: int64 CUDA tensor (10 per CTA) for the decode kernel's phase
+        stamps, or None to stop tracing."""
+        if stamps is None:
+            _check(_lib.moe_layer_set_trace(self.handle, None, 0))
+        else:
+            if stamps.dtype != torch.int64 or not stamps.is_cuda or not stamps.is_contiguous():
+                raise ValueError("stamps must be a contiguous int64 CUDA tensor")
+            _check(_lib.moe_layer_set_trace(self.handle, ctypes.c_void_p(stamps.data_ptr()), stamps.numel()))
+        self._trace = stamps
 
     def set_probe(self, which, begin=None, end=None):
         for ev in (begin, end):  # torch creates the CUDA event at its first record

@@ -17,6 +17,8 @@ constexpr int kMaxDim = 8192;     // D and I upper bound (GEMV chunks per lane <
 // Device error word bits (moe_layer_device_status).
 constexpr int kErrNoSelection = 1;   // a token had no finite selection score left
 constexpr int kErrRouteCount = 2;    // routing table inconsistent
+constexpr int kErrTooManyRows = 8;   // an expert had more rows than the streaming tile
+constexpr int kErrSyncTimeout = 16;  // a wait of the persistent decode kernel ran out of time
 
 struct DevExpert {
     const uint8_t *gq, *uq, *dq;
@@ -35,6 +37,24 @@ struct RouteMeta {
     int ubeg[kMaxE + 2];
 };
 
+// Arrival counters of the persistent decode kernel (zero between launches:
+// the last CTA of each launch clears them).
+constexpr int kRedRows = 64;                    // output rows per reduce block
+constexpr int kMaxRedBlk = kMaxDim / kRedRows;  // reduce blocks of the largest D
+struct FusedSync {
+    int quant_cnt;         // quantiser CTAs finished
+    int gu_cnt;            // CTAs finished with gate/up
+    int done_cnt;          // CTAs finished with everything
+    int blk[kMaxRedBlk];   // down rows written per reduce block
+};
+
+// Phase time stamps of the persistent decode kernel (moe_layer_set_trace):
+// per CTA, %globaltimer at kernel start, after the router/quantiser roles,
+// after the quantiser wait, after the shared expert's gate/up, after the
+// router wait, after top-K + union, after the routed gate/up, after the
+// gate/up barrier, after the down rows, at the end.
+constexpr int kTraceStamps = 10;
+
 struct DebugPtrs {
     int8_t *xq;
     int32_t *gate_acc, *up_acc;
@@ -44,6 +64,43 @@ struct DebugPtrs {
 };
 
 // ------------------------------------------------------------------ helpers
+
+// Sentinels of the decode kernel's data-as-flag hand-overs: a logit slot or a
+// packed selection that has not been written yet.  0xFFFFFFFF is a NaN that
+// arithmetic never produces (it yields the canonical 0x7FFFFFFF).
+constexpr uint32_t kLogitEmpty = 0xFFFFFFFFu;
+constexpr unsigned long long kSelEmpty = 0xFFFFFFFFFFFFFFFFull;
+constexpr unsigned long long kWaitNs = 1000000000ull;  // bound of every wait: 1 s
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ int ld_acquire(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Coherent (L2) loads and stores for values other CTAs of the same grid poll.
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const void *p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const void *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed_u32(void *p, uint32_t v) {
+    asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed_u64(void *p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 
 __device__ __forceinline__ float warp_sum_f(float v) {
 #pragma unroll
@@ -124,6 +181,15 @@ __device__ __forceinline__ int dot_word(uint32_t w, int xe, int xo, int acc) {
     acc = __dp4a(lo, xe, acc);
     acc = __dp4a(hi, xo, acc);
     return acc;
+}
+
+// Shared-memory activations: row m holds the even/odd int8 row split in two
+// planes, plane A = the first 16 bytes of every 32-byte chunk (activation
+// groups 4c, 4c+1), plane B = the last 16 (groups 4c+2, 4c+3), so that the
+// 16-byte reads of a warp are contiguous (no bank conflicts).
+__device__ __forceinline__ int8_t *plane_byte(int8_t *xs, int kdim, int m, int byte) {
+    const int ch = byte >> 5, in = byte & 31;
+    return xs + (size_t)m * kdim + (in >= 16 ? (kdim >> 1) : 0) + ch * 16 + (in & 15);
 }
 
 __device__ __forceinline__ float silu_f(float g) { return __fdiv_rn(g, __fadd_rn(1.f, expf(-g))); }

@@ -1,0 +1,611 @@
+// decode_dev.cuh -- the routed-MoE layer for decode-sized batches (1 to 16
+// tokens) as one persistent kernel: activation quantiser, sigmoid+bias top-K
+// router, expert union, fused gate/up, down and the ordered weighted sum.
+//
+// Sources: reader.mx "惊呆了！25GB 内存上运行 GLM 5.2 744B 模型" §11 (router:
+// sigmoid(logit)+bias picks top-K, weight = plain sigmoid * routed_scale;
+// the batch union so each expert's weights are read once; SwiGLU expert
+// h = siluf(gate)*up, down, weighted add, shared expert added) and §12 (int8
+// per-row activations x int4 weights with an exact integer dot, then the
+// activation and row scales); besthub.dev "Running 744B MoE on 25GB RAM"
+// §11, §12.
+//
+// Design (GB300).  At decode sizes the layer reads ~19 MB per union expert
+// and does almost no arithmetic: it is one long weight stream, and every
+// kernel boundary costs a ramp-up and a tail of several microseconds.  So the
+// whole layer is one cooperative launch with every CTA resident (2 per SM),
+// moving through three phases that hand data over through L2:
+//   1. CTA b < E computes the logits of experts b, b + G, ... (its router
+//      row is requested first: everything downstream waits on the logits);
+//      the last T CTAs quantise one token each.  Every CTA then requests the
+//      first rows of its slice of the shared expert's gate/up, which needs
+//      no routing, and streams that slice as soon as the quantised tokens
+//      are in (arrival counter).  Meanwhile the quantiser CTA of each token,
+//      once all logits have landed (arrival counter), selects that token's
+//      top-K and publishes it (arrival counter).
+//   2. Every CTA reads the published selections and builds the union tables
+//      itself, in shared memory; then it streams its contiguous slice of the
+//      routed experts' gate/up rows (h and max|h| to L2).
+//   3. A grid-wide arrival barrier; each CTA requests its first down rows
+//      before waiting.  The CTA requantises the h rows of the experts in its
+//      slice and streams their down rows into per-slot partial outputs.  An
+//      arrival counter per block of 64 output rows sums the rows written; the
+//      CTA that completes a block adds that block's slots in the fixed slot
+//      order (shared expert last), so the result does not depend on which
+//      CTA arrives when.
+// Every wait is bounded (one second of %globaltimer): on time-out the kernel
+// sets kErrSyncTimeout in the error word and runs on to its end, so nothing
+// hangs and the stream stays usable.  The last CTA to finish clears the
+// counters for the next launch.
+#pragma once
+
+#include "route_dev.cuh"
+#include "stream_dev.cuh"
+
+namespace moe {
+namespace dec {
+
+constexpr int kMaxContrib = 128;                       // reduce-block arrivals listed per CTA
+
+// Thread 0 records phase stamp k of this CTA when tracing is on.
+__device__ __forceinline__ void stamp(const LayerArgs &a, int k) {
+    if (a.trace && threadIdx.x == 0 && (long long)(blockIdx.x + 1) * kTraceStamps <= a.trace_n)
+        a.trace[(size_t)blockIdx.x * kTraceStamps + k] = global_ns();
+}
+
+// All threads: the CTA's global writes so far become visible device-wide,
+// then *cnt += 1.
+__device__ __forceinline__ void cta_arrive(int *cnt) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(cnt, 1);
+    }
+}
+
+// All threads: wait (bounded) until *cnt >= target; afterwards everything the
+// arriving CTAs wrote before arriving is visible to every thread of the CTA.
+__device__ __forceinline__ void cta_wait(const int *cnt, int target, int32_t *err) {
+    if (threadIdx.x == 0) {
+        if (ld_acquire(cnt) < target) {
+            const unsigned long long t0 = global_ns();
+            while (ld_acquire(cnt) < target) {
+                if (global_ns() - t0 > kWaitNs) {
+                    atomicOr(err, kErrSyncTimeout);
+                    break;
+                }
+                __nanosleep(32);
+            }
+        }
+        __threadfence();
+    }
+    __syncthreads();
+}
+
+// Shared-memory state of one CTA (besides the activation tile).
+struct DecodeSmem {
+    int ent[kSmallT];                 // entry ids (t*S + slot) of the staged expert's rows
+    int xsum[kSmallT];                // code sums of those activation rows
+    float sx[kSmallT];                // their scales
+    int hpart[8][kSmallT];            // per-warp partial code sums of requantised h rows
+    float red[8][kSmallT];            // per-warp partial logits
+    int idx[kSmallT * kMaxK];         // top-K selections, (token, slot) order
+    float w[kSmallT * kMaxK];         // their routing weights
+    int first[kSmallT * kMaxK];       // selection is its expert's first
+    int rows[kSmallT * (kMaxK + 1)];  // entry ids grouped by union entry
+    int uexp[kSmallT * kMaxK + 1];    // union entry -> expert (shared expert = E, last)
+    int ubeg[kSmallT * kMaxK + 2];    // union entry -> first grouped row
+    int sh_uexp[1];                   // one-entry view of the shared expert
+    int sh_ubeg[2];
+    int nu;                           // routed union entries
+    int nblk;                         // reduce blocks this CTA completed
+    int last;                         // this CTA finished last
+    int blk_list[kMaxRedBlk];          // reduce blocks this CTA completed
+    int ncontrib;                      // (block, rows) contributions listed
+    int2 contrib[kMaxContrib];
+    unsigned long long tk[4][8][kMaxK];  // top-K candidates (topk_small_cta)
+    float tkp[4][8][kMaxK];              // their sigmoids
+};
+
+template <int KIND>
+__device__ __forceinline__ int units_of_warp(int p0, int p1, int warp) {
+    constexpr int UPG = KIND == kGateUp ? 2 : 1;
+    return p1 - p0 > warp ? ((p1 - p0 - warp + 7) / 8) * UPG : 0;
+}
+
+// Requests unit j of this warp (group p0 + warp + 8*(j / UPG) of the union
+// view, matrix j % UPG) into R.  ex_u/ex cache the current expert's pointers.
+template <int KIND, int CPL>
+__device__ __forceinline__ void request(UnitRegs<KIND, CPL> &R, const LayerArgs &a, const int *uexp, int gpe,
+                                        int p0, int n_my, int j, int &ex_u, DevExpert &ex) {
+    constexpr int UPG = KIND == kGateUp ? 2 : 1, RPG = UnitShape<KIND, CPL>::kRows;
+    if (j >= n_my) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kdim = KIND == kGateUp ? a.D : a.I;
+    const int rowb = kdim >> 1, nch = rowb >> 4;
+    const int p = p0 + warp + 8 * (j / UPG), u = p / gpe;
+    if (u != ex_u) {
+        ex_u = u;
+        ex = a.experts[uexp[u]];
+    }
+    const int o = (p - u * gpe) * RPG;
+    const uint8_t *mat;
+    const float *sc;
+    if (KIND == kGateUp) {
+        mat = (j % UPG == 0) ? ex.gq : ex.uq;
+        sc = (j % UPG == 0) ? ex.gs : ex.us;
+    } else {
+        mat = ex.dq;
+        sc = ex.ds;
+    }
+    load_unit<KIND, CPL>(R, mat, sc, o, rowb, nch, lane);
+}
+
+// Requests the first two units of the warp's share of groups [p0, p1).
+template <int KIND, int CPL>
+__device__ __forceinline__ void prime(UnitRegs<KIND, CPL> &A, UnitRegs<KIND, CPL> &B, const LayerArgs &a,
+                                      const int *uexp, int gpe, int p0, int p1, int &ex_u, DevExpert &ex) {
+    const int n_my = units_of_warp<KIND>(p0, p1, threadIdx.x >> 5);
+    ex_u = -1;
+    request<KIND, CPL>(A, a, uexp, gpe, p0, n_my, 0, ex_u, ex);
+    request<KIND, CPL>(B, a, uexp, gpe, p0, n_my, 1, ex_u, ex);
+}
+
+// Streams row groups [p0, p1) of a union view (gate/up: a gate row with the
+// same up row; down: two rows) through the CTA's eight warps; A and B hold
+// the warp's first two units (prime).  Per union entry the CTA stages the
+// activations (gate/up: the quantised tokens; down: h requantised from L2)
+// in the two-plane layout, then each warp multiplies its units while the
+// next one is in flight.  Must be called by all threads with the same range.
+template <int KIND, int CPL, int MCH>
+__device__ __forceinline__ void stream_phase(const LayerArgs &a, DecodeSmem &sm, int8_t *xs, const int *uexp,
+                                             const int *ubeg, int p0, int p1, UnitRegs<KIND, CPL> &A,
+                                             UnitRegs<KIND, CPL> &B, int &ex_u, DevExpert &ex) {
+    constexpr int UPG = KIND == kGateUp ? 2 : 1, RPG = UnitShape<KIND, CPL>::kRows;
+    // at one token every gate/up entry multiplies the same row (token 0),
+    // staged once in xs / sm.sx[0] / sm.xsum[0] by the caller
+    constexpr bool kFixedX = KIND == kGateUp && MCH == 1;
+    if (p0 >= p1) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = a.S;
+    const int kdim = KIND == kGateUp ? a.D : a.I;
+    const int rows_out = KIND == kGateUp ? a.I : a.D;
+    const int nch = (kdim >> 1) >> 4;
+    const int gpe = rows_out / RPG;
+    const int n_my = units_of_warp<KIND>(p0, p1, warp);
+
+    float amax_run = 0.f;  // lane m: max|h| of token row m of the staged entry (gate/up)
+    int hsum = 0;          // lane m: code sum of the requantised h row m (down)
+    int held_g = 0;        // lane m: gate sum waiting for its up row
+    float held_gs = 0.f;   // that gate row's scale
+    int r0 = 0, M = 0, j = 0;
+    bool flip = false;     // the next unit is in B
+    const int ua = p0 / gpe, ub = (p1 - 1) / gpe;
+    for (int ue = ua; ue <= ub; ++ue) {
+        if (KIND == kGateUp && ue > ua && lane < M) atomicMax(a.dham + r0 + lane, __float_as_uint(amax_run));
+        __syncthreads();
+        r0 = ubeg[ue];
+        M = ubeg[ue + 1] - r0;
+        if (M > MCH) {
+            if (threadIdx.x == 0) atomicOr(a.err, kErrTooManyRows);
+            M = MCH;
+        }
+        if (threadIdx.x < M) sm.ent[threadIdx.x] = sm.rows[r0 + threadIdx.x];
+        __syncthreads();
+        if (kFixedX) {
+            // one token: the tile, its scale and code sum were staged once
+        } else if (KIND == kGateUp) {
+            if (threadIdx.x < M) {
+                const int t = sm.ent[threadIdx.x] / S;
+                sm.xsum[threadIdx.x] = __ldcg(a.xsum + t);
+                sm.sx[threadIdx.x] = __ldcg(a.sx + t);
+            }
+            const int n16 = kdim >> 4;
+            for (int i = threadIdx.x; i < M * n16; i += blockDim.x) {
+                const int m = i / n16, c = i - m * n16;
+                *reinterpret_cast<int4 *>(plane_byte(xs, kdim, m, 16 * c)) =
+                    __ldcg(reinterpret_cast<const int4 *>(a.xq + (size_t)(sm.ent[m] / S) * kdim) + c);
+            }
+        } else {
+            const int n8 = kdim >> 3;
+            const bool first_block = p0 <= ue * gpe;  // this CTA owns the entry's first rows
+            for (int m = 0; m < M; ++m) {
+                float s, inv;
+                act_scale(__uint_as_float(__ldcg(a.dham + r0 + m)), s, inv);
+                if (threadIdx.x == 0) sm.sx[m] = s;
+                int sum = 0;
+                for (int gi = threadIdx.x; gi < n8; gi += blockDim.x) {
+                    const float *hp = a.h + (size_t)(r0 + m) * kdim + 8 * gi;
+                    const float4 v0 = ld_cg_f4(hp), v1 = ld_cg_f4(hp + 4);
+                    const int q0 = quant_i8(v0.x, inv), q1 = quant_i8(v0.y, inv), q2 = quant_i8(v0.z, inv),
+                              q3 = quant_i8(v0.w, inv), q4 = quant_i8(v1.x, inv), q5 = quant_i8(v1.y, inv),
+                              q6 = quant_i8(v1.z, inv), q7 = quant_i8(v1.w, inv);
+                    sum += q0 + q1 + q2 + q3 + q4 + q5 + q6 + q7;
+                    const uint32_t ev = (q0 & 255) | ((q2 & 255) << 8) | ((q4 & 255) << 16) | ((uint32_t)(q6 & 255) << 24);
+                    const uint32_t od = (q1 & 255) | ((q3 & 255) << 8) | ((q5 & 255) << 16) | ((uint32_t)(q7 & 255) << 24);
+                    *reinterpret_cast<uint2 *>(plane_byte(xs, kdim, m, 8 * gi)) = make_uint2(ev, od);
+                    if (a.dbg.hq && first_block) {
+                        const uint32_t n0 = (q0 & 255) | ((q1 & 255) << 8) | ((q2 & 255) << 16) | ((uint32_t)(q3 & 255) << 24);
+                        const uint32_t n1 = (q4 & 255) | ((q5 & 255) << 8) | ((q6 & 255) << 16) | ((uint32_t)(q7 & 255) << 24);
+                        *reinterpret_cast<uint2 *>(a.dbg.hq + (size_t)sm.ent[m] * kdim + 8 * gi) = make_uint2(n0, n1);
+                    }
+                }
+                sum = warp_sum_i(sum);
+                if (lane == 0) sm.hpart[warp][m] = sum;
+            }
+            if (a.dbg.sh && first_block && threadIdx.x < M) a.dbg.sh[sm.ent[threadIdx.x]] = sm.sx[threadIdx.x];
+        }
+        __syncthreads();
+        if (KIND == kDown) {
+            hsum = 0;
+            if (lane < M)
+#pragma unroll
+                for (int w = 0; w < 8; ++w) hsum += sm.hpart[w][lane];
+        }
+        amax_run = 0.f;
+
+        const int g_end = min(p1, (ue + 1) * gpe);  // groups of entry ue end here
+        auto in_seg = [&](int jj) { return jj < n_my && p0 + warp + 8 * (jj / UPG) < g_end; };
+        auto process = [&](const UnitRegs<KIND, CPL> &R, int jj) {
+            const int p = p0 + warp + 8 * (jj / UPG);
+            const int o0 = (p - ue * gpe) * RPG;
+            if (KIND == kGateUp) {
+                int acc[MCH];
+#pragma unroll
+                for (int m = 0; m < MCH; ++m) acc[m] = 0;
+                dot_rows<CPL, MCH>(acc, R.w[0], xs, kdim, M, nch, lane);
+                const int mine = lane_sum<MCH>(acc, M, lane);
+                if (jj % UPG == 0) {
+                    held_g = mine;
+                    held_gs = R.s[0];
+                } else if (lane < M) {
+                    const int gi = held_g - 8 * sm.xsum[lane], ui = mine - 8 * sm.xsum[lane];
+                    const float gf = __fmul_rn(__fmul_rn((float)gi, sm.sx[lane]), held_gs);
+                    const float uf = __fmul_rn(__fmul_rn((float)ui, sm.sx[lane]), R.s[0]);
+                    const float hv = __fmul_rn(silu_f(gf), uf);
+                    a.h[(size_t)(r0 + lane) * a.I + o0] = hv;
+                    amax_run = fmaxf(amax_run, fabsf(hv));
+                    if (a.dbg.gate_acc) a.dbg.gate_acc[(size_t)sm.ent[lane] * a.I + o0] = gi;
+                    if (a.dbg.up_acc) a.dbg.up_acc[(size_t)sm.ent[lane] * a.I + o0] = ui;
+                }
+            } else {
+#pragma unroll
+                for (int rr = 0; rr < RPG; ++rr) {
+                    int acc[MCH];
+#pragma unroll
+                    for (int m = 0; m < MCH; ++m) acc[m] = 0;
+                    dot_rows<CPL, MCH>(acc, R.w[rr], xs, kdim, M, nch, lane);
+                    const int mine = lane_sum<MCH>(acc, M, lane);
+                    if (lane < M) {
+                        const int o = o0 + rr;
+                        const int di = mine - 8 * hsum;
+                        const float y = __fmul_rn(__fmul_rn((float)di, sm.sx[lane]), R.s[rr]);
+                        a.part[(size_t)sm.ent[lane] * a.D + o] = y;
+                        if (a.dbg.down_acc) a.dbg.down_acc[(size_t)sm.ent[lane] * a.D + o] = di;
+                    }
+                }
+            }
+        };
+        // X holds unit j, Y unit j + 1; each processed set is refilled with
+        // the unit two ahead.  Returns true when the next unit is in Y.
+        auto run = [&](UnitRegs<KIND, CPL> &X, UnitRegs<KIND, CPL> &Y) -> bool {
+            while (in_seg(j)) {
+                process(X, j);
+                request<KIND, CPL>(X, a, uexp, gpe, p0, n_my, j + 2, ex_u, ex);
+                ++j;
+                if (!in_seg(j)) return true;
+                process(Y, j);
+                request<KIND, CPL>(Y, a, uexp, gpe, p0, n_my, j + 2, ex_u, ex);
+                ++j;
+            }
+            return false;
+        };
+        flip = flip ? !run(B, A) : run(A, B);
+    }
+    if (KIND == kGateUp && lane < M) atomicMax(a.dham + r0 + lane, __float_as_uint(amax_run));
+}
+
+// The union tables of the batch from its T*K selections in sm.idx ((token,
+// slot) order), built in shared memory by the whole CTA (T*K <= blockDim).
+// Thread i ranks selection i by (expert, i): that rank is its row in the
+// expert-grouped order (rows of one expert keep (token, slot) order).  The
+// first selection of each expert also ranks its expert among the distinct
+// ones: the union is in ascending expert id, the shared expert last.
+__device__ __forceinline__ void build_union(DecodeSmem &sm, int T, int K, int S, int E, int n_shared) {
+    const int n = T * K, tid = threadIdx.x;
+    int e = -1, less = 0;
+    bool first = true;
+    if (tid == 0) sm.nu = 0;
+    if (tid < n) {
+        e = sm.idx[tid];
+        for (int j = 0; j < n; ++j) {
+            const int ej = sm.idx[j];
+            less += ej < e;
+            if (ej == e && j < tid) {
+                ++less;
+                first = false;
+            }
+        }
+        sm.rows[less] = (tid / K) * S + (tid % K);
+        sm.first[tid] = first;
+    }
+    __syncthreads();
+    if (tid < n && first) {
+        int upos = 0;
+        for (int j = 0; j < n; ++j) upos += sm.first[j] && sm.idx[j] < e;
+        sm.uexp[upos] = e;
+        sm.ubeg[upos] = less;
+        atomicAdd(&sm.nu, 1);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        const int nr = sm.nu;
+        sm.ubeg[nr] = n;
+        if (n_shared) {
+            sm.uexp[nr] = E;
+            sm.ubeg[nr + 1] = n + T;
+        }
+    }
+    __syncthreads();
+}
+
+template <int CPLG, int CPLD, int MCH>
+__global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
+    extern __shared__ __align__(16) int8_t xs[];  // [MCH][max(D, I)] activation tile
+    __shared__ DecodeSmem sm;
+    const int tid = threadIdx.x;
+    const int b = blockIdx.x, G = gridDim.x;
+    const int T = a.T, D = a.D, I = a.I, E = a.E, K = a.K, S = a.S, n_sel = T * K;
+    FusedSync *sy = a.sync;
+
+    // one-entry view of the shared expert: grouped rows [n_sel, n_sel + T)
+    if (tid < T) sm.rows[n_sel + tid] = tid * S + K;
+    if (tid == 0) {
+        sm.sh_uexp[0] = E;
+        sm.sh_ubeg[0] = n_sel;
+        sm.sh_ubeg[1] = n_sel + T;
+    }
+    __syncthreads();
+    stamp(a, 0);
+
+    // ---- phase 1.  The router rows go first (everything downstream waits on
+    // the logits), then the first rows of the shared expert, which need no
+    // routing.
+    WrRegs<CPLG, MCH == 1> wr;  // D <= 1024 * CPLG
+    if (b < E) logits_request(wr, a.Wr + (size_t)b * D, a.x, D);
+    int ex_u = -1;
+    DevExpert ex{};
+    UnitRegs<kGateUp, CPLG> A, B;
+    const int sp0 = a.n_shared ? (int)((long long)b * I / G) : 0;
+    const int sp1 = a.n_shared ? (int)((long long)(b + 1) * I / G) : 0;
+    prime<kGateUp, CPLG>(A, B, a, sm.sh_uexp, I, sp0, sp1, ex_u, ex);
+
+    // router logits of experts b, b + G, ... (the arithmetic of the
+    // four-kernel router), published as data: the slot itself is the flag
+    if (b < E) {
+        for (int e = b; e < E; e += G) {
+            if (e != b) logits_request(wr, a.Wr + (size_t)e * D, a.x, D);
+            const float l = logits_finish(wr, a.x, T, D, sm.red);
+            if (tid < T) {
+                const uint32_t bits = __float_as_uint(l);
+                st_relaxed_u32(a.dlog + tid * E + e, bits == kLogitEmpty ? 0x7FFFFFFFu : bits);
+            }
+        }
+    }
+    stamp(a, 1);
+
+    // quantiser: the last T CTAs, one token each (the global rows are the
+    // tokens of the staged tiles for T > 1, and the debug outputs).  At one
+    // token every CTA also quantises token 0 into its own tile.
+    const int tq = G - 1 - b;
+    if (MCH == 1) {
+        quant_token_perm(a.x, D, tq == 0 ? a.xq : nullptr, tq == 0 ? a.sx : nullptr, tq == 0 ? a.xsum : nullptr,
+                         tq == 0 ? a.dbg.xq : nullptr, xs, &sm.sx[0], &sm.xsum[0]);
+    } else if (tq < T) {
+        quant_token_perm(a.x + (size_t)tq * D, D, a.xq + (size_t)tq * D, a.sx + tq, a.xsum + tq,
+                         a.dbg.xq ? a.dbg.xq + (size_t)tq * D : nullptr);
+        cta_arrive(&sy->quant_cnt);
+    }
+
+    // top-K: the quantiser CTA of token tq selects that token's experts
+    // (topk_small_cta, the routine of the four-kernel router) as soon as its
+    // logits are in, and publishes them as data, while the other CTAs stream
+    // the shared expert
+    if (tq < T)
+        topk_small_cta<true>(a.dlog + (size_t)tq * E, a.bias, 1, E, K, a.routed_scale, nullptr, nullptr,
+                             a.dsel + (size_t)tq * K, a.err, sm.tk, sm.tkp);
+
+    // shared expert gate/up, once the quantised tokens are in
+    if (MCH > 1) cta_wait(&sy->quant_cnt, T, a.err);
+    stamp(a, 2);
+    stream_phase<kGateUp, CPLG, MCH>(a, sm, xs, sm.sh_uexp, sm.sh_ubeg, sp0, sp1, A, B, ex_u, ex);
+    stamp(a, 3);
+
+    // ---- phase 2: every CTA reads the published selections (bounded wait;
+    // an entry still empty at the time-out becomes expert 0 with weight 0)
+    // and builds the union itself
+    {
+        const unsigned long long t_begin = global_ns();
+        for (;;) {
+            bool miss = false;
+            for (int i = tid; i < n_sel; i += blockDim.x) {
+                const unsigned long long v = ld_relaxed_u64(a.dsel + i);
+                const int e = (int)(v >> 32);
+                miss |= v == kSelEmpty;
+                sm.idx[i] = (e >= 0 && e < E) ? e : 0;
+                sm.w[i] = v == kSelEmpty ? 0.f : __uint_as_float((uint32_t)v);
+            }
+            if (!__syncthreads_or(miss)) break;
+            const bool late = tid == 0 && global_ns() - t_begin > kWaitNs;
+            if (__syncthreads_or(late)) {
+                if (tid == 0) atomicOr(a.err, kErrSyncTimeout);
+                break;
+            }
+            __nanosleep(64);
+        }
+    }
+    stamp(a, 4);
+    build_union(sm, T, K, S, E, a.n_shared);
+    stamp(a, 5);
+    const int n_r = sm.nu, n_u = n_r + a.n_shared;
+    if (b == 0) {  // the tables for the debug entry point and other readers
+        for (int i = tid; i < n_sel; i += blockDim.x) {
+            a.idx[i] = sm.idx[i];
+            a.wts[i] = sm.w[i];
+        }
+        for (int i = tid; i < n_sel + a.n_shared * T; i += blockDim.x) a.rows[i] = sm.rows[i];
+        for (int i = tid; i < n_u; i += blockDim.x) a.meta->uexp[i] = sm.uexp[i];
+        for (int i = tid; i <= n_u; i += blockDim.x) a.meta->ubeg[i] = sm.ubeg[i];
+        if (tid == 0) {
+            a.meta->n_union = n_u;
+            a.meta->n_gu_items = n_u * a.nb_gu;
+            a.meta->n_dn_items = n_u * a.nb_dn;
+        }
+    }
+
+    // routed experts' gate/up: contiguous slices of (entry, row pair)
+    const long long Nr = (long long)n_r * I;
+    const int rp0 = (int)(b * Nr / G), rp1 = (int)((b + 1) * Nr / G);
+    prime<kGateUp, CPLG>(A, B, a, sm.uexp, I, rp0, rp1, ex_u, ex);
+    stream_phase<kGateUp, CPLG, MCH>(a, sm, xs, sm.uexp, sm.ubeg, rp0, rp1, A, B, ex_u, ex);
+    stamp(a, 6);
+
+    // ---- phase 3: the first down rows are requested, then every CTA waits
+    // for every h row and max|h|
+    constexpr int RPD = UnitShape<kDown, CPLD>::kRows;  // down rows per group
+    const int gpd = D / RPD;
+    const long long Nd = (long long)n_u * gpd;
+    const int dp0 = (int)(b * Nd / G), dp1 = (int)((b + 1) * Nd / G);
+    UnitRegs<kDown, CPLD> A2, B2;
+    prime<kDown, CPLD>(A2, B2, a, sm.uexp, gpd, dp0, dp1, ex_u, ex);
+    cta_arrive(&sy->gu_cnt);
+    cta_wait(&sy->gu_cnt, G, a.err);
+    stamp(a, 7);
+    stream_phase<kDown, CPLD, MCH>(a, sm, xs, sm.uexp, sm.ubeg, dp0, dp1, A2, B2, ex_u, ex);
+    stamp(a, 8);
+
+    // rows written per reduce block; the CTA whose rows complete a block
+    // (n_u entries x its rows) reduces it.  Thread 0 lists the (block, rows)
+    // contributions of this CTA, and one thread per contribution arrives, so
+    // the arrivals travel to L2 together.
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();  // this CTA's partial rows are visible before any arrival
+        int nc = 0;
+        sm.nblk = 0;
+        if (dp0 < dp1) {
+            for (int u = dp0 / gpd; u <= (dp1 - 1) / gpd; ++u) {
+                const int lo = RPD * (max(dp0, u * gpd) - u * gpd), hi = RPD * (min(dp1, (u + 1) * gpd) - u * gpd);
+                for (int bb = lo / kRedRows; bb * kRedRows < hi; ++bb) {
+                    const int b_lo = bb * kRedRows, b_hi = min(D, b_lo + kRedRows);
+                    const int cnt = min(hi, b_hi) - max(lo, b_lo);
+                    if (nc < kMaxContrib) {
+                        sm.contrib[nc++] = make_int2(bb, cnt);
+                    } else if (atomicAdd(&sy->blk[bb], cnt) + cnt == n_u * (b_hi - b_lo)) {
+                        sm.blk_list[atomicAdd(&sm.nblk, 1)] = bb;  // beyond the list: arrive here
+                    }
+                }
+            }
+        }
+        sm.ncontrib = nc;
+    }
+    __syncthreads();
+    if (tid < sm.ncontrib) {
+        const int bb = sm.contrib[tid].x, cnt = sm.contrib[tid].y;
+        const int rows = min(D, (bb + 1) * kRedRows) - bb * kRedRows;
+        if (atomicAdd(&sy->blk[bb], cnt) + cnt == n_u * rows) {
+            __threadfence();  // every other contribution to the block is visible from here on
+            sm.blk_list[atomicAdd(&sm.nblk, 1)] = bb;
+        }
+    }
+    if (tid == 0) __threadfence();
+    __syncthreads();
+    // reduce the completed blocks: one (block, token, 4 rows) task per
+    // thread, every slot loaded before the ordered sum
+    {
+        const int n4 = kRedRows / 4, nt = sm.nblk * T * n4;
+        for (int q = tid; q < nt; q += blockDim.x) {
+            const int blk = q / (T * n4), rem = q - blk * T * n4, t = rem / n4;
+            const int o = sm.blk_list[blk] * kRedRows + 4 * (rem - t * n4);
+            if (o >= D) continue;
+            const float *pt = a.part + (size_t)t * S * D + o;
+            float4 y[kMaxK + 1];
+#pragma unroll
+            for (int k = 0; k <= kMaxK; ++k)
+                if (k < S) y[k] = ld_cg_f4(pt + (size_t)k * D);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < kMaxK; ++k) {
+                if (k < K) {
+                    const float wk = sm.w[t * K + k];
+                    acc.x = __fadd_rn(acc.x, __fmul_rn(wk, y[k].x));
+                    acc.y = __fadd_rn(acc.y, __fmul_rn(wk, y[k].y));
+                    acc.z = __fadd_rn(acc.z, __fmul_rn(wk, y[k].z));
+                    acc.w = __fadd_rn(acc.w, __fmul_rn(wk, y[k].w));
+                }
+            }
+            if (a.n_shared) {
+#pragma unroll
+                for (int k = 0; k <= kMaxK; ++k) {
+                    if (k == K) {
+                        acc.x = __fadd_rn(acc.x, y[k].x);
+                        acc.y = __fadd_rn(acc.y, y[k].y);
+                        acc.z = __fadd_rn(acc.z, y[k].z);
+                        acc.w = __fadd_rn(acc.w, y[k].w);
+                    }
+                }
+            }
+            if (a.resid) {
+                const float4 r = *reinterpret_cast<const float4 *>(a.resid + (size_t)t * D + o);
+                acc.x = __fadd_rn(r.x, acc.x);
+                acc.y = __fadd_rn(r.y, acc.y);
+                acc.z = __fadd_rn(r.z, acc.z);
+                acc.w = __fadd_rn(r.w, acc.w);
+            }
+            *reinterpret_cast<float4 *>(a.out + (size_t)t * D + o) = acc;
+        }
+    }
+
+    // the last CTA to finish clears every counter for the next launch
+    stamp(a, 9);
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        sm.last = atomicAdd(&sy->done_cnt, 1) == G - 1;
+    }
+    __syncthreads();
+    if (sm.last) {
+        for (int i = tid; i < kMaxRedBlk; i += blockDim.x) sy->blk[i] = 0;
+        for (int i = tid; i < T * E; i += blockDim.x) st_relaxed_u32(a.dlog + i, kLogitEmpty);
+        for (int i = tid; i < n_sel; i += blockDim.x) st_relaxed_u64(a.dsel + i, kSelEmpty);
+        for (int i = tid; i < T * S; i += blockDim.x) a.dham[i] = 0u;
+        if (tid == 0) {
+            sy->quant_cnt = 0;
+            sy->gu_cnt = 0;
+            sy->done_cnt = 0;
+        }
+    }
+}
+
+using DecodeFn = void (*)(LayerArgs);
+
+// The kernel for T tokens at chunk counts (CPLG, CPLD): instantiated by one
+// translation unit per (CPLG, CPLD) pair so they compile in parallel.
+template <int CPLG, int CPLD>
+DecodeFn pick_m(int T) {
+    if (T <= 1) return decode_layer_kernel<CPLG, CPLD, 1>;
+    if (T <= 2) return decode_layer_kernel<CPLG, CPLD, 2>;
+    if (T <= 4) return decode_layer_kernel<CPLG, CPLD, 4>;
+    if (T <= 8) return decode_layer_kernel<CPLG, CPLD, 8>;
+    return decode_layer_kernel<CPLG, CPLD, 16>;
+}
+
+}  // namespace dec
+
+// One per instantiated pair (k_decode_c*.cu).
+dec::DecodeFn decode_pick_c11(int T);
+dec::DecodeFn decode_pick_c21(int T);
+dec::DecodeFn decode_pick_c42(int T);
+dec::DecodeFn decode_pick_c62(int T);
+
+}  // namespace moe

@@ -1,0 +1,10 @@
+// k_decode_c62.cu -- instantiations of the persistent decode kernel
+// (decode_dev.cuh) for packed rows of up to 6 (gate/up) and 2 (down)
+// 16-byte chunks per lane.
+#include "decode_dev.cuh"
+
+namespace moe {
+
+dec::DecodeFn decode_pick_c62(int T) { return dec::pick_m<6, 2>(T); }
+
+}  // namespace moe

@@ -5,10 +5,7 @@
 // sigmoid(logit)+bias picks top-K, weight = plain sigmoid * routed_scale;
 // batch union so each expert is read once) and §12 (qrow_i8 per-row int8
 // quantiser); besthub.dev "Running 744B MoE on 25GB RAM" §11, §12.
-#include <cfloat>
-#include <climits>
-
-#include "layer_args.cuh"
+#include "route_dev.cuh"
 
 namespace moe {
 
@@ -50,62 +47,6 @@ __device__ int block_excl_scan(const int *in, int *out, int n, int *wtot) {
     return total;
 }
 
-// ---------------------------------------------------------------- quantiser
-
-// One token row, whole block (256 threads): writes the even/odd permuted int8
-// row, its scale and the sum of its codes (used by the offset-nibble dot
-// product).  D % 8 == 0, D <= 8192, 16-byte aligned rows.  Each thread owns up
-// to four 8-element groups, loaded once into registers before any use.
-__device__ void quant_token_perm(const float *__restrict__ xrow, int D, int8_t *__restrict__ xq_row,
-                                 float *sx_out, int32_t *xsum_out, int8_t *nat_row) {
-    __shared__ float red_f[32];
-    __shared__ int red_i[32];
-    constexpr int G = kMaxDim / (8 * 256);
-    const int ng = D >> 3;
-    float4 v[2 * G];
-#pragma unroll
-    for (int k = 0; k < G; ++k) {
-        const int g = threadIdx.x + 256 * k;
-        if (g < ng) {
-            v[2 * k] = __ldg(reinterpret_cast<const float4 *>(xrow + 8 * g));
-            v[2 * k + 1] = __ldg(reinterpret_cast<const float4 *>(xrow + 8 * g + 4));
-        } else {
-            v[2 * k] = v[2 * k + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    }
-    float amax = 0.f;
-#pragma unroll
-    for (int k = 0; k < 2 * G; ++k)
-        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[k].x), fabsf(v[k].y)), fmaxf(fabsf(v[k].z), fabsf(v[k].w))));
-    amax = block_max_nonneg(amax, red_f);
-    float s, inv;
-    act_scale(amax, s, inv);
-    int sum = 0;
-#pragma unroll
-    for (int k = 0; k < G; ++k) {
-        const int g = threadIdx.x + 256 * k;
-        if (g >= ng) continue;
-        const float4 a = v[2 * k], b = v[2 * k + 1];
-        const int q0 = quant_i8(a.x, inv), q1 = quant_i8(a.y, inv), q2 = quant_i8(a.z, inv),
-                  q3 = quant_i8(a.w, inv), q4 = quant_i8(b.x, inv), q5 = quant_i8(b.y, inv),
-                  q6 = quant_i8(b.z, inv), q7 = quant_i8(b.w, inv);
-        sum += q0 + q1 + q2 + q3 + q4 + q5 + q6 + q7;
-        const uint32_t ev = (q0 & 255) | ((q2 & 255) << 8) | ((q4 & 255) << 16) | ((uint32_t)(q6 & 255) << 24);
-        const uint32_t od = (q1 & 255) | ((q3 & 255) << 8) | ((q5 & 255) << 16) | ((uint32_t)(q7 & 255) << 24);
-        *reinterpret_cast<uint2 *>(xq_row + 8 * g) = make_uint2(ev, od);
-        if (nat_row) {
-            const uint32_t n0 = (q0 & 255) | ((q1 & 255) << 8) | ((q2 & 255) << 16) | ((uint32_t)(q3 & 255) << 24);
-            const uint32_t n1 = (q4 & 255) | ((q5 & 255) << 8) | ((q6 & 255) << 16) | ((uint32_t)(q7 & 255) << 24);
-            *reinterpret_cast<uint2 *>(nat_row + 8 * g) = make_uint2(n0, n1);
-        }
-    }
-    sum = block_sum_i(sum, red_i);
-    if (threadIdx.x == 0) {
-        *sx_out = s;
-        *xsum_out = sum;
-    }
-}
-
 __global__ void __launch_bounds__(256) quant_perm_kernel(LayerArgs a) {
     const int t = blockIdx.x;
     quant_token_perm(a.x + (size_t)t * a.D, a.D, a.xq + (size_t)t * a.D, a.sx + t, a.xsum + t,
@@ -124,73 +65,6 @@ __global__ void __launch_bounds__(256) quant_natural_kernel(const float *__restr
     act_scale(amax, s, inv);
     for (int i = threadIdx.x; i < D; i += blockDim.x) xq[(size_t)blockIdx.x * D + i] = (int8_t)quant_i8(row[i], inv);
     if (threadIdx.x == 0) sx[blockIdx.x] = s;
-}
-
-// ------------------------------------------------------------------ top-K
-
-// sigmoid / selection score of one expert, fp32 IEEE as on the pages.
-__device__ __forceinline__ void score(float logit, float b, float &p, float &c) {
-    p = __fdiv_rn(1.f, __fadd_rn(1.f, expf(-logit)));
-    c = __fadd_rn(p, b);
-}
-
-// Order-preserving map of a float onto uint32 (for non-NaN values): larger
-// float <=> larger key, equal floats <=> equal keys.
-__device__ __forceinline__ uint32_t order_key(float v) {
-    const uint32_t u = __float_as_uint(v);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// Greedy top-K of one token by one warp.  Lane l holds experts l + 32 j.
-// Each round takes the largest c among the experts not yet taken; an exact
-// tie goes to the lower expert index (the pages' strict '>' ascending scan).
-// A round is one warp max over the order keys and one warp min over the
-// indices of the lanes that hold that key.  NaN scores never win.
-template <int EPL>
-__device__ void select_topk(const float (&c)[EPL], const float (&p)[EPL], int E, int K, float scale,
-                            int32_t *idx_out, float *w_out, int *s_idx_out, int32_t *err) {
-    const int lane = threadIdx.x & 31;
-    uint32_t key[EPL];
-#pragma unroll
-    for (int j = 0; j < EPL; ++j) key[j] = (lane + 32 * j < E && !(c[j] != c[j])) ? order_key(c[j]) : 0u;
-    uint32_t taken = 0;
-    for (int k = 0; k < K; ++k) {
-        // lane-local best: largest key, lowest index on a tie (ascending j)
-        uint32_t bk = 0;
-        int bj = -1;
-#pragma unroll
-        for (int j = 0; j < EPL; ++j)
-            if (!((taken >> j) & 1u) && key[j] > bk) {
-                bk = key[j];
-                bj = j;
-            }
-        const uint32_t wk = __reduce_max_sync(0xffffffffu, bk);
-        int bi;
-        if (wk == 0u) {
-            // no finite score left (non-finite input): lowest free index, weight 0
-            int cand = INT_MAX;
-#pragma unroll
-            for (int j = EPL - 1; j >= 0; --j)
-                if (!((taken >> j) & 1u) && lane + 32 * j < E) cand = lane + 32 * j;
-            bi = __reduce_min_sync(0xffffffffu, cand);
-            if (lane == 0 && err) atomicOr(err, kErrNoSelection);
-        } else {
-            bi = __reduce_min_sync(0xffffffffu, (bk == wk && bj >= 0) ? lane + 32 * bj : INT_MAX);
-        }
-        const int owner = bi & 31, oj = bi >> 5;
-        float pv = 0.f;
-#pragma unroll
-        for (int j = 0; j < EPL; ++j)
-            if (j == oj) pv = p[j];
-        pv = __shfl_sync(0xffffffffu, pv, owner);
-        if (wk == 0u) pv = 0.f;
-        if (lane == owner) taken |= 1u << oj;
-        if (lane == 0) {
-            idx_out[k] = bi;
-            w_out[k] = __fmul_rn(pv, scale);
-            if (s_idx_out) s_idx_out[k] = bi;
-        }
-    }
 }
 
 // ------------------------------------------------------- routing tables
@@ -249,63 +123,31 @@ __device__ void build_routing_small(const LayerArgs &a, const int *s_idx, int T)
 
 // --------------------------------------------------- small-batch router
 
-// T <= kSmallT.  CTAs [0, ceil(E/2)) compute the logits of two experts each
-// (four warps per expert, each a quarter of D);
-// CTAs [ceil(E/2), ceil(E/2)+T) quantise one token each.  The last CTA to
-// finish (arrival counter, no waiting) runs top-K and builds the union.
-template <int EPL>
+// T <= kSmallT.  CTA e < E computes the logits of expert e (expert_logits_cta);
+// CTAs [E, E+T) quantise one token each.  The last CTA to
+// finish (arrival counter, no waiting) runs top-K (topk_small_cta) and builds
+// the union.
 __global__ void __launch_bounds__(256) router_small_kernel(LayerArgs a) {
     __shared__ float red[8][kSmallT];
+    __shared__ unsigned long long tk[4][8][kMaxK];
+    __shared__ float tkp[4][8][kMaxK];
     __shared__ int s_idx[kSmallT * kMaxK];
     __shared__ int s_last;
     const int T = a.T, D = a.D, E = a.E;
-    const int n_lcta = (E + 1) >> 1;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x;
 
-    if ((int)blockIdx.x >= n_lcta) {
-        const int t = blockIdx.x - n_lcta;
+    if ((int)blockIdx.x >= E) {
+        const int t = blockIdx.x - E;
         quant_token_perm(a.x + (size_t)t * D, D, a.xq + (size_t)t * D, a.sx + t, a.xsum + t,
                          a.dbg.xq ? a.dbg.xq + (size_t)t * D : nullptr);
         if (t == 0)
             for (int i = tid; i < T * a.S; i += blockDim.x) a.hamax[i] = 0u;
     } else {
-        // warp = (expert, quarter of D); all of the warp's router weights are
-        // loaded before any use so the CTA has its whole 2 x 24 KB in flight
-        const int e = blockIdx.x * 2 + (warp >> 2), q = warp & 3;
-        const int L4 = D >> 4;  // float4 per quarter row
-        float4 w[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const int c = j * 32 + lane;
-            w[j] = (e < E && c < L4) ? __ldg(reinterpret_cast<const float4 *>(a.Wr + (size_t)e * D) + q * L4 + c)
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        for (int t = 0; t < T; ++t) {
-            const float4 *xr = reinterpret_cast<const float4 *>(a.x + (size_t)t * D) + q * L4;
-            float v = 0.f;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int c = j * 32 + lane;
-                if (c < L4) {
-                    const float4 xv = __ldg(xr + c);
-                    v = fmaf(w[j].x, xv.x, v);
-                    v = fmaf(w[j].y, xv.y, v);
-                    v = fmaf(w[j].z, xv.z, v);
-                    v = fmaf(w[j].w, xv.w, v);
-                }
-            }
-            v = warp_sum_f(v);
-            if (lane == 0) red[warp][t] = v;
-        }
-        __syncthreads();
-        if (tid < 2 * kSmallT) {
-            const int which = tid / kSmallT, t = tid % kSmallT, e2 = blockIdx.x * 2 + which;
-            if (t < T && e2 < E) {
-                const int w0 = which * 4;
-                const float l = ((red[w0][t] + red[w0 + 1][t]) + red[w0 + 2][t]) + red[w0 + 3][t];
-                a.logits[t * E + e2] = l;
-                __threadfence();  // the writer makes its logit visible before the arrival
-            }
+        const int e = blockIdx.x;
+        const float l = expert_logits_cta(a.Wr + (size_t)e * D, a.x, T, D, red);
+        if (tid < T) {
+            a.logits[tid * E + e] = l;
+            __threadfence();  // the writer makes its logit visible before the arrival
         }
     }
 
@@ -316,22 +158,8 @@ __global__ void __launch_bounds__(256) router_small_kernel(LayerArgs a) {
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    for (int t = warp; t < T; t += 8) {
-        float c[EPL], p[EPL];
-#pragma unroll
-        for (int j = 0; j < EPL; ++j) {
-            const int e = lane + 32 * j;
-            if (e < E) {
-                score(__ldcg(a.logits + t * E + e), __ldg(a.bias + e), p[j], c[j]);
-            } else {
-                p[j] = 0.f;
-                c[j] = -INFINITY;
-            }
-        }
-        select_topk<EPL>(c, p, E, a.K, a.routed_scale, a.idx + t * a.K, a.wts + t * a.K,
-                         s_idx + t * a.K, a.err);
-    }
-    __syncthreads();
+    topk_small_cta<false>(a.logits, a.bias, T, E, a.K, a.routed_scale, s_idx, a.wts, nullptr, a.err, tk, tkp);
+    for (int i = tid; i < T * a.K; i += blockDim.x) a.idx[i] = s_idx[i];
     build_routing_small(a, s_idx, T);
     if (tid == 0) a.meta->counter = 0;
 }
@@ -497,14 +325,7 @@ __global__ void __launch_bounds__(1024) permute_large_kernel(LayerArgs a) {
 static int epl_for(int E) { return E <= 32 ? 1 : E <= 64 ? 2 : E <= 128 ? 4 : E <= 256 ? 8 : 16; }
 
 cudaError_t launch_router_small(const LayerArgs &a, cudaStream_t s) {
-    const int grid = (a.E + 1) / 2 + a.T;
-    switch (epl_for(a.E)) {
-        case 1: router_small_kernel<1><<<grid, 256, 0, s>>>(a); break;
-        case 2: router_small_kernel<2><<<grid, 256, 0, s>>>(a); break;
-        case 4: router_small_kernel<4><<<grid, 256, 0, s>>>(a); break;
-        case 8: router_small_kernel<8><<<grid, 256, 0, s>>>(a); break;
-        default: router_small_kernel<16><<<grid, 256, 0, s>>>(a); break;
-    }
+    router_small_kernel<<<a.E + a.T, 256, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -17,89 +17,9 @@
 // nibble-lane layout, staged once per expert the CTA meets (one CTA-wide
 // barrier pair per expert boundary).  Offset nibbles go straight into dp4a
 // (sum((n-8)x) = sum(nx) - 8 sum(x)), a warp reduction finishes each row.
-#include "layer_args.cuh"
+#include "stream_dev.cuh"
 
 namespace moe {
-
-constexpr int kErrTooManyRows = 8;  // device error bit: an expert had more rows than the tile
-
-enum Kind { kGateUp = 0, kDown = 1 };
-
-// A unit is what one warp multiplies between two pipeline steps: one packed
-// row (gate or up) for the gate/up kernel, two rows for the down kernel.
-template <int KIND>
-struct UnitShape {
-    static constexpr int kRows = KIND == kGateUp ? 1 : 2;
-};
-
-template <int KIND, int CPL>
-struct UnitRegs {
-    int4 w[UnitShape<KIND>::kRows][CPL];
-    float s[UnitShape<KIND>::kRows];
-};
-
-template <int KIND, int CPL>
-__device__ __forceinline__ void load_unit(UnitRegs<KIND, CPL> &r, const uint8_t *mat, const float *scale, int o,
-                                          int rowb, int nch, int lane) {
-#pragma unroll
-    for (int rr = 0; rr < UnitShape<KIND>::kRows; ++rr) {
-        const uint8_t *row = mat + (size_t)(o + rr) * rowb;
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) {
-            const int ch = lane + 32 * c;
-            if (ch < nch) r.w[rr][c] = ld_stream16(row + (size_t)ch * 16);
-        }
-        r.s[rr] = __ldg(scale + o + rr);
-    }
-}
-
-// Shared-memory activations: row m holds the even/odd int8 row split in two
-// planes, plane A = the first 16 bytes of every 32-byte chunk (activation
-// groups 4c, 4c+1), plane B = the last 16 (groups 4c+2, 4c+3), so that the
-// 16-byte reads of a warp are contiguous (no bank conflicts).
-__device__ __forceinline__ int8_t *plane_byte(int8_t *xs, int kdim, int m, int byte) {
-    const int ch = byte >> 5, in = byte & 31;
-    return xs + (size_t)m * kdim + (in >= 16 ? (kdim >> 1) : 0) + ch * 16 + (in & 15);
-}
-
-// acc[m] += dot(row, x_m) over this lane's chunks (offset nibbles, even/odd x).
-template <int CPL, int MCH>
-__device__ __forceinline__ void dot_rows(int (&acc)[MCH], const int4 (&w)[CPL], const int8_t *xs, int kdim, int M,
-                                         int nch, int lane) {
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) {
-        const int ch = lane + 32 * c;
-        if (ch < nch) {
-#pragma unroll
-            for (int m = 0; m < MCH; ++m) {
-                if (m < M) {
-                    const int4 *pa = reinterpret_cast<const int4 *>(xs + (size_t)m * kdim);
-                    const int4 x0 = pa[ch], x1 = pa[(kdim >> 5) + ch];
-                    int v = acc[m];
-                    v = dot_word((uint32_t)w[c].x, x0.x, x0.y, v);
-                    v = dot_word((uint32_t)w[c].y, x0.z, x0.w, v);
-                    v = dot_word((uint32_t)w[c].z, x1.x, x1.y, v);
-                    v = dot_word((uint32_t)w[c].w, x1.z, x1.w, v);
-                    acc[m] = v;
-                }
-            }
-        }
-    }
-}
-
-// Warp sums of acc[0..M); lane m receives the sum of token row m.
-template <int MCH>
-__device__ __forceinline__ int lane_sum(const int (&acc)[MCH], int M, int lane) {
-    int mine = 0;
-#pragma unroll
-    for (int m = 0; m < MCH; ++m) {
-        if (m < M) {
-            const int v = warp_sum_i(acc[m]);
-            if (lane == m) mine = v;
-        }
-    }
-    return mine;
-}
 
 // Work list of one CTA: a contiguous range [p0, p1) of row groups over all
 // union experts (gate/up: row pairs, each = a gate unit then an up unit;
@@ -107,7 +27,7 @@ __device__ __forceinline__ int lane_sum(const int (&acc)[MCH], int M, int lane) 
 template <int KIND, int CPL, int MCH>
 __global__ void __launch_bounds__(256) stream_kernel(LayerArgs a) {
     constexpr int UPG = KIND == kGateUp ? 2 : 1;        // units per row group
-    constexpr int RPG = UnitShape<KIND>::kRows;          // output rows per row group
+    constexpr int RPG = UnitShape<KIND, CPL>::kRows;          // output rows per row group
     extern __shared__ __align__(16) int8_t xs[];         // [MCH][kdim] even/odd int8 activations
     __shared__ int s_ent[MCH], s_xsum[MCH];
     __shared__ float s_sx[MCH];

@@ -28,6 +28,14 @@ struct LayerArgs {
     int32_t *hsum;       // [Tmax * S] code sums of hq rows
     float *shq;          // [Tmax * S] scales of hq rows
     int32_t *dn_cnt;     // [nb_dn] arrival counters of the fused reduce
+    FusedSync *sync;     // counters of the persistent decode kernel
+    // hand-over buffers of the persistent decode kernel; every launch leaves
+    // them as it found them (logits / selections empty, max|h| zero)
+    float *dlog;                 // [kSmallT, E] logits, kLogitEmpty until written
+    unsigned long long *dsel;    // [kSmallT, K] packed selections, kSelEmpty until written
+    uint32_t *dham;              // [kSmallT * S] bits of max|h| per grouped row
+    unsigned long long *trace;  // [trace_n] phase stamps of that kernel, or null
+    int trace_n;
     float *out;          // [T, D]
     const float *resid;  // [T, D] or null: out = resid + MoE
     int32_t *err;
@@ -55,6 +63,10 @@ cudaError_t launch_pack_int4(const float *w, uint8_t *q4, float *scale, int64_t 
 cudaError_t launch_gateup_stream(const LayerArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_down_stream(const LayerArgs &a, int grid, cudaStream_t s);
 bool stream_supported(int D, int I);
+// Persistent single-kernel layer for T <= kSmallT (cooperative launch).
+// decode_grid: CTAs of the launch for this T (0 if the kernel cannot run).
+cudaError_t decode_grid(const LayerArgs &a, int num_sms, int *grid);
+cudaError_t launch_decode_layer(const LayerArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_grouped_gateup(const LayerArgs &a, int num_sms, cudaStream_t s);
 cudaError_t launch_requant_h(const LayerArgs &a, cudaStream_t s);
 cudaError_t launch_grouped_down(const LayerArgs &a, int num_sms, cudaStream_t s);

@@ -55,14 +55,22 @@ struct Handle {
     int32_t *hsum;
     float *shq;
     int32_t *dn_cnt;
+    moe::FusedSync *sync;
+    float *dlog;
+    unsigned long long *dsel;
+    uint32_t *dham;
     int32_t *err;
     float *xnorm;  // [Tmax, D] RMSNorm output of moe_block_forward
     int nb_gu, rpi_gu, nb_dn, rpi_dn;
     int grid_gu[4], grid_dn[4];
     int num_sms;
     bool stream_ok;  // shapes and alignment the streaming kernels cover
+    bool single_kernel;  // decode batches run the persistent single-kernel layer
+    int dec_grid[moe::kSmallT + 1];  // its grid per token count (0: not available)
     int probe_which;
     cudaEvent_t probe_begin, probe_end;
+    unsigned long long *trace;  // phase stamps of the persistent decode kernel
+    int trace_n;
 };
 
 constexpr int kRpiGu = 16;  // gate/up rows per item: 2 per warp
@@ -92,6 +100,10 @@ size_t layout(const MoeLayerDesc &d, Handle *h) {
     const size_t o_hsum = take(4 * T * S);
     const size_t o_shq = take(4 * T * S);
     const size_t o_cnt = take(4 * nb_dn);
+    const size_t o_sync = take(sizeof(moe::FusedSync));
+    const size_t o_dlog = take(4 * moe::kSmallT * E);
+    const size_t o_dsel = take(8 * moe::kSmallT * K);
+    const size_t o_dham = take(4 * moe::kSmallT * S);
     const size_t o_err = take(4);
     const size_t o_xn = take(4 * T * D);
     if (h) {
@@ -111,6 +123,10 @@ size_t layout(const MoeLayerDesc &d, Handle *h) {
         h->hsum = reinterpret_cast<int32_t *>(b + o_hsum);
         h->shq = reinterpret_cast<float *>(b + o_shq);
         h->dn_cnt = reinterpret_cast<int32_t *>(b + o_cnt);
+        h->sync = reinterpret_cast<moe::FusedSync *>(b + o_sync);
+        h->dlog = reinterpret_cast<float *>(b + o_dlog);
+        h->dsel = reinterpret_cast<unsigned long long *>(b + o_dsel);
+        h->dham = reinterpret_cast<uint32_t *>(b + o_dham);
         h->err = reinterpret_cast<int32_t *>(b + o_err);
         h->xnorm = reinterpret_cast<float *>(b + o_xn);
     }
@@ -147,6 +163,34 @@ cudaError_t record(cudaEvent_t ev, cudaStream_t s) {
     return cudaEventRecord(ev, s);
 }
 
+// The state the persistent decode kernel expects at launch (and restores at
+// its end): zero counters and max|h| words, empty logit and selection slots.
+cudaError_t reset_decode_state(const Handle *h, cudaStream_t s) {
+    cudaError_t ce = cudaMemsetAsync(h->sync, 0, sizeof(moe::FusedSync), s);
+    if (ce == cudaSuccess) ce = cudaMemsetAsync(h->dham, 0, 4 * moe::kSmallT * (size_t)h->S, s);
+    if (ce == cudaSuccess) ce = cudaMemsetAsync(h->dlog, 0xFF, 4 * moe::kSmallT * (size_t)h->d.E, s);
+    if (ce == cudaSuccess) ce = cudaMemsetAsync(h->dsel, 0xFF, 8 * moe::kSmallT * (size_t)h->d.K, s);
+    return ce;
+}
+
+// Grids of the persistent decode kernel for T = 1..kSmallT (0 where it
+// cannot run: unsupported shape or no cooperative launch).
+cudaError_t prepare_decode(Handle *h) {
+    moe::LayerArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.D = h->d.D; a.I = h->d.I; a.E = h->d.E; a.K = h->d.K; a.S = h->S; a.n_shared = h->d.n_shared;
+    h->dec_grid[0] = 0;
+    for (int T = 1; T <= moe::kSmallT; ++T) {
+        a.T = T;
+        h->dec_grid[T] = 0;
+        if (T > h->d.max_tokens) continue;
+        cudaError_t ce = moe::decode_grid(a, h->num_sms, &h->dec_grid[T]);
+        if (ce != cudaSuccess) return ce;
+    }
+    h->single_kernel = true;
+    return cudaSuccess;
+}
+
 // The launch sequence of one forward.  x is the layer input (already
 // normalised for a block), out/resid as in LayerArgs.
 int run_layer(Handle *h, const float *x, int T, float *out, const float *resid, const moe::DebugPtrs &dbg,
@@ -158,7 +202,9 @@ int run_layer(Handle *h, const float *x, int T, float *out, const float *resid, 
     a.x = x; a.Wr = h->Wr; a.bias = h->bias; a.experts = h->experts;
     a.xq = h->xq; a.sx = h->sx; a.xsum = h->xsum; a.logits = h->logits; a.idx = h->idx; a.wts = h->wts;
     a.rows = h->rows; a.meta = h->meta; a.h = h->h; a.hamax = h->hamax; a.part = h->part; a.dn_cnt = h->dn_cnt;
-    a.hq = h->hq; a.hsum = h->hsum; a.shq = h->shq;
+    a.hq = h->hq; a.hsum = h->hsum; a.shq = h->shq; a.sync = h->sync;
+    a.dlog = h->dlog; a.dsel = h->dsel; a.dham = h->dham;
+    a.trace = h->trace; a.trace_n = h->trace_n;
     a.out = out; a.resid = resid; a.err = h->err;
     a.nb_gu = h->nb_gu; a.rpi_gu = h->rpi_gu; a.nb_dn = h->nb_dn; a.rpi_dn = h->rpi_dn;
     a.dbg = dbg;
@@ -166,6 +212,18 @@ int run_layer(Handle *h, const float *x, int T, float *out, const float *resid, 
     const int mi = moe::mch_index(mch);
     const bool small = T <= moe::kSmallT;
     cudaError_t ce;
+
+    // decode-sized batches: the whole layer as one persistent kernel (every
+    // probe id brackets it)
+    if (small && h->single_kernel && h->dec_grid[T] > 0) {
+        if (h->probe_which != MOE_PROBE_NONE && (ce = record(h->probe_begin, s)) != cudaSuccess)
+            return cuda_fail(ce, "probe record");
+        if ((ce = moe::launch_decode_layer(a, h->dec_grid[T], s)) != cudaSuccess)
+            return cuda_fail(ce, "decode layer launch");
+        if (h->probe_which != MOE_PROBE_NONE && (ce = record(h->probe_end, s)) != cudaSuccess)
+            return cuda_fail(ce, "probe record");
+        return MOE_OK;
+    }
 
     if (h->probe_which == MOE_PROBE_ROUTER && (ce = record(h->probe_begin, s)) != cudaSuccess)
         return cuda_fail(ce, "probe record");
@@ -312,7 +370,8 @@ int moe_layer_create(const MoeLayerDesc *desc, const float *Wr, const float *bia
     }
     h->num_sms = nsm;
     h->stream_ok = moe::stream_supported(desc->D, desc->I);
-    if ((ce = moe::prepare_expert_kernels(desc->D, desc->I, nsm, h->grid_gu, h->grid_dn)) != cudaSuccess) {
+    if ((ce = moe::prepare_expert_kernels(desc->D, desc->I, nsm, h->grid_gu, h->grid_dn)) != cudaSuccess ||
+        (ce = prepare_decode(h)) != cudaSuccess) {
         delete h;
         return cuda_fail(ce, "kernel attributes");
     }
@@ -342,6 +401,7 @@ int moe_layer_create(const MoeLayerDesc *desc, const float *Wr, const float *bia
     ce = cudaMemcpy(h->experts, tab, sizeof(moe::DevExpert) * ne, cudaMemcpyHostToDevice);
     delete[] tab;
     if (ce == cudaSuccess) ce = cudaMemset(h->ws, 0, h->ws_bytes);
+    if (ce == cudaSuccess) ce = reset_decode_state(h, 0);
     if (ce == cudaSuccess) ce = cudaDeviceSynchronize();
     if (ce != cudaSuccess) {
         cudaFree(h->ws);
@@ -418,9 +478,54 @@ int moe_layer_device_status(void *handle, cudaStream_t stream, int *status_out) 
     cudaError_t ce = cudaStreamSynchronize(stream);
     if (ce == cudaSuccess) ce = cudaMemcpy(&v, h->err, 4, cudaMemcpyDeviceToHost);
     if (ce == cudaSuccess) ce = cudaMemset(h->err, 0, 4);
+    // a wait that ran out of time may leave the decode kernel's state behind
+    if (ce == cudaSuccess && (v & moe::kErrSyncTimeout)) ce = reset_decode_state(h, stream);
+    if (ce == cudaSuccess && (v & moe::kErrSyncTimeout)) ce = cudaStreamSynchronize(stream);
     if (ce != cudaSuccess) return cuda_fail(ce, "device status");
     *status_out = v;
     return v ? fail(MOE_ERR_DEVICE, "device error flags 0x%x", v) : MOE_OK;
+}
+
+int moe_layer_set_option(void *handle, int option, int value) {
+    Handle *h = as_handle(handle);
+    if (!h) return fail(MOE_ERR_INVALID_ARG, "invalid handle");
+    switch (option) {
+        case MOE_OPT_DECODE_SINGLE_KERNEL:
+            if (value != 0 && value != 1) return fail(MOE_ERR_INVALID_ARG, "value %d: need 0 or 1", value);
+            h->single_kernel = value != 0;
+            return MOE_OK;
+        default:
+            return fail(MOE_ERR_INVALID_ARG, "unknown option %d", option);
+    }
+}
+
+int moe_layer_get_option(void *handle, int option, int *value_out) {
+    Handle *h = as_handle(handle);
+    if (!h || !value_out) return fail(MOE_ERR_INVALID_ARG, "invalid handle or NULL value_out");
+    switch (option) {
+        case MOE_OPT_DECODE_SINGLE_KERNEL:
+            *value_out = h->single_kernel ? 1 : 0;
+            return MOE_OK;
+        case MOE_OPT_DECODE_SINGLE_KERNEL_AVAILABLE: {
+            int any = 0;
+            for (int T = 1; T <= moe::kSmallT; ++T) any |= h->dec_grid[T] > 0;
+            *value_out = any;
+            return MOE_OK;
+        }
+        default:
+            return fail(MOE_ERR_INVALID_ARG, "unknown option %d", option);
+    }
+}
+
+int moe_layer_set_trace(void *handle, uint64_t *stamps_dev, int n_stamps) {
+    Handle *h = as_handle(handle);
+    if (!h) return fail(MOE_ERR_INVALID_ARG, "invalid handle");
+    if (n_stamps < 0 || (n_stamps > 0 && !stamps_dev)) return fail(MOE_ERR_INVALID_ARG, "bad trace buffer");
+    if (stamps_dev && (reinterpret_cast<uintptr_t>(stamps_dev) & 7u))
+        return fail(MOE_ERR_INVALID_ARG, "trace buffer must be 8-byte aligned");
+    h->trace = n_stamps > 0 ? reinterpret_cast<unsigned long long *>(stamps_dev) : nullptr;
+    h->trace_n = n_stamps;
+    return MOE_OK;
 }
 
 int moe_layer_set_probe(void *handle, int which, cudaEvent_t begin, cudaEvent_t end) {
@@ -512,12 +617,14 @@ extern "C" int moe_layer_forward_static(const MoeLayerDesc *desc, const float *W
     h.nb_dn = (d.D + kRpiDn - 1) / kRpiDn;
     h.num_sms = st.num_sms;
     h.stream_ok = moe::stream_supported(d.D, d.I);
-    if ((ce = moe::prepare_expert_kernels(d.D, d.I, st.num_sms, h.grid_gu, h.grid_dn)) != cudaSuccess)
+    if ((ce = moe::prepare_expert_kernels(d.D, d.I, st.num_sms, h.grid_gu, h.grid_dn)) != cudaSuccess ||
+        (ce = prepare_decode(&h)) != cudaSuccess)
         return cuda_fail(ce, "kernel attributes");
     // the arrival counters, routing tables and error word must start at zero;
     // everything else is written before it is read
     if ((ce = cudaMemsetAsync(h.meta, 0, sizeof(moe::RouteMeta), stream)) != cudaSuccess ||
         (ce = cudaMemsetAsync(h.dn_cnt, 0, 4 * (size_t)((d.D + 15) / 16), stream)) != cudaSuccess ||
+        (ce = reset_decode_state(&h, stream)) != cudaSuccess ||
         (ce = cudaMemsetAsync(h.err, 0, 4, stream)) != cudaSuccess)
         return cuda_fail(ce, "static workspace clear");
     return run_layer(&h, x, n_tokens, out, nullptr, moe::DebugPtrs{}, stream);
