@@ -225,6 +225,12 @@ int moe_layer_set_probe(void *handle, int which, cudaEvent_t begin, cudaEvent_t 
 #define MOE_OPT_DECODE_SINGLE_KERNEL 1
 /* read-only: 1 when the single-kernel path can run for this handle */
 #define MOE_OPT_DECODE_SINGLE_KERNEL_AVAILABLE 2
+/* 1 (default): batches of more than 16 tokens run their expert GEMMs on the
+ * tcgen05 tensor cores (kind::f16 with the int4 / int8 values carried exactly,
+ * fp32 accumulation, which is exact for these sizes); 0: on the legacy integer
+ * MMA (mma.sync s8 x u8).  Both give bit-identical int32 dot products.  Needs
+ * D % 128 == 0 and I % 64 == 0. */
+#define MOE_OPT_TCGEN05_GEMM 3
 
 /*
  * Set / read a handle option (host).  Not part of the pages' interface: these

@@ -71,6 +71,10 @@ cudaError_t launch_grouped_gateup(const LayerArgs &a, int num_sms, cudaStream_t 
 cudaError_t launch_requant_h(const LayerArgs &a, cudaStream_t s);
 cudaError_t launch_grouped_down(const LayerArgs &a, int num_sms, cudaStream_t s);
 bool grouped_supported(int D, int I);
+// Tensor-core (tcgen05, f16-exact) expert GEMMs of large batches.
+bool umma_supported(int D, int I);
+cudaError_t launch_umma_gateup(const LayerArgs &a, int num_sms, cudaStream_t s);
+cudaError_t launch_umma_down(const LayerArgs &a, int num_sms, cudaStream_t s);
 // Occupancy-derived grid sizes and kernel attributes (call once per device).
 cudaError_t prepare_expert_kernels(int D, int I, int num_sms, int grid_gu[4], int grid_dn[4]);
 int mch_index(int mch);

@@ -66,6 +66,7 @@ struct Handle {
     int num_sms;
     bool stream_ok;  // shapes and alignment the streaming kernels cover
     bool single_kernel;  // decode batches run the persistent single-kernel layer
+    bool tcgen05_gemm;   // larger batches run the tcgen05 expert GEMMs
     int dec_grid[moe::kSmallT + 1];  // its grid per token count (0: not available)
     int probe_which;
     cudaEvent_t probe_begin, probe_end;
@@ -188,6 +189,7 @@ cudaError_t prepare_decode(Handle *h) {
         if (ce != cudaSuccess) return ce;
     }
     h->single_kernel = true;
+    h->tcgen05_gemm = true;
     return cudaSuccess;
 }
 
@@ -240,16 +242,20 @@ int run_layer(Handle *h, const float *x, int T, float *out, const float *resid, 
         return cuda_fail(ce, "probe record");
 
     // larger batches with tile-aligned shapes: tensor-core grouped GEMMs
-    if (!small && moe::grouped_supported(a.D, a.I)) {
+    // (tcgen05 with f16-exact operands; the legacy integer MMA on request)
+    const bool umma = h->tcgen05_gemm && moe::umma_supported(a.D, a.I);
+    if (!small && (umma || moe::grouped_supported(a.D, a.I))) {
         if (h->probe_which == MOE_PROBE_GATE_UP && (ce = record(h->probe_begin, s)) != cudaSuccess)
             return cuda_fail(ce, "probe record");
-        if ((ce = moe::launch_grouped_gateup(a, h->num_sms, s)) != cudaSuccess) return cuda_fail(ce, "gateup launch");
+        ce = umma ? moe::launch_umma_gateup(a, h->num_sms, s) : moe::launch_grouped_gateup(a, h->num_sms, s);
+        if (ce != cudaSuccess) return cuda_fail(ce, "gateup launch");
         if (h->probe_which == MOE_PROBE_GATE_UP && (ce = record(h->probe_end, s)) != cudaSuccess)
             return cuda_fail(ce, "probe record");
         if (h->probe_which == MOE_PROBE_DOWN && (ce = record(h->probe_begin, s)) != cudaSuccess)
             return cuda_fail(ce, "probe record");
         if ((ce = moe::launch_requant_h(a, s)) != cudaSuccess) return cuda_fail(ce, "requant launch");
-        if ((ce = moe::launch_grouped_down(a, h->num_sms, s)) != cudaSuccess) return cuda_fail(ce, "down launch");
+        ce = umma ? moe::launch_umma_down(a, h->num_sms, s) : moe::launch_grouped_down(a, h->num_sms, s);
+        if (ce != cudaSuccess) return cuda_fail(ce, "down launch");
         if ((ce = moe::launch_reduce(a, s)) != cudaSuccess) return cuda_fail(ce, "reduce launch");
         if (h->probe_which == MOE_PROBE_DOWN && (ce = record(h->probe_end, s)) != cudaSuccess)
             return cuda_fail(ce, "probe record");
@@ -494,6 +500,10 @@ int moe_layer_set_option(void *handle, int option, int value) {
             if (value != 0 && value != 1) return fail(MOE_ERR_INVALID_ARG, "value %d: need 0 or 1", value);
             h->single_kernel = value != 0;
             return MOE_OK;
+        case MOE_OPT_TCGEN05_GEMM:
+            if (value != 0 && value != 1) return fail(MOE_ERR_INVALID_ARG, "value %d: need 0 or 1", value);
+            h->tcgen05_gemm = value != 0;
+            return MOE_OK;
         default:
             return fail(MOE_ERR_INVALID_ARG, "unknown option %d", option);
     }
@@ -505,6 +515,9 @@ int moe_layer_get_option(void *handle, int option, int *value_out) {
     switch (option) {
         case MOE_OPT_DECODE_SINGLE_KERNEL:
             *value_out = h->single_kernel ? 1 : 0;
+            return MOE_OK;
+        case MOE_OPT_TCGEN05_GEMM:
+            *value_out = h->tcgen05_gemm ? 1 : 0;
             return MOE_OK;
         case MOE_OPT_DECODE_SINGLE_KERNEL_AVAILABLE: {
             int any = 0;
