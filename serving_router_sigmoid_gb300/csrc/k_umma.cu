@@ -60,20 +60,24 @@ constexpr int kLoadWarp0 = 21;            // four load warps
 constexpr int kLoadWarps = 4;
 constexpr int kBKs = 64;                  // K elements per stage
 constexpr int kTok = 128;                 // token columns per tile at most
-constexpr int kSt = 3;                    // f16 operand stages
+constexpr int kSt = 5;                    // operand stages (weights in TMEM, activations in shared memory)
 constexpr int kRA = 4;                    // weight raw ring: slots of up to 4 stages (128 bytes per row)
 constexpr int kRB = 6;                    // activation raw ring (stages of lookahead)
-constexpr uint32_t kAF16 = 128 * 128;     // 128 rows x 64 f16
 constexpr uint32_t kBF16 = kTok * 128;    // 128 tokens x 64 f16
-constexpr uint32_t kARowPitch = 144;      // raw weight row pitch: 128 bytes + 16 of padding (no bank conflicts)
-constexpr uint32_t kARaw = 128 * kARowPitch;  // 128 rows x up to 4 stages of 64 int4
+constexpr uint32_t kARowPitch = 144;      // raw weight row pitch: 128 bytes + 16 of padding
+// raw weight row r sits at r * pitch (+64 for the second 64-row half), so the
+// 16-byte reads of 8 consecutive tile rows fall in 8 different bank groups
+__device__ __forceinline__ uint32_t raw_row_off(int r) { return (uint32_t)r * kARowPitch + (r >= 64 ? 64u : 0u); }
+constexpr uint32_t kARaw = 128 * kARowPitch + 64;  // 128 rows x up to 4 stages of 64 int4
 constexpr uint32_t kBRaw = kTok * 64;     // 128 tokens x 64 int8
-constexpr uint32_t kOffB = kSt * kAF16;
+constexpr uint32_t kOffB = 0;
 constexpr uint32_t kOffRA = kOffB + kSt * kBF16;
 constexpr uint32_t kOffRB = kOffRA + kRA * kARaw;
-constexpr uint32_t kDyn = kOffRB + kRB * kBRaw;  // 216 KB
+constexpr uint32_t kDyn = kOffRB + kRB * kBRaw;  // 200 KB
 constexpr size_t kSmemBytes = kDyn + 1024;       // + alignment to 1024 bytes
-constexpr uint32_t kTmemCols = 2 * kTok;
+constexpr uint32_t kTmemCols = 512;       // accumulators [0, 256), weight stages [256, 256 + 32 kSt)
+constexpr uint32_t kTmemA = 2 * kTok;     // first weight-stage column
+constexpr uint32_t kAcolStage = 32;       // columns per weight stage: 64 f16 as 32 pairs
 
 struct UmmaSmem {
     uint64_t full[kSt], empty[kSt], acc_full[2], acc_empty[2], drain;
@@ -270,9 +274,12 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(LayerArgs a) {
         // ------------------------------------------------------ converters
         const int grp = (tid - kConv0) >> 8;      // this group converts stages i = grp (mod 2)
         const int ct = (tid - kConv0) & 255;
-        const int ra = ct >> 1, ah = ct & 1;      // weight chunk: raw row ra, 16-byte half ah
+        // weights: the warp writes its TMEM lane quarter (warp % 4); tile row
+        // m = 32 * quarter + lane, 16-byte half ah = converter warp / 4; raw
+        // row ra holds tile row m (gate/up rows interleave: m = 2i gate, 2i+1 up)
+        const int cw = ct >> 5, m = 32 * (warp & 3) + lane, ah = cw >> 2;
+        const int ra = KIND == kGU ? ((m & 1) * 64 + (m >> 1)) : m;
         const int bj = ct >> 2, bq = ct & 3;      // activation chunks: token rows bj, bj + 64, quarter bq
-        const int arow = KIND == kGU ? ((ra & 63) * 2 + (ra >> 6)) : ra;  // row in the f16 tile
         const int lch = ch == 4 ? 2 : ch == 2 ? 1 : 0;
         const int n_stages = n_my * kst;
         // activation copies run kRB stages (kRB / 2 of this group's) ahead in
@@ -330,18 +337,23 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(LayerArgs a) {
                 c_ti = ti;
                 c_npad = tile_of(a, sm, nu, nwb, b + ti * G).npad;
             }
-            // weights: 4 packed words -> 4 f16 chunks of tile row arow
-            const uint4 w = *reinterpret_cast<const uint4 *>(dyn + kOffRA + (uint32_t)rs * kARaw + ra * kARowPitch +
+            // weights: 4 packed words -> 16 f16 pairs of tile row m, to TMEM
+            const uint4 w = *reinterpret_cast<const uint4 *>(dyn + kOffRA + (uint32_t)rs * kARaw + raw_row_off(ra) +
                                                              within * 32 + ah * 16);
             if (within + 2 >= ch) {  // this group's last stage of the slot: one arrival per warp
                 __syncwarp();
                 if (lane == 0) mb_arrive(&sm.raw_empty[rs]);
             }
-            uint8_t *fa = dyn + (uint32_t)fs * kAF16;
-            *reinterpret_cast<uint4 *>(fa + sw_off(arow, ah * 4 + 0)) = w4_to_f16(w.x);
-            *reinterpret_cast<uint4 *>(fa + sw_off(arow, ah * 4 + 1)) = w4_to_f16(w.y);
-            *reinterpret_cast<uint4 *>(fa + sw_off(arow, ah * 4 + 2)) = w4_to_f16(w.z);
-            *reinterpret_cast<uint4 *>(fa + sw_off(arow, ah * 4 + 3)) = w4_to_f16(w.w);
+            {
+                const uint4 p0 = w4_to_f16(w.x), p1 = w4_to_f16(w.y), p2 = w4_to_f16(w.z), p3 = w4_to_f16(w.w);
+                const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kTmemA + (uint32_t)fs * kAcolStage +
+                                    (uint32_t)ah * 16;
+                asm volatile(
+                    "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(ta),
+                    "r"(p0.x), "r"(p0.y), "r"(p0.z), "r"(p0.w), "r"(p1.x), "r"(p1.y), "r"(p1.z), "r"(p1.w), "r"(p2.x),
+                    "r"(p2.y), "r"(p2.z), "r"(p2.w), "r"(p3.x), "r"(p3.y), "r"(p3.z), "r"(p3.w)
+                    : "memory");
+            }
             // activations: per token row 16 bytes = two 8-groups -> two f16 chunks
             uint8_t *fb = dyn + kOffB + (uint32_t)fs * kBF16;
             const uint8_t *rb = dyn + kOffRB + (uint32_t)bslot * kBRaw;
@@ -354,7 +366,9 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(LayerArgs a) {
                 *reinterpret_cast<uint4 *>(fb + sw_off(j, 2 * bq)) = make_uint4(g0a.x, g0a.y, g0b.x, g0b.y);
                 *reinterpret_cast<uint4 *>(fb + sw_off(j, 2 * bq + 1)) = make_uint4(g1a.x, g1a.y, g1b.x, g1b.y);
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // activations: to the MMA's proxy
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");    // weights: in TMEM
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
             if (lane == 0) mb_arrive(&sm.full[fs]);
             issue_b();
@@ -385,14 +399,14 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(LayerArgs a) {
                         break;
                     }
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                    const uint32_t a0 = sbase + (uint32_t)fs * kAF16, b0 = sbase + kOffB + (uint32_t)fs * kBF16;
+                    const uint32_t at = tmem + kTmemA + (uint32_t)fs * kAcolStage, b0 = sbase + kOffB + (uint32_t)fs * kBF16;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t acc = (ks | kk) != 0 ? 1u : 0u;
                         asm volatile(
                             "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-                            " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(dt),
-                            "l"(desc_sw128(a0 + kk * 32)), "l"(desc_sw128(b0 + kk * 32)), "r"(idesc), "r"(acc));
+                            " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(dt),
+                            "r"(at + kk * 8), "l"(desc_sw128(b0 + kk * 32)), "r"(idesc), "r"(acc));
                     }
                     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                                      su32(&sm.empty[fs]))
@@ -449,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(LayerArgs a) {
                 if (col < pcs) {
                     const uint8_t *src = (row < 64 ? r0p + (size_t)row * rowb : r1p + (size_t)(row - 64) * rowb) +
                                          ks0 * 32 + col * 16;
-                    cp_async16(dst + row * kARowPitch + col * 16, src, 16u);
+                    cp_async16(dst + raw_row_off(row) + col * 16, src, 16u);
                 }
             }
             cp_async_arrive(&sm.raw_full[rs]);
