@@ -246,6 +246,93 @@ __global__ void __launch_bounds__(256) router_tile_kernel(const float *__restric
     }
 }
 
+// ------------------------------------------------ large-batch router (2 kernels)
+
+// Logits of a large batch as a register-tiled fp32 GEMM: CTA tile 64 tokens x
+// 64 experts, K in chunks of 32 through shared memory (stored k-major so a
+// thread reads 4 tokens and 4 experts as two float4), 256 threads each
+// accumulating 4 tokens x 4 experts with one fmaf chain per output in
+// ascending d.  The next chunk is loaded into registers while the current
+// one is multiplied.  D % 32 == 0.
+constexpr int kRLT = 64, kRLE = 64, kRLK = 32;
+__global__ void __launch_bounds__(256) router_logits_kernel(const float *__restrict__ x, const float *__restrict__ Wr,
+                                                            int T, int D, int E, float *__restrict__ logits) {
+    __shared__ __align__(16) float xs[kRLK][kRLT + 4];
+    __shared__ __align__(16) float ws[kRLK][kRLE + 4];
+    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+    const int t0 = blockIdx.x * kRLT, e0 = blockIdx.y * kRLE;
+    // loader: 64 rows x 32 floats per operand = 512 float4, two per thread
+    const int lr = tid >> 3, lc = (tid & 7) * 4;  // rows lr and lr + 32, float columns lc..lc+3
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    auto ld = [&](const float *base, int row0, int nrows, int rstride, int r, int k0) {
+        const int row = row0 + r;
+        return row < nrows ? __ldg(reinterpret_cast<const float4 *>(base + (size_t)row * rstride + k0 + lc))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    float4 xa = ld(x, t0, T, D, lr, 0), xb = ld(x, t0, T, D, lr + 32, 0);
+    float4 wa = ld(Wr, e0, E, D, lr, 0), wb = ld(Wr, e0, E, D, lr + 32, 0);
+    for (int k0 = 0; k0 < D; k0 += kRLK) {
+        __syncthreads();
+        xs[lc + 0][lr] = xa.x; xs[lc + 1][lr] = xa.y; xs[lc + 2][lr] = xa.z; xs[lc + 3][lr] = xa.w;
+        xs[lc + 0][lr + 32] = xb.x; xs[lc + 1][lr + 32] = xb.y; xs[lc + 2][lr + 32] = xb.z; xs[lc + 3][lr + 32] = xb.w;
+        ws[lc + 0][lr] = wa.x; ws[lc + 1][lr] = wa.y; ws[lc + 2][lr] = wa.z; ws[lc + 3][lr] = wa.w;
+        ws[lc + 0][lr + 32] = wb.x; ws[lc + 1][lr + 32] = wb.y; ws[lc + 2][lr + 32] = wb.z; ws[lc + 3][lr + 32] = wb.w;
+        __syncthreads();
+        if (k0 + kRLK < D) {  // the next chunk travels while this one is multiplied
+            xa = ld(x, t0, T, D, lr, k0 + kRLK);
+            xb = ld(x, t0, T, D, lr + 32, k0 + kRLK);
+            wa = ld(Wr, e0, E, D, lr, k0 + kRLK);
+            wb = ld(Wr, e0, E, D, lr + 32, k0 + kRLK);
+        }
+#pragma unroll
+        for (int k = 0; k < kRLK; ++k) {
+            const float4 xv = *reinterpret_cast<const float4 *>(&xs[k][ty * 4]);
+            const float4 wv = *reinterpret_cast<const float4 *>(&ws[k][tx * 4]);
+            const float xr[4] = {xv.x, xv.y, xv.z, xv.w}, wr[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xr[i], wr[j], acc[i][j]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int t = t0 + ty * 4 + i;
+        if (t >= T) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int e = e0 + tx * 4 + j;
+            if (e < E) logits[(size_t)t * E + e] = acc[i][j];
+        }
+    }
+}
+
+// Top-K of a large batch from its logits: one warp per token (select_topk).
+template <int EPL>
+__global__ void __launch_bounds__(256) router_select_kernel(const float *__restrict__ logits,
+                                                            const float *__restrict__ bias, int T, int E, int K,
+                                                            float scale, int32_t *__restrict__ idx,
+                                                            float *__restrict__ w, int32_t *err) {
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (t >= T) return;
+    float c[EPL], p[EPL];
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) {
+        const int e = lane + 32 * j;
+        if (e < E) {
+            score(__ldg(logits + (size_t)t * E + e), __ldg(bias + e), p[j], c[j]);
+        } else {
+            p[j] = 0.f;
+            c[j] = -INFINITY;
+        }
+    }
+    select_topk<EPL>(c, p, E, K, scale, idx + (size_t)t * K, w + (size_t)t * K, nullptr, err);
+}
+
 // ------------------------------------------------- large-batch permute
 
 // One CTA of 1024 threads.  Stable counting sort of the T*K selections by
@@ -358,6 +445,27 @@ cudaError_t launch_router_tile(const float *x, const float *Wr, const float *bia
         case 4: return launch_tile_t<4>(x, Wr, bias, T, D, E, K, scale, idx, w, err, s);
         case 8: return launch_tile_t<8>(x, Wr, bias, T, D, E, K, scale, idx, w, err, s);
         default: return launch_tile_t<16>(x, Wr, bias, T, D, E, K, scale, idx, w, err, s);
+    }
+}
+
+template <int EPL>
+static cudaError_t launch_select_t(const float *logits, const float *bias, int T, int E, int K, float scale,
+                                   int32_t *idx, float *w, int32_t *err, cudaStream_t s) {
+    router_select_kernel<EPL><<<(T + 7) / 8, 256, 0, s>>>(logits, bias, T, E, K, scale, idx, w, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_router_gemm(const float *x, const float *Wr, const float *bias, int T, int D, int E, int K,
+                               float scale, float *logits, int32_t *idx, float *w, int32_t *err, cudaStream_t s) {
+    router_logits_kernel<<<dim3((T + kRLT - 1) / kRLT, (E + kRLE - 1) / kRLE), 256, 0, s>>>(x, Wr, T, D, E, logits);
+    cudaError_t ce = cudaGetLastError();
+    if (ce != cudaSuccess) return ce;
+    switch (epl_for(E)) {
+        case 1: return launch_select_t<1>(logits, bias, T, E, K, scale, idx, w, err, s);
+        case 2: return launch_select_t<2>(logits, bias, T, E, K, scale, idx, w, err, s);
+        case 4: return launch_select_t<4>(logits, bias, T, E, K, scale, idx, w, err, s);
+        case 8: return launch_select_t<8>(logits, bias, T, E, K, scale, idx, w, err, s);
+        default: return launch_select_t<16>(logits, bias, T, E, K, scale, idx, w, err, s);
     }
 }
 

@@ -16,7 +16,7 @@ struct LayerArgs {
     int8_t *xq;          // [Tmax, D] int8, even/odd permuted 8-groups
     float *sx;           // [Tmax]
     int32_t *xsum;       // [Tmax] sum of xq over the row
-    float *logits;       // [kSmallT, E]
+    float *logits;       // [max(kSmallT, Tmax), E]
     int32_t *idx;        // [Tmax, K]
     float *wts;          // [Tmax, K]
     int32_t *rows;       // [Tmax * S] entry ids (t*S + slot) grouped by union expert
@@ -51,6 +51,10 @@ cudaError_t launch_router_tile(const float *x, const float *Wr, const float *bia
                                int E, int K, float scale, int32_t *idx, float *w, int32_t *err,
                                cudaStream_t s);
 cudaError_t launch_permute(const LayerArgs &a, cudaStream_t s);
+// Large-batch router through a logits buffer [T, E]: tiled fp32 GEMM, then
+// one warp per token for the top-K.
+cudaError_t launch_router_gemm(const float *x, const float *Wr, const float *bias, int T, int D, int E, int K,
+                               float scale, float *logits, int32_t *idx, float *w, int32_t *err, cudaStream_t s);
 cudaError_t launch_gateup(const LayerArgs &a, int mch, int grid, cudaStream_t s);
 cudaError_t launch_down(const LayerArgs &a, int mch, int grid, bool fused_reduce, cudaStream_t s);
 cudaError_t launch_reduce(const LayerArgs &a, cudaStream_t s);

@@ -89,7 +89,7 @@ size_t layout(const MoeLayerDesc &d, Handle *h) {
     const size_t o_xq = take(T * D);
     const size_t o_sx = take(4 * T);
     const size_t o_xsum = take(4 * T);
-    const size_t o_logits = take(4 * moe::kSmallT * E);
+    const size_t o_logits = take(4 * (T > (size_t)moe::kSmallT ? T : (size_t)moe::kSmallT) * E);
     const size_t o_idx = take(4 * T * K);
     const size_t o_wts = take(4 * T * K);
     const size_t o_rows = take(4 * T * S);
@@ -233,8 +233,8 @@ int run_layer(Handle *h, const float *x, int T, float *out, const float *resid, 
         if ((ce = moe::launch_router_small(a, s)) != cudaSuccess) return cuda_fail(ce, "router_small launch");
     } else {
         if ((ce = moe::launch_quant_perm(a, s)) != cudaSuccess) return cuda_fail(ce, "quant launch");
-        if ((ce = moe::launch_router_tile(x, h->Wr, h->bias, T, a.D, a.E, a.K, a.routed_scale, h->idx, h->wts,
-                                          h->err, s)) != cudaSuccess)
+        if ((ce = moe::launch_router_gemm(x, h->Wr, h->bias, T, a.D, a.E, a.K, a.routed_scale, h->logits, h->idx,
+                                          h->wts, h->err, s)) != cudaSuccess)
             return cuda_fail(ce, "router_tile launch");
         if ((ce = moe::launch_permute(a, s)) != cudaSuccess) return cuda_fail(ce, "permute launch");
     }
