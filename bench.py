@@ -54,12 +54,16 @@ DEFAULT_WORKLOAD = "glm_moe_layer_decode_b1"
 # (HBM-bound); larger batches run the grouped GEMM (tensor-pipe bound).
 HOT_KERNEL_DECODE = "stream_kernel<0> (fused int4 gate/up, SiLU*up, max abs h)"
 HOT_KERNEL_SINGLE = "decode_layer_kernel (the whole layer as one persistent kernel)"
-HOT_KERNEL_PREFILL = "grouped_gemm_kernel<0> (int4 x int8 gate/up GEMM, SiLU*up, max abs h)"
+HOT_KERNEL_PREFILL = "umma_gemm_kernel<0> (tcgen05 f16-exact gate/up GEMM, SiLU*up, max abs h)"
 # DRAM bytes (read + write) per launch of the dominant kernel from one ncu
 # capture of the current kernel source, or None.  Keyed by workload.
 TRAFFIC = {
-    # profiles/grouped_gemm_prefill_2048.md: 1.99 GB read + 0.14 GB written
-    "glm_moe_layer_prefill_2048": 2.131e9,
+    # profiles/launches_glm_moe_layer_decode_b1.md: decode_layer_kernel on the
+    # full workload, 176.7 MB read + 0.37 MB written per launch
+    "glm_moe_layer_decode_b1": 177.1e6,
+    # profiles/umma_gemm_prefill_2048.md: umma_gemm_kernel<0> (gate/up),
+    # 2.51 GB read + 0.13 GB written
+    "glm_moe_layer_prefill_2048": 2.642e9,
 }
 
 
