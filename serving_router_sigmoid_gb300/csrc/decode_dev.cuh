@@ -39,6 +39,8 @@
 // counters for the next launch.
 #pragma once
 
+#include <type_traits>
+
 #include "route_dev.cuh"
 #include "stream_dev.cuh"
 
@@ -100,6 +102,7 @@ struct DecodeSmem {
     int nu;                           // routed union entries
     int nblk;                         // reduce blocks this CTA completed
     int last;                         // this CTA finished last
+    int slice[4];                     // this CTA's routed gate/up and down group ranges
     int blk_list[kMaxRedBlk];          // reduce blocks this CTA completed
     int ncontrib;                      // (block, rows) contributions listed
     int2 contrib[kMaxContrib];
@@ -246,15 +249,19 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, DecodeSmem &sm,
 
         const int g_end = min(p1, (ue + 1) * gpe);  // groups of entry ue end here
         auto in_seg = [&](int jj) { return jj < n_my && p0 + warp + 8 * (jj / UPG) < g_end; };
-        auto process = [&](const UnitRegs<KIND, CPL> &R, int jj) {
+        // the loops are compiled for MM token rows: 1, 2 or the batch's
+        // widest entry, the smallest that holds this entry's M (an expert
+        // that one or two tokens chose does not pay for the widest entry)
+        auto process = [&](auto mm, const UnitRegs<KIND, CPL> &R, int jj) {
+            constexpr int MM = decltype(mm)::value;
             const int p = p0 + warp + 8 * (jj / UPG);
             const int o0 = (p - ue * gpe) * RPG;
             if (KIND == kGateUp) {
-                int acc[MCH];
+                int acc[MM];
 #pragma unroll
-                for (int m = 0; m < MCH; ++m) acc[m] = 0;
-                dot_rows<CPL, MCH>(acc, R.w[0], xs, kdim, M, nch, lane);
-                const int mine = lane_sum<MCH>(acc, M, lane);
+                for (int m = 0; m < MM; ++m) acc[m] = 0;
+                dot_rows<CPL, MM>(acc, R.w[0], xs, kdim, M, nch, lane);
+                const int mine = lane_sum<MM>(acc, M, lane);
                 if (jj % UPG == 0) {
                     held_g = mine;
                     held_gs = R.s[0];
@@ -271,11 +278,11 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, DecodeSmem &sm,
             } else {
 #pragma unroll
                 for (int rr = 0; rr < RPG; ++rr) {
-                    int acc[MCH];
+                    int acc[MM];
 #pragma unroll
-                    for (int m = 0; m < MCH; ++m) acc[m] = 0;
-                    dot_rows<CPL, MCH>(acc, R.w[rr], xs, kdim, M, nch, lane);
-                    const int mine = lane_sum<MCH>(acc, M, lane);
+                    for (int m = 0; m < MM; ++m) acc[m] = 0;
+                    dot_rows<CPL, MM>(acc, R.w[rr], xs, kdim, M, nch, lane);
+                    const int mine = lane_sum<MM>(acc, M, lane);
                     if (lane < M) {
                         const int o = o0 + rr;
                         const int di = mine - 8 * hsum;
@@ -288,21 +295,58 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, DecodeSmem &sm,
         };
         // X holds unit j, Y unit j + 1; each processed set is refilled with
         // the unit two ahead.  Returns true when the next unit is in Y.
-        auto run = [&](UnitRegs<KIND, CPL> &X, UnitRegs<KIND, CPL> &Y) -> bool {
+        auto run = [&](auto mm, UnitRegs<KIND, CPL> &X, UnitRegs<KIND, CPL> &Y) -> bool {
             while (in_seg(j)) {
-                process(X, j);
+                process(mm, X, j);
                 request<KIND, CPL>(X, a, uexp, gpe, p0, n_my, j + 2, ex_u, ex);
                 ++j;
                 if (!in_seg(j)) return true;
-                process(Y, j);
+                process(mm, Y, j);
                 request<KIND, CPL>(Y, a, uexp, gpe, p0, n_my, j + 2, ex_u, ex);
                 ++j;
             }
             return false;
         };
-        flip = flip ? !run(B, A) : run(A, B);
+        auto run_m = [&](UnitRegs<KIND, CPL> &X, UnitRegs<KIND, CPL> &Y) -> bool {
+            using C1 = std::integral_constant<int, 1>;
+            using C2 = std::integral_constant<int, MCH < 2 ? MCH : 2>;
+            using CW = std::integral_constant<int, MCH>;
+            if (MCH == 1 || M <= 1) return run(C1{}, X, Y);
+            if (MCH == 2 || M <= 2) return run(C2{}, X, Y);
+            return run(CW{}, X, Y);
+        };
+        flip = flip ? !run_m(B, A) : run_m(A, B);
     }
     if (KIND == kGateUp && lane < M) atomicMax(a.dham + r0 + lane, __float_as_uint(amax_run));
+}
+
+// Contiguous slices of the row groups of entries [0, n) (gpe groups each)
+// weighted by cost: a group of an entry costs 2 + the token width its loops
+// are compiled for (1, 2 or the batch's widest, see stream_phase): the weight
+// stream plus that many token rows of dot products.  CTA b gets the groups
+// whose cumulative cost falls in [b W / G, (b+1) W / G); every CTA evaluates
+// the same monotone map, so the slices tile the groups exactly.
+template <int MCH>
+__device__ __forceinline__ long long group_cost(const int *ubeg, int u) {
+    const int M = ubeg[u + 1] - ubeg[u];
+    return 2 + (M <= 1 ? 1 : M <= 2 ? 2 : MCH);
+}
+template <int MCH>
+__device__ __forceinline__ int group_at_cost(const int *ubeg, int n, int gpe, long long c) {
+    long long pre = 0;
+    for (int u = 0; u < n; ++u) {
+        const long long w = group_cost<MCH>(ubeg, u), span = (long long)gpe * w;
+        if (c < pre + span) return u * gpe + (int)((c - pre) / w);
+        pre += span;
+    }
+    return n * gpe;
+}
+template <int MCH>
+__device__ __forceinline__ void cost_slice(const int *ubeg, int n, int gpe, int b, int G, int &p0, int &p1) {
+    long long W = 0;
+    for (int u = 0; u < n; ++u) W += (long long)gpe * group_cost<MCH>(ubeg, u);
+    p0 = group_at_cost<MCH>(ubeg, n, gpe, (long long)b * W / G);
+    p1 = group_at_cost<MCH>(ubeg, n, gpe, (long long)(b + 1) * W / G);
 }
 
 // The union tables of the batch from its T*K selections in sm.idx ((token,
@@ -463,19 +507,34 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
         }
     }
 
-    // routed experts' gate/up: contiguous slices of (entry, row pair)
-    const long long Nr = (long long)n_r * I;
-    const int rp0 = (int)(b * Nr / G), rp1 = (int)((b + 1) * Nr / G);
+    // routed experts' gate/up and all entries' down: cost-weighted
+    // contiguous slices of (entry, row group)
+    constexpr int RPD = UnitShape<kDown, CPLD>::kRows;  // down rows per group
+    const int gpd = D / RPD;
+    int rp0, rp1, dp0, dp1;
+    if (MCH == 1) {  // one token: every group costs the same, an even split
+        const long long Nr = (long long)n_r * I, Nd = (long long)n_u * gpd;
+        rp0 = (int)(b * Nr / G);
+        rp1 = (int)((b + 1) * Nr / G);
+        dp0 = (int)(b * Nd / G);
+        dp1 = (int)((b + 1) * Nd / G);
+    } else {
+        if (tid == 0) {
+            cost_slice<MCH>(sm.ubeg, n_r, I, b, G, sm.slice[0], sm.slice[1]);
+            cost_slice<MCH>(sm.ubeg, n_u, gpd, b, G, sm.slice[2], sm.slice[3]);
+        }
+        __syncthreads();
+        rp0 = sm.slice[0];
+        rp1 = sm.slice[1];
+        dp0 = sm.slice[2];
+        dp1 = sm.slice[3];
+    }
     prime<kGateUp, CPLG>(A, B, a, sm.uexp, I, rp0, rp1, ex_u, ex);
     stream_phase<kGateUp, CPLG, MCH>(a, sm, xs, sm.uexp, sm.ubeg, rp0, rp1, A, B, ex_u, ex);
     stamp(a, 6);
 
     // ---- phase 3: the first down rows are requested, then every CTA waits
     // for every h row and max|h|
-    constexpr int RPD = UnitShape<kDown, CPLD>::kRows;  // down rows per group
-    const int gpd = D / RPD;
-    const long long Nd = (long long)n_u * gpd;
-    const int dp0 = (int)(b * Nd / G), dp1 = (int)((b + 1) * Nd / G);
     UnitRegs<kDown, CPLD> A2, B2;
     prime<kDown, CPLD>(A2, B2, a, sm.uexp, gpd, dp0, dp1, ex_u, ex);
     cta_arrive(&sy->gu_cnt);
