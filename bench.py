@@ -280,7 +280,10 @@ def run_ours(args, cfg, stack, rank, world, local):
         torch.cuda.synchronize()
         probe_id = {"gateup": moe.MOE_PROBE_GATE_UP, "down": moe.MOE_PROBE_DOWN,
                     "router": moe.MOE_PROBE_ROUTER}[args.probe]
-        if not stack:
+        # the single-kernel layer is the whole step: the step time is its
+        # launch time, and no probe events sit between its launches
+        use_probe = stack or not single
+        if not stack and use_probe:
             for l, layer in enumerate(layers):
                 layer.set_probe(probe_id, *probes[l])
         if use_graph:
@@ -330,14 +333,15 @@ def run_ours(args, cfg, stack, rank, world, local):
         ev0.record(s)
         for i in range(K):
             launch(w_done + i)
-            if i >= 1:
+            if i >= 1 and use_probe:
                 b, e = probes[(w_done + i - 1) % n_graph]
                 e.synchronize()
                 probe_ms.append(b.elapsed_time(e))
         ev1.record(s)
     torch.cuda.synchronize()
-    b, e = probes[(w_done + K - 1) % n_graph]
-    probe_ms.append(b.elapsed_time(e))
+    if use_probe:
+        b, e = probes[(w_done + K - 1) % n_graph]
+        probe_ms.append(b.elapsed_time(e))
     clocks.mark_off()
     if world > 1:
         torch.distributed.barrier()
@@ -358,7 +362,10 @@ def run_ours(args, cfg, stack, rank, world, local):
     gu_bytes = u1_mean * gateup_bytes_per_expert(cfg) + T * cfg.D + T * cfg.S * cfg.I * 4
     step_bytes_layer = u1_mean * layer_bytes_per_expert(cfg) + cfg.E * cfg.D * 4 + cfg.E * 4 + 2 * T * cfg.D * 4
     step_bytes = step_bytes_layer * (len(layers) if stack else 1)
-    probe_avg_ms = sum(probe_ms) / len(probe_ms)
+    if use_probe:
+        probe_avg_ms, launches_timed = sum(probe_ms) / len(probe_ms), len(probe_ms)
+    else:  # back-to-back launches of the one kernel: the gaps between them count
+        probe_avg_ms, launches_timed = ms_per_step, K
     grouped = T > 16
     if single:
         # one kernel is the whole layer: its algorithmic bytes are the step's
@@ -367,17 +374,17 @@ def run_ours(args, cfg, stack, rank, world, local):
         roof = {"bound": "hbm", "kernel": HOT_KERNEL_SINGLE, "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_kind": peak_kind + " HBM copy bandwidth",
                 "traffic": TRAFFIC.get(args.workload), "algorithmic_bytes_per_launch": step_bytes_layer,
-                "avg_launch_ms": probe_avg_ms, "launches_timed": len(probe_ms)}
+                "avg_launch_ms": probe_avg_ms, "launches_timed": launches_timed}
     elif args.probe != "gateup":
         roof = {"bound": "hbm", "kernel": args.probe, "achieved": None, "peak": None, "unit": "GB/s",
-                "frac": None, "traffic": None, "avg_launch_ms": probe_avg_ms, "launches_timed": len(probe_ms)}
+                "frac": None, "traffic": None, "avg_launch_ms": probe_avg_ms, "launches_timed": launches_timed}
     elif not grouped:
         peak, peak_kind = measured_peak("hbm_gbs")
         achieved = gu_bytes / (probe_avg_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "kernel": HOT_KERNEL_DECODE, "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_kind": peak_kind + " HBM copy bandwidth",
                 "traffic": TRAFFIC.get(args.workload), "algorithmic_bytes_per_launch": gu_bytes,
-                "avg_launch_ms": probe_avg_ms, "launches_timed": len(probe_ms)}
+                "avg_launch_ms": probe_avg_ms, "launches_timed": launches_timed}
     else:
         # int8 ops of the gate/up GEMM: every routed (token, expert) pair and
         # every token through the shared expert, 2 ops per multiply-add
@@ -390,7 +397,7 @@ def run_ours(args, cfg, stack, rank, world, local):
                 "peak_kind": peak_kind + " dense bf16 (sustained); sm_103a has no int8 tcgen05 kind, so the "
                              "densest tensor rate for these operands is the 16-bit one",
                 "traffic": TRAFFIC.get(args.workload), "algorithmic_ops_per_launch": ops,
-                "avg_launch_ms": probe_avg_ms, "launches_timed": len(probe_ms)}
+                "avg_launch_ms": probe_avg_ms, "launches_timed": launches_timed}
 
     # end to end through the C ABI: pinned host x -> device, forward, out -> pinned host
     e2e = None

@@ -415,8 +415,12 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
     // ---- phase 1.  The router rows go first (everything downstream waits on
     // the logits), then the first rows of the shared expert, which need no
     // routing.
-    WrRegs<CPLG, MCH == 1> wr;  // D <= 1024 * CPLG
-    if (b < E) logits_request(wr, a.Wr + (size_t)b * D, a.x, D);
+    WrRegs<CPLG, MCH == 1> wr;  // D <= 1024 * CPLG; at one token also token 0's activations
+    if (b < E) {
+        logits_request(wr, a.Wr + (size_t)b * D, a.x, D);
+    } else {
+        if constexpr (MCH == 1) x0_request(wr, a.x, D);
+    }
     int ex_u = -1;
     DevExpert ex{};
     UnitRegs<kGateUp, CPLG> A, B;
@@ -438,23 +442,23 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
     }
     stamp(a, 1);
 
-    // quantiser: the last T CTAs, one token each (the global rows are the
-    // tokens of the staged tiles for T > 1, and the debug outputs).  At one
-    // token every CTA also quantises token 0 into its own tile.
+    // quantiser.  At one token every CTA quantises token 0 into its own tile
+    // from the registers the router loads left (the last CTA also writes the
+    // global row: the debug outputs).  Else the last T CTAs, one token each,
+    // write the global rows the staged tiles are read from.
     const int tq = G - 1 - b;
-    if (MCH == 1) {
-        quant_token_perm(a.x, D, tq == 0 ? a.xq : nullptr, tq == 0 ? a.sx : nullptr, tq == 0 ? a.xsum : nullptr,
-                         tq == 0 ? a.dbg.xq : nullptr, xs, &sm.sx[0], &sm.xsum[0]);
+    if constexpr (MCH == 1) {
+        quant_x0_tile(wr, D, xs, &sm.sx[0], &sm.xsum[0], tq == 0 ? a.xq : nullptr, tq == 0 ? a.sx : nullptr,
+                      tq == 0 ? a.xsum : nullptr, tq == 0 ? a.dbg.xq : nullptr);
     } else if (tq < T) {
         quant_token_perm(a.x + (size_t)tq * D, D, a.xq + (size_t)tq * D, a.sx + tq, a.xsum + tq,
                          a.dbg.xq ? a.dbg.xq + (size_t)tq * D : nullptr);
         cta_arrive(&sy->quant_cnt);
     }
 
-    // top-K: the quantiser CTA of token tq selects that token's experts
-    // (topk_small_cta, the routine of the four-kernel router) as soon as its
-    // logits are in, and publishes them as data, while the other CTAs stream
-    // the shared expert
+    // top-K: CTA G-1-t selects token t's experts (topk_small_cta, the
+    // routine of the four-kernel router) as soon as its logits are in, and
+    // publishes them as data, while the other CTAs stream the shared expert
     if (tq < T)
         topk_small_cta<true>(a.dlog + (size_t)tq * E, a.bias, 1, E, K, a.routed_scale, nullptr, nullptr,
                              a.dsel + (size_t)tq * K, a.err, sm.tk, sm.tkp);
@@ -533,11 +537,12 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
     stream_phase<kGateUp, CPLG, MCH>(a, sm, xs, sm.uexp, sm.ubeg, rp0, rp1, A, B, ex_u, ex);
     stamp(a, 6);
 
-    // ---- phase 3: the first down rows are requested, then every CTA waits
-    // for every h row and max|h|
+    // ---- phase 3: the CTA arrives, requests its first down rows, then
+    // waits for every h row and max|h| (arrival first: its fence would
+    // otherwise wait for these loads too)
+    cta_arrive(&sy->gu_cnt);
     UnitRegs<kDown, CPLD> A2, B2;
     prime<kDown, CPLD>(A2, B2, a, sm.uexp, gpd, dp0, dp1, ex_u, ex);
-    cta_arrive(&sy->gu_cnt);
     cta_wait(&sy->gu_cnt, G, a.err);
     stamp(a, 7);
     stream_phase<kDown, CPLD, MCH>(a, sm, xs, sm.uexp, sm.ubeg, dp0, dp1, A2, B2, ex_u, ex);

@@ -366,6 +366,77 @@ __device__ __forceinline__ float logits_finish(const WrRegs<NW, X0> &r, const fl
     return l;
 }
 
+// Loads only token 0's activations into r.x0, in logits_request's layout (for
+// a CTA that computes no logit but quantises token 0 from registers).
+template <int NW>
+__device__ __forceinline__ void x0_request(WrRegs<NW, true> &r, const float *__restrict__ x, int D) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int L8 = D >> 5;
+    const float4 *xr = reinterpret_cast<const float4 *>(x) + warp * L8;
+#pragma unroll
+    for (int j = 0; j < NW; ++j) {
+        const int c = j * 32 + lane;
+        r.x0[j] = c < L8 ? __ldg(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+// Token 0 quantised from the registers of logits_request / x0_request, with
+// the arithmetic of quant_token_perm (absmax / 127 scale, round to nearest
+// even; the max and the integer code sum do not depend on the order), into
+// the two-plane tile with its scale and code sum; xq_row / sx_out / xsum_out
+// / nat_row (each may be null) receive the global rows.  Thread (w, lane)
+// holds float4 number w * D/32 + 32 j + lane of the row: elements 4f..4f+3,
+// the low or high half of 8-group f/2, i.e. two bytes of its even word and
+// two of its odd word in the permuted layout.  All threads call it.
+template <int NW>
+__device__ __forceinline__ void quant_x0_tile(const WrRegs<NW, true> &r, int D, int8_t *tile, float *tile_sx,
+                                              int *tile_xsum, int8_t *xq_row, float *sx_out, int32_t *xsum_out,
+                                              int8_t *nat_row) {
+    __shared__ float red_f[32];
+    __shared__ int red_i[32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int L8 = D >> 5;
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < NW; ++j) {
+        const float4 v = r.x0[j];  // zero beyond the row
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+    amax = block_max_nonneg(amax, red_f);
+    float s, inv;
+    act_scale(amax, s, inv);
+    int sum = 0;
+#pragma unroll
+    for (int j = 0; j < NW; ++j) {
+        const int c = j * 32 + lane;
+        if (c >= L8) continue;
+        const int f = warp * L8 + c;
+        const float4 v = r.x0[j];
+        const int q0 = quant_i8(v.x, inv), q1 = quant_i8(v.y, inv), q2 = quant_i8(v.z, inv),
+                  q3 = quant_i8(v.w, inv);
+        sum += q0 + q1 + q2 + q3;
+        const int byte = 8 * (f >> 1) + 2 * (f & 1);  // even half-word; the odd one 4 bytes on
+        const uint16_t ev = (uint16_t)((q0 & 255) | ((q2 & 255) << 8));
+        const uint16_t od = (uint16_t)((q1 & 255) | ((q3 & 255) << 8));
+        *reinterpret_cast<uint16_t *>(plane_byte(tile, D, 0, byte)) = ev;
+        *reinterpret_cast<uint16_t *>(plane_byte(tile, D, 0, byte + 4)) = od;
+        if (xq_row) {
+            *reinterpret_cast<uint16_t *>(xq_row + byte) = ev;
+            *reinterpret_cast<uint16_t *>(xq_row + byte + 4) = od;
+        }
+        if (nat_row)
+            *reinterpret_cast<uint32_t *>(nat_row + 4 * f) =
+                (q0 & 255) | ((q1 & 255) << 8) | ((q2 & 255) << 16) | ((uint32_t)(q3 & 255) << 24);
+    }
+    sum = block_sum_i(sum, red_i);
+    if (threadIdx.x == 0) {
+        *tile_sx = s;
+        *tile_xsum = sum;
+        if (sx_out) *sx_out = s;
+        if (xsum_out) *xsum_out = sum;
+    }
+}
+
 __device__ __forceinline__ float expert_logits_cta(const float *__restrict__ wrow, const float *__restrict__ x,
                                                    int T, int D, float (*red)[kSmallT]) {
     WrRegs<kMaxDim / 1024, false> r;
