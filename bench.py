@@ -297,13 +297,29 @@ def run_ours(args, cfg, stack, rank, world, local):
         elif stack:
             layers[0].set_probe(probe_id, *probes[0])
             n_graph = 1
+        # without probes, runs of n_layers consecutive steps are also captured
+        # in one graph, as a serving engine captures a model's layers: the
+        # steps then follow each other without a graph launch in between
+        run_graph = None
+        if use_graph and not use_probe and n_layers > 1:
+            run_graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(run_graph, stream=s):
+                for i in range(n_layers):
+                    step_fn(i)
         torch.cuda.synchronize()
 
-    def launch(i):
+    def launch(i, left=1):
+        """Issues step i (and, through the run graph, the steps after it
+        when a whole run starts at i and fits in `left`); returns the number
+        of steps issued."""
+        if run_graph is not None and i % n_layers == 0 and left >= n_layers:
+            run_graph.replay()
+            return n_layers
         if use_graph:
             graphs[i % n_graph].replay()
         else:
             step_fn(i)
+        return 1
 
     kernels_per_forward = (1 if single else 4 if T <= 16 else 7) + (1 if stack else 0)
     launches_per_step = kernels_per_forward * (len(layers) if stack else 1)
@@ -315,10 +331,11 @@ def run_ours(args, cfg, stack, rank, world, local):
     w_done = 0
     t0 = time.time()
     with torch.cuda.stream(s):
+        n_sync = 0
         while w_done < args.warmup or time.time() - t0 < 0.5:
-            launch(w_done)
-            w_done += 1
-            if w_done % 64 == 0:
+            w_done += launch(w_done, 1 << 30)
+            if w_done >= n_sync + 64:
+                n_sync = w_done
                 s.synchronize()
         s.synchronize()
 
@@ -331,10 +348,11 @@ def run_ours(args, cfg, stack, rank, world, local):
     clocks.mark_on()
     with torch.cuda.stream(s):
         ev0.record(s)
-        for i in range(K):
-            launch(w_done + i)
-            if i >= 1 and use_probe:
-                b, e = probes[(w_done + i - 1) % n_graph]
+        i = 0
+        while i < K:
+            i += launch(w_done + i, K - i)
+            if i >= 2 and use_probe:
+                b, e = probes[(w_done + i - 2) % n_graph]
                 e.synchronize()
                 probe_ms.append(b.elapsed_time(e))
         ev1.record(s)
@@ -454,7 +472,8 @@ def run_ours(args, cfg, stack, rank, world, local):
                    "top_k": cfg.K, "shared_experts": cfg.n_shared, "tokens_per_step": T,
                    "layers_per_step": len(layers) if stack else 1, "layer_sets_cycled": n_layers,
                    "routed_scale": cfg.routed_scale, "zipf_skew": cfg.skew,
-                   "experts_streamed_per_layer": u1_mean, "cuda_graph": use_graph, "light": args.light,
+                   "experts_streamed_per_layer": u1_mean, "cuda_graph": use_graph,
+                   "steps_per_graph": n_layers if run_graph is not None else 1, "light": args.light,
                    "decode_plan": ("single persistent kernel" if single else "four kernels") if T <= 16 else None,
                    "l2": ("inputs larger than L2: the steps cycle %d resident layer weight sets "
                           "(%.2f GB between reuses of a set)" % (n_layers, (n_layers - 1) * step_bytes_layer / 1e9))

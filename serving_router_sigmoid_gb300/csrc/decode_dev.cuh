@@ -520,8 +520,19 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
         const long long Nr = (long long)n_r * I, Nd = (long long)n_u * gpd;
         rp0 = (int)(b * Nr / G);
         rp1 = (int)((b + 1) * Nr / G);
-        dp0 = (int)(b * Nd / G);
-        dp1 = (int)((b + 1) * Nd / G);
+        if (G >= n_u) {
+            // down: the CTAs split into one run per entry (entry u gets CTAs
+            // [u G / n_u, (u+1) G / n_u)), so that no CTA stages the h of two
+            // entries; each run splits its entry's groups evenly
+            const int u = (int)(((long long)b * n_u + n_u - 1) / G);  // first u with (u+1) G / n_u > b
+            const int c0 = (int)((long long)u * G / n_u), c1 = (int)((long long)(u + 1) * G / n_u);
+            const int j = b - c0, c = c1 - c0;
+            dp0 = u * gpd + (int)((long long)j * gpd / c);
+            dp1 = u * gpd + (int)((long long)(j + 1) * gpd / c);
+        } else {
+            dp0 = (int)(b * Nd / G);
+            dp1 = (int)((b + 1) * Nd / G);
+        }
     } else {
         if (tid == 0) {
             cost_slice<MCH>(sm.ubeg, n_r, I, b, G, sm.slice[0], sm.slice[1]);
