@@ -16,23 +16,27 @@
 // whole layer is one cooperative launch with every CTA resident (2 per SM),
 // moving through three phases that hand data over through L2:
 //   1. CTA b < E computes the logits of experts b, b + G, ... (its router
-//      row is requested first: everything downstream waits on the logits);
-//      the last T CTAs quantise one token each.  Every CTA then requests the
+//      row is requested first: everything downstream waits on the logits)
+//      and publishes each as data (the slot itself is the flag).  At one
+//      token every CTA quantises the token into its own tile from the
+//      registers the router loads brought; for T > 1 the last T CTAs
+//      quantise one token each (arrival counter).  Every CTA requests the
 //      first rows of its slice of the shared expert's gate/up, which needs
-//      no routing, and streams that slice as soon as the quantised tokens
-//      are in (arrival counter).  Meanwhile the quantiser CTA of each token,
-//      once all logits have landed (arrival counter), selects that token's
-//      top-K and publishes it (arrival counter).
-//   2. Every CTA reads the published selections and builds the union tables
-//      itself, in shared memory; then it streams its contiguous slice of the
-//      routed experts' gate/up rows (h and max|h| to L2).
-//   3. A grid-wide arrival barrier; each CTA requests its first down rows
-//      before waiting.  The CTA requantises the h rows of the experts in its
-//      slice and streams their down rows into per-slot partial outputs.  An
-//      arrival counter per block of 64 output rows sums the rows written; the
-//      CTA that completes a block adds that block's slots in the fixed slot
-//      order (shared expert last), so the result does not depend on which
-//      CTA arrives when.
+//      no routing, and streams that slice once the tokens are quantised.
+//      Meanwhile CTA G-1-t polls token t's logits, selects its top-K and
+//      publishes the selections as data.
+//   2. Every CTA polls the published selections and builds the union
+//      tables itself, in shared memory; then it streams its contiguous
+//      slice of the routed experts' gate/up rows (h to L2).
+//   3. A grid-wide arrival barrier; each CTA arrives, then requests its
+//      first down rows, then waits.  The CTA stages the h rows of the
+//      entries in its slice (max|h| of each row by a block reduction of the
+//      loaded values, then the int8 codes) and streams their down rows into
+//      per-slot partial outputs; at one token the CTAs form one run per
+//      union entry.  An arrival counter per block of 64 output rows sums the
+//      rows written; the CTA that completes a block adds that block's slots
+//      in the fixed slot order (shared expert last), so the result does not
+//      depend on which CTA arrives when.
 // Every wait is bounded (one second of %globaltimer): on time-out the kernel
 // sets kErrSyncTimeout in the error word and runs on to its end, so nothing
 // hangs and the stream stays usable.  The last CTA to finish clears the
@@ -177,7 +181,6 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, DecodeSmem &sm,
     const int gpe = rows_out / RPG;
     const int n_my = units_of_warp<KIND>(p0, p1, warp);
 
-    float amax_run = 0.f;  // lane m: max|h| of token row m of the staged entry (gate/up)
     int hsum = 0;          // lane m: code sum of the requantised h row m (down)
     int held_g = 0;        // lane m: gate sum waiting for its up row
     float held_gs = 0.f;   // that gate row's scale
@@ -185,7 +188,6 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, DecodeSmem &sm,
     bool flip = false;     // the next unit is in B
     const int ua = p0 / gpe, ub = (p1 - 1) / gpe;
     for (int ue = ua; ue <= ub; ++ue) {
-        if (KIND == kGateUp && ue > ua && lane < M) atomicMax(a.dham + r0 + lane, __float_as_uint(amax_run));
         __syncthreads();
         r0 = ubeg[ue];
         M = ubeg[ue + 1] - r0;
@@ -210,20 +212,33 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, DecodeSmem &sm,
                     __ldcg(reinterpret_cast<const int4 *>(a.xq + (size_t)(sm.ent[m] / S) * kdim) + c);
             }
         } else {
-            const int n8 = kdim >> 3;
+            // the entry's h rows, one 8-group per thread (the down chunk
+            // counts instantiated give I <= 2048 = 8 * blockDim): max|h| of
+            // the row by a block reduction of the loaded values, then the
+            // scale, the codes and their sum
+            static_assert(KIND != kDown || CPL <= 2, "one 8-group of an h row per thread");
+            const int n8 = kdim >> 3, gi = threadIdx.x;
             const bool first_block = p0 <= ue * gpe;  // this CTA owns the entry's first rows
             for (int m = 0; m < M; ++m) {
-                float s, inv;
-                act_scale(__uint_as_float(__ldcg(a.dham + r0 + m)), s, inv);
-                if (threadIdx.x == 0) sm.sx[m] = s;
-                int sum = 0;
-                for (int gi = threadIdx.x; gi < n8; gi += blockDim.x) {
+                float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
+                if (gi < n8) {
                     const float *hp = a.h + (size_t)(r0 + m) * kdim + 8 * gi;
-                    const float4 v0 = ld_cg_f4(hp), v1 = ld_cg_f4(hp + 4);
+                    v0 = ld_cg_f4(hp);
+                    v1 = ld_cg_f4(hp + 4);
+                }
+                float amax = fmaxf(fmaxf(fmaxf(fabsf(v0.x), fabsf(v0.y)), fmaxf(fabsf(v0.z), fabsf(v0.w))),
+                                   fmaxf(fmaxf(fabsf(v1.x), fabsf(v1.y)), fmaxf(fabsf(v1.z), fabsf(v1.w))));
+                amax = block_max_nonneg(amax, &sm.red[0][0]);
+                float s, inv;
+                act_scale(amax, s, inv);
+                if (threadIdx.x == 0) sm.sx[m] = s;
+                if (a.dbg.sh && first_block && threadIdx.x == m) a.dbg.sh[sm.ent[m]] = s;
+                int sum = 0;
+                if (gi < n8) {
                     const int q0 = quant_i8(v0.x, inv), q1 = quant_i8(v0.y, inv), q2 = quant_i8(v0.z, inv),
                               q3 = quant_i8(v0.w, inv), q4 = quant_i8(v1.x, inv), q5 = quant_i8(v1.y, inv),
                               q6 = quant_i8(v1.z, inv), q7 = quant_i8(v1.w, inv);
-                    sum += q0 + q1 + q2 + q3 + q4 + q5 + q6 + q7;
+                    sum = q0 + q1 + q2 + q3 + q4 + q5 + q6 + q7;
                     const uint32_t ev = (q0 & 255) | ((q2 & 255) << 8) | ((q4 & 255) << 16) | ((uint32_t)(q6 & 255) << 24);
                     const uint32_t od = (q1 & 255) | ((q3 & 255) << 8) | ((q5 & 255) << 16) | ((uint32_t)(q7 & 255) << 24);
                     *reinterpret_cast<uint2 *>(plane_byte(xs, kdim, m, 8 * gi)) = make_uint2(ev, od);
@@ -236,7 +251,6 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, DecodeSmem &sm,
                 sum = warp_sum_i(sum);
                 if (lane == 0) sm.hpart[warp][m] = sum;
             }
-            if (a.dbg.sh && first_block && threadIdx.x < M) a.dbg.sh[sm.ent[threadIdx.x]] = sm.sx[threadIdx.x];
         }
         __syncthreads();
         if (KIND == kDown) {
@@ -245,7 +259,6 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, DecodeSmem &sm,
 #pragma unroll
                 for (int w = 0; w < 8; ++w) hsum += sm.hpart[w][lane];
         }
-        amax_run = 0.f;
 
         const int g_end = min(p1, (ue + 1) * gpe);  // groups of entry ue end here
         auto in_seg = [&](int jj) { return jj < n_my && p0 + warp + 8 * (jj / UPG) < g_end; };
@@ -271,7 +284,6 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, DecodeSmem &sm,
                     const float uf = __fmul_rn(__fmul_rn((float)ui, sm.sx[lane]), R.s[0]);
                     const float hv = __fmul_rn(silu_f(gf), uf);
                     a.h[(size_t)(r0 + lane) * a.I + o0] = hv;
-                    amax_run = fmaxf(amax_run, fabsf(hv));
                     if (a.dbg.gate_acc) a.dbg.gate_acc[(size_t)sm.ent[lane] * a.I + o0] = gi;
                     if (a.dbg.up_acc) a.dbg.up_acc[(size_t)sm.ent[lane] * a.I + o0] = ui;
                 }
@@ -317,7 +329,6 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, DecodeSmem &sm,
         };
         flip = flip ? !run_m(B, A) : run_m(A, B);
     }
-    if (KIND == kGateUp && lane < M) atomicMax(a.dham + r0 + lane, __float_as_uint(amax_run));
 }
 
 // Contiguous slices of the row groups of entries [0, n) (gpe groups each)
@@ -653,7 +664,6 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
         for (int i = tid; i < kMaxRedBlk; i += blockDim.x) sy->blk[i] = 0;
         for (int i = tid; i < T * E; i += blockDim.x) st_relaxed_u32(a.dlog + i, kLogitEmpty);
         for (int i = tid; i < n_sel; i += blockDim.x) st_relaxed_u64(a.dsel + i, kSelEmpty);
-        for (int i = tid; i < T * S; i += blockDim.x) a.dham[i] = 0u;
         if (tid == 0) {
             sy->quant_cnt = 0;
             sy->gu_cnt = 0;

@@ -30,10 +30,9 @@ struct LayerArgs {
     int32_t *dn_cnt;     // [nb_dn] arrival counters of the fused reduce
     FusedSync *sync;     // counters of the persistent decode kernel
     // hand-over buffers of the persistent decode kernel; every launch leaves
-    // them as it found them (logits / selections empty, max|h| zero)
+    // them as it found them (logits / selections empty)
     float *dlog;                 // [kSmallT, E] logits, kLogitEmpty until written
     unsigned long long *dsel;    // [kSmallT, K] packed selections, kSelEmpty until written
-    uint32_t *dham;              // [kSmallT * S] bits of max|h| per grouped row
     unsigned long long *trace;  // [trace_n] phase stamps of that kernel, or null
     int trace_n;
     float *out;          // [T, D]

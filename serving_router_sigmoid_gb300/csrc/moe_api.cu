@@ -58,7 +58,6 @@ struct Handle {
     moe::FusedSync *sync;
     float *dlog;
     unsigned long long *dsel;
-    uint32_t *dham;
     int32_t *err;
     float *xnorm;  // [Tmax, D] RMSNorm output of moe_block_forward
     int nb_gu, rpi_gu, nb_dn, rpi_dn;
@@ -104,7 +103,6 @@ size_t layout(const MoeLayerDesc &d, Handle *h) {
     const size_t o_sync = take(sizeof(moe::FusedSync));
     const size_t o_dlog = take(4 * moe::kSmallT * E);
     const size_t o_dsel = take(8 * moe::kSmallT * K);
-    const size_t o_dham = take(4 * moe::kSmallT * S);
     const size_t o_err = take(4);
     const size_t o_xn = take(4 * T * D);
     if (h) {
@@ -127,7 +125,6 @@ size_t layout(const MoeLayerDesc &d, Handle *h) {
         h->sync = reinterpret_cast<moe::FusedSync *>(b + o_sync);
         h->dlog = reinterpret_cast<float *>(b + o_dlog);
         h->dsel = reinterpret_cast<unsigned long long *>(b + o_dsel);
-        h->dham = reinterpret_cast<uint32_t *>(b + o_dham);
         h->err = reinterpret_cast<int32_t *>(b + o_err);
         h->xnorm = reinterpret_cast<float *>(b + o_xn);
     }
@@ -168,7 +165,6 @@ cudaError_t record(cudaEvent_t ev, cudaStream_t s) {
 // its end): zero counters and max|h| words, empty logit and selection slots.
 cudaError_t reset_decode_state(const Handle *h, cudaStream_t s) {
     cudaError_t ce = cudaMemsetAsync(h->sync, 0, sizeof(moe::FusedSync), s);
-    if (ce == cudaSuccess) ce = cudaMemsetAsync(h->dham, 0, 4 * moe::kSmallT * (size_t)h->S, s);
     if (ce == cudaSuccess) ce = cudaMemsetAsync(h->dlog, 0xFF, 4 * moe::kSmallT * (size_t)h->d.E, s);
     if (ce == cudaSuccess) ce = cudaMemsetAsync(h->dsel, 0xFF, 8 * moe::kSmallT * (size_t)h->d.K, s);
     return ce;
@@ -205,7 +201,7 @@ int run_layer(Handle *h, const float *x, int T, float *out, const float *resid, 
     a.xq = h->xq; a.sx = h->sx; a.xsum = h->xsum; a.logits = h->logits; a.idx = h->idx; a.wts = h->wts;
     a.rows = h->rows; a.meta = h->meta; a.h = h->h; a.hamax = h->hamax; a.part = h->part; a.dn_cnt = h->dn_cnt;
     a.hq = h->hq; a.hsum = h->hsum; a.shq = h->shq; a.sync = h->sync;
-    a.dlog = h->dlog; a.dsel = h->dsel; a.dham = h->dham;
+    a.dlog = h->dlog; a.dsel = h->dsel;
     a.trace = h->trace; a.trace_n = h->trace_n;
     a.out = out; a.resid = resid; a.err = h->err;
     a.nb_gu = h->nb_gu; a.rpi_gu = h->rpi_gu; a.nb_dn = h->nb_dn; a.rpi_dn = h->rpi_dn;
