@@ -332,32 +332,36 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, DecodeSmem &sm,
 }
 
 // Contiguous slices of the row groups of entries [0, n) (gpe groups each)
-// weighted by cost: a group of an entry costs 2 + the token width its loops
-// are compiled for (1, 2 or the batch's widest, see stream_phase): the weight
-// stream plus that many token rows of dot products.  CTA b gets the groups
-// whose cumulative cost falls in [b W / G, (b+1) W / G); every CTA evaluates
-// the same monotone map, so the slices tile the groups exactly.
-template <int MCH>
+// weighted by cost.  The cost of a group of an entry chosen by M tokens is
+// its measured time on this part in units of ~0.05 us (per-CTA phase traces
+// of an 8-token verify batch, CTAs whose slice lies in one entry): the loops
+// of one or two token rows cost about the weight stream (6, 7); wider loops
+// (compiled for the batch's widest entry, see stream_phase) cost a base plus
+// a per-token share, larger for the down rows (7 + 3 M) than for the
+// gate/up pairs (6 + 2 M).  CTA b gets the groups whose cumulative cost
+// falls in [b W / G, (b+1) W / G); every CTA evaluates the same monotone
+// map, so the slices tile the groups exactly.
+template <int KIND>
 __device__ __forceinline__ long long group_cost(const int *ubeg, int u) {
     const int M = ubeg[u + 1] - ubeg[u];
-    return 2 + (M <= 1 ? 1 : M <= 2 ? 2 : MCH);
+    return M <= 1 ? 6 : M <= 2 ? 7 : KIND == kGateUp ? 6 + 2 * M : 7 + 3 * M;
 }
-template <int MCH>
+template <int KIND>
 __device__ __forceinline__ int group_at_cost(const int *ubeg, int n, int gpe, long long c) {
     long long pre = 0;
     for (int u = 0; u < n; ++u) {
-        const long long w = group_cost<MCH>(ubeg, u), span = (long long)gpe * w;
+        const long long w = group_cost<KIND>(ubeg, u), span = (long long)gpe * w;
         if (c < pre + span) return u * gpe + (int)((c - pre) / w);
         pre += span;
     }
     return n * gpe;
 }
-template <int MCH>
+template <int KIND>
 __device__ __forceinline__ void cost_slice(const int *ubeg, int n, int gpe, int b, int G, int &p0, int &p1) {
     long long W = 0;
-    for (int u = 0; u < n; ++u) W += (long long)gpe * group_cost<MCH>(ubeg, u);
-    p0 = group_at_cost<MCH>(ubeg, n, gpe, (long long)b * W / G);
-    p1 = group_at_cost<MCH>(ubeg, n, gpe, (long long)(b + 1) * W / G);
+    for (int u = 0; u < n; ++u) W += (long long)gpe * group_cost<KIND>(ubeg, u);
+    p0 = group_at_cost<KIND>(ubeg, n, gpe, (long long)b * W / G);
+    p1 = group_at_cost<KIND>(ubeg, n, gpe, (long long)(b + 1) * W / G);
 }
 
 // The union tables of the batch from its T*K selections in sm.idx ((token,
@@ -546,8 +550,8 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
         }
     } else {
         if (tid == 0) {
-            cost_slice<MCH>(sm.ubeg, n_r, I, b, G, sm.slice[0], sm.slice[1]);
-            cost_slice<MCH>(sm.ubeg, n_u, gpd, b, G, sm.slice[2], sm.slice[3]);
+            cost_slice<kGateUp>(sm.ubeg, n_r, I, b, G, sm.slice[0], sm.slice[1]);
+            cost_slice<kDown>(sm.ubeg, n_u, gpd, b, G, sm.slice[2], sm.slice[3]);
         }
         __syncthreads();
         rp0 = sm.slice[0];
