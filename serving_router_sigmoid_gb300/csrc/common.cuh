@@ -13,6 +13,7 @@ constexpr int kMaxE = 512;        // routed experts per layer
 constexpr int kMaxK = 16;         // experts per token
 constexpr int kSmallT = 16;       // token count served by the fused small-batch router
 constexpr int kMaxDim = 8192;     // D and I upper bound (GEMV chunks per lane <= 8)
+constexpr int kRouterSplitK = 4;  // partial logit buffers of the large-batch router (K split)
 
 // Device error word bits (moe_layer_device_status).
 constexpr int kErrNoSelection = 1;   // a token had no finite selection score left

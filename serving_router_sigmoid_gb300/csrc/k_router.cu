@@ -253,10 +253,16 @@ __global__ void __launch_bounds__(256) router_tile_kernel(const float *__restric
 // thread reads 4 tokens and 4 experts as two float4), 256 threads each
 // accumulating 4 tokens x 4 experts with one fmaf chain per output in
 // ascending d.  The next chunk is loaded into registers while the current
-// one is multiplied.  D % 32 == 0.
+// one is multiplied.  K is split into gridDim.z contiguous ranges of whole
+// chunks (4 CTAs per tile: T = 2048 otherwise fills only 128 SMs, one CTA
+// each); range z writes its partial logits to logits + z T E and the select
+// kernel adds the partials in z order.  D % 32 == 0.
 constexpr int kRLT = 64, kRLE = 64, kRLK = 32;
 __global__ void __launch_bounds__(256) router_logits_kernel(const float *__restrict__ x, const float *__restrict__ Wr,
                                                             int T, int D, int E, float *__restrict__ logits) {
+    const int nch = D / kRLK, z = blockIdx.z, nz = gridDim.z;
+    const int kb = (int)((long long)z * nch / nz) * kRLK, ke = (int)((long long)(z + 1) * nch / nz) * kRLK;
+    logits += (size_t)z * T * E;
     __shared__ __align__(16) float xs[kRLK][kRLT + 4];
     __shared__ __align__(16) float ws[kRLK][kRLE + 4];
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
@@ -273,16 +279,16 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const float *__restr
         return row < nrows ? __ldg(reinterpret_cast<const float4 *>(base + (size_t)row * rstride + k0 + lc))
                            : make_float4(0.f, 0.f, 0.f, 0.f);
     };
-    float4 xa = ld(x, t0, T, D, lr, 0), xb = ld(x, t0, T, D, lr + 32, 0);
-    float4 wa = ld(Wr, e0, E, D, lr, 0), wb = ld(Wr, e0, E, D, lr + 32, 0);
-    for (int k0 = 0; k0 < D; k0 += kRLK) {
+    float4 xa = ld(x, t0, T, D, lr, kb), xb = ld(x, t0, T, D, lr + 32, kb);
+    float4 wa = ld(Wr, e0, E, D, lr, kb), wb = ld(Wr, e0, E, D, lr + 32, kb);
+    for (int k0 = kb; k0 < ke; k0 += kRLK) {
         __syncthreads();
         xs[lc + 0][lr] = xa.x; xs[lc + 1][lr] = xa.y; xs[lc + 2][lr] = xa.z; xs[lc + 3][lr] = xa.w;
         xs[lc + 0][lr + 32] = xb.x; xs[lc + 1][lr + 32] = xb.y; xs[lc + 2][lr + 32] = xb.z; xs[lc + 3][lr + 32] = xb.w;
         ws[lc + 0][lr] = wa.x; ws[lc + 1][lr] = wa.y; ws[lc + 2][lr] = wa.z; ws[lc + 3][lr] = wa.w;
         ws[lc + 0][lr + 32] = wb.x; ws[lc + 1][lr + 32] = wb.y; ws[lc + 2][lr + 32] = wb.z; ws[lc + 3][lr + 32] = wb.w;
         __syncthreads();
-        if (k0 + kRLK < D) {  // the next chunk travels while this one is multiplied
+        if (k0 + kRLK < ke) {  // the next chunk travels while this one is multiplied
             xa = ld(x, t0, T, D, lr, k0 + kRLK);
             xb = ld(x, t0, T, D, lr + 32, k0 + kRLK);
             wa = ld(Wr, e0, E, D, lr, k0 + kRLK);
@@ -311,9 +317,10 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const float *__restr
     }
 }
 
-// Top-K of a large batch from its logits: one warp per token (select_topk).
+// Top-K of a large batch from its logits (the sum of nz partial buffers in
+// order): one warp per token (select_topk).
 template <int EPL>
-__global__ void __launch_bounds__(256) router_select_kernel(const float *__restrict__ logits,
+__global__ void __launch_bounds__(256) router_select_kernel(const float *__restrict__ logits, int nz,
                                                             const float *__restrict__ bias, int T, int E, int K,
                                                             float scale, int32_t *__restrict__ idx,
                                                             float *__restrict__ w, int32_t *err) {
@@ -324,7 +331,9 @@ __global__ void __launch_bounds__(256) router_select_kernel(const float *__restr
     for (int j = 0; j < EPL; ++j) {
         const int e = lane + 32 * j;
         if (e < E) {
-            score(__ldg(logits + (size_t)t * E + e), __ldg(bias + e), p[j], c[j]);
+            float l = __ldg(logits + (size_t)t * E + e);
+            for (int z = 1; z < nz; ++z) l = __fadd_rn(l, __ldg(logits + ((size_t)z * T + t) * E + e));
+            score(l, __ldg(bias + e), p[j], c[j]);
         } else {
             p[j] = 0.f;
             c[j] = -INFINITY;
@@ -449,23 +458,25 @@ cudaError_t launch_router_tile(const float *x, const float *Wr, const float *bia
 }
 
 template <int EPL>
-static cudaError_t launch_select_t(const float *logits, const float *bias, int T, int E, int K, float scale,
+static cudaError_t launch_select_t(const float *logits, int nz, const float *bias, int T, int E, int K, float scale,
                                    int32_t *idx, float *w, int32_t *err, cudaStream_t s) {
-    router_select_kernel<EPL><<<(T + 7) / 8, 256, 0, s>>>(logits, bias, T, E, K, scale, idx, w, err);
+    router_select_kernel<EPL><<<(T + 7) / 8, 256, 0, s>>>(logits, nz, bias, T, E, K, scale, idx, w, err);
     return cudaGetLastError();
 }
 
 cudaError_t launch_router_gemm(const float *x, const float *Wr, const float *bias, int T, int D, int E, int K,
                                float scale, float *logits, int32_t *idx, float *w, int32_t *err, cudaStream_t s) {
-    router_logits_kernel<<<dim3((T + kRLT - 1) / kRLT, (E + kRLE - 1) / kRLE), 256, 0, s>>>(x, Wr, T, D, E, logits);
+    const int nz = D / kRLK < kRouterSplitK ? D / kRLK : kRouterSplitK;
+    router_logits_kernel<<<dim3((T + kRLT - 1) / kRLT, (E + kRLE - 1) / kRLE, nz), 256, 0, s>>>(x, Wr, T, D, E,
+                                                                                                logits);
     cudaError_t ce = cudaGetLastError();
     if (ce != cudaSuccess) return ce;
     switch (epl_for(E)) {
-        case 1: return launch_select_t<1>(logits, bias, T, E, K, scale, idx, w, err, s);
-        case 2: return launch_select_t<2>(logits, bias, T, E, K, scale, idx, w, err, s);
-        case 4: return launch_select_t<4>(logits, bias, T, E, K, scale, idx, w, err, s);
-        case 8: return launch_select_t<8>(logits, bias, T, E, K, scale, idx, w, err, s);
-        default: return launch_select_t<16>(logits, bias, T, E, K, scale, idx, w, err, s);
+        case 1: return launch_select_t<1>(logits, nz, bias, T, E, K, scale, idx, w, err, s);
+        case 2: return launch_select_t<2>(logits, nz, bias, T, E, K, scale, idx, w, err, s);
+        case 4: return launch_select_t<4>(logits, nz, bias, T, E, K, scale, idx, w, err, s);
+        case 8: return launch_select_t<8>(logits, nz, bias, T, E, K, scale, idx, w, err, s);
+        default: return launch_select_t<16>(logits, nz, bias, T, E, K, scale, idx, w, err, s);
     }
 }
 
