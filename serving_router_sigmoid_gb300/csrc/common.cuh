@@ -38,15 +38,22 @@ struct RouteMeta {
     int ubeg[kMaxE + 2];
 };
 
-// Arrival counters of the persistent decode kernel (zero between launches:
-// the last CTA of each launch clears them).
+// Arrival counters of the persistent decode kernel.  There are two sets, and
+// with them two sets of its hand-over buffers: launch n uses set n % 2 (the
+// parity of `epoch`, which CTA 0 advances once every CTA has read it) and
+// restores set (n + 1) % 2, which launch n - 1 used, for launch n + 1.  So no
+// CTA has to wait at the end of a launch for all others to finish before
+// the state can be cleared.
 constexpr int kRedRows = 64;                    // output rows per reduce block
 constexpr int kMaxRedBlk = kMaxDim / kRedRows;  // reduce blocks of the largest D
 struct FusedSync {
     int quant_cnt;         // quantiser CTAs finished
     int gu_cnt;            // CTAs finished with gate/up
-    int done_cnt;          // CTAs finished with everything
     int blk[kMaxRedBlk];   // down rows written per reduce block
+};
+struct DecodeState {
+    unsigned int epoch;    // launches so far (its parity selects the set)
+    FusedSync set[2];
 };
 
 // Phase time stamps of the persistent decode kernel (moe_layer_set_trace):

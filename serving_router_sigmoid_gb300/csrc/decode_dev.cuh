@@ -39,8 +39,9 @@
 //      depend on which CTA arrives when.
 // Every wait is bounded (one second of %globaltimer): on time-out the kernel
 // sets kErrSyncTimeout in the error word and runs on to its end, so nothing
-// hangs and the stream stays usable.  The last CTA to finish clears the
-// counters for the next launch.
+// hangs and the stream stays usable.  The counters and hand-over buffers
+// come in two sets used by alternate launches (DecodeState): each launch
+// restores the set the previous one used, so no CTA waits at the end.
 #pragma once
 
 #include <type_traits>
@@ -105,7 +106,7 @@ struct DecodeSmem {
     int sh_ubeg[2];
     int nu;                           // routed union entries
     int nblk;                         // reduce blocks this CTA completed
-    int last;                         // this CTA finished last
+    unsigned int epoch;               // the launch's epoch (DecodeState)
     int slice[4];                     // this CTA's routed gate/up and down group ranges
     int blk_list[kMaxRedBlk];          // reduce blocks this CTA completed
     int ncontrib;                      // (block, rows) contributions listed
@@ -415,17 +416,36 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
     const int tid = threadIdx.x;
     const int b = blockIdx.x, G = gridDim.x;
     const int T = a.T, D = a.D, I = a.I, E = a.E, K = a.K, S = a.S, n_sel = T * K;
-    FusedSync *sy = a.sync;
 
     // one-entry view of the shared expert: grouped rows [n_sel, n_sel + T)
     if (tid < T) sm.rows[n_sel + tid] = tid * S + K;
     if (tid == 0) {
+        sm.epoch = ld_relaxed_u32(&a.dstate->epoch);
         sm.sh_uexp[0] = E;
         sm.sh_ubeg[0] = n_sel;
         sm.sh_ubeg[1] = n_sel + T;
     }
     __syncthreads();
     stamp(a, 0);
+    // this launch's set of counters and hand-over buffers; the other set
+    // (the previous launch's) is restored for the next launch, a share per CTA
+    const int par = (int)(sm.epoch & 1u);
+    FusedSync *sy = &a.dstate->set[par];
+    float *const dlog = a.dlog + (size_t)par * kSmallT * E;
+    unsigned long long *const dsel = a.dsel + (size_t)par * kSmallT * K;
+    {
+        FusedSync *so = &a.dstate->set[par ^ 1];
+        float *const olog = a.dlog + (size_t)(par ^ 1) * kSmallT * E;
+        unsigned long long *const osel = a.dsel + (size_t)(par ^ 1) * kSmallT * K;
+        const int stride = G * blockDim.x;
+        for (int i = b * blockDim.x + tid; i < kSmallT * E; i += stride) st_relaxed_u32(olog + i, kLogitEmpty);
+        for (int i = b * blockDim.x + tid; i < kSmallT * K; i += stride) st_relaxed_u64(osel + i, kSelEmpty);
+        for (int i = b * blockDim.x + tid; i < kMaxRedBlk; i += stride) so->blk[i] = 0;
+        if (b == 0 && tid == 0) {
+            so->quant_cnt = 0;
+            so->gu_cnt = 0;
+        }
+    }
 
     // ---- phase 1.  The router rows go first (everything downstream waits on
     // the logits), then the first rows of the shared expert, which need no
@@ -451,7 +471,7 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
             const float l = logits_finish(wr, a.x, T, D, sm.red);
             if (tid < T) {
                 const uint32_t bits = __float_as_uint(l);
-                st_relaxed_u32(a.dlog + tid * E + e, bits == kLogitEmpty ? 0x7FFFFFFFu : bits);
+                st_relaxed_u32(dlog + tid * E + e, bits == kLogitEmpty ? 0x7FFFFFFFu : bits);
             }
         }
     }
@@ -475,8 +495,8 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
     // routine of the four-kernel router) as soon as its logits are in, and
     // publishes them as data, while the other CTAs stream the shared expert
     if (tq < T)
-        topk_small_cta<true>(a.dlog + (size_t)tq * E, a.bias, 1, E, K, a.routed_scale, nullptr, nullptr,
-                             a.dsel + (size_t)tq * K, a.err, sm.tk, sm.tkp);
+        topk_small_cta<true>(dlog + (size_t)tq * E, a.bias, 1, E, K, a.routed_scale, nullptr, nullptr,
+                             dsel + (size_t)tq * K, a.err, sm.tk, sm.tkp);
 
     // shared expert gate/up, once the quantised tokens are in
     if (MCH > 1) cta_wait(&sy->quant_cnt, T, a.err);
@@ -492,7 +512,7 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
         for (;;) {
             bool miss = false;
             for (int i = tid; i < n_sel; i += blockDim.x) {
-                const unsigned long long v = ld_relaxed_u64(a.dsel + i);
+                const unsigned long long v = ld_relaxed_u64(dsel + i);
                 const int e = (int)(v >> 32);
                 miss |= v == kSelEmpty;
                 sm.idx[i] = (e >= 0 && e < E) ? e : 0;
@@ -570,6 +590,8 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
     UnitRegs<kDown, CPLD> A2, B2;
     prime<kDown, CPLD>(A2, B2, a, sm.uexp, gpd, dp0, dp1, ex_u, ex);
     cta_wait(&sy->gu_cnt, G, a.err);
+    // every CTA has read the epoch (before it arrived): advance it
+    if (b == 0 && tid == 0) st_relaxed_u32(&a.dstate->epoch, sm.epoch + 1u);
     stamp(a, 7);
     stream_phase<kDown, CPLD, MCH>(a, sm, xs, sm.uexp, sm.ubeg, dp0, dp1, A2, B2, ex_u, ex);
     stamp(a, 8);
@@ -656,24 +678,7 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
         }
     }
 
-    // the last CTA to finish clears every counter for the next launch
     stamp(a, 9);
-    __syncthreads();
-    if (tid == 0) {
-        __threadfence();
-        sm.last = atomicAdd(&sy->done_cnt, 1) == G - 1;
-    }
-    __syncthreads();
-    if (sm.last) {
-        for (int i = tid; i < kMaxRedBlk; i += blockDim.x) sy->blk[i] = 0;
-        for (int i = tid; i < T * E; i += blockDim.x) st_relaxed_u32(a.dlog + i, kLogitEmpty);
-        for (int i = tid; i < n_sel; i += blockDim.x) st_relaxed_u64(a.dsel + i, kSelEmpty);
-        if (tid == 0) {
-            sy->quant_cnt = 0;
-            sy->gu_cnt = 0;
-            sy->done_cnt = 0;
-        }
-    }
 }
 
 using DecodeFn = void (*)(LayerArgs);

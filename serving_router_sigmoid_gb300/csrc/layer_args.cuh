@@ -28,11 +28,11 @@ struct LayerArgs {
     int32_t *hsum;       // [Tmax * S] code sums of hq rows
     float *shq;          // [Tmax * S] scales of hq rows
     int32_t *dn_cnt;     // [nb_dn] arrival counters of the fused reduce
-    FusedSync *sync;     // counters of the persistent decode kernel
-    // hand-over buffers of the persistent decode kernel; every launch leaves
-    // them as it found them (logits / selections empty)
-    float *dlog;                 // [kSmallT, E] logits, kLogitEmpty until written
-    unsigned long long *dsel;    // [kSmallT, K] packed selections, kSelEmpty until written
+    DecodeState *dstate;  // counters of the persistent decode kernel (two sets)
+    // hand-over buffers of the persistent decode kernel, one per set of
+    // counters; a set is empty (logits / selections) when its launch starts
+    float *dlog;                 // [2][kSmallT, E] logits, kLogitEmpty until written
+    unsigned long long *dsel;    // [2][kSmallT, K] packed selections, kSelEmpty until written
     unsigned long long *trace;  // [trace_n] phase stamps of that kernel, or null
     int trace_n;
     float *out;          // [T, D]

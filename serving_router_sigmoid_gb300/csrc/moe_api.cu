@@ -55,7 +55,7 @@ struct Handle {
     int32_t *hsum;
     float *shq;
     int32_t *dn_cnt;
-    moe::FusedSync *sync;
+    moe::DecodeState *dstate;
     float *dlog;
     unsigned long long *dsel;
     int32_t *err;
@@ -101,9 +101,9 @@ size_t layout(const MoeLayerDesc &d, Handle *h) {
     const size_t o_hsum = take(4 * T * S);
     const size_t o_shq = take(4 * T * S);
     const size_t o_cnt = take(4 * nb_dn);
-    const size_t o_sync = take(sizeof(moe::FusedSync));
-    const size_t o_dlog = take(4 * moe::kSmallT * E);
-    const size_t o_dsel = take(8 * moe::kSmallT * K);
+    const size_t o_sync = take(sizeof(moe::DecodeState));
+    const size_t o_dlog = take(2 * 4 * moe::kSmallT * E);
+    const size_t o_dsel = take(2 * 8 * moe::kSmallT * K);
     const size_t o_err = take(4);
     const size_t o_xn = take(4 * T * D);
     if (h) {
@@ -123,7 +123,7 @@ size_t layout(const MoeLayerDesc &d, Handle *h) {
         h->hsum = reinterpret_cast<int32_t *>(b + o_hsum);
         h->shq = reinterpret_cast<float *>(b + o_shq);
         h->dn_cnt = reinterpret_cast<int32_t *>(b + o_cnt);
-        h->sync = reinterpret_cast<moe::FusedSync *>(b + o_sync);
+        h->dstate = reinterpret_cast<moe::DecodeState *>(b + o_sync);
         h->dlog = reinterpret_cast<float *>(b + o_dlog);
         h->dsel = reinterpret_cast<unsigned long long *>(b + o_dsel);
         h->err = reinterpret_cast<int32_t *>(b + o_err);
@@ -165,9 +165,9 @@ cudaError_t record(cudaEvent_t ev, cudaStream_t s) {
 // The state the persistent decode kernel expects at launch (and restores at
 // its end): zero counters and max|h| words, empty logit and selection slots.
 cudaError_t reset_decode_state(const Handle *h, cudaStream_t s) {
-    cudaError_t ce = cudaMemsetAsync(h->sync, 0, sizeof(moe::FusedSync), s);
-    if (ce == cudaSuccess) ce = cudaMemsetAsync(h->dlog, 0xFF, 4 * moe::kSmallT * (size_t)h->d.E, s);
-    if (ce == cudaSuccess) ce = cudaMemsetAsync(h->dsel, 0xFF, 8 * moe::kSmallT * (size_t)h->d.K, s);
+    cudaError_t ce = cudaMemsetAsync(h->dstate, 0, sizeof(moe::DecodeState), s);
+    if (ce == cudaSuccess) ce = cudaMemsetAsync(h->dlog, 0xFF, 2 * 4 * moe::kSmallT * (size_t)h->d.E, s);
+    if (ce == cudaSuccess) ce = cudaMemsetAsync(h->dsel, 0xFF, 2 * 8 * moe::kSmallT * (size_t)h->d.K, s);
     return ce;
 }
 
@@ -201,7 +201,7 @@ int run_layer(Handle *h, const float *x, int T, float *out, const float *resid, 
     a.x = x; a.Wr = h->Wr; a.bias = h->bias; a.experts = h->experts;
     a.xq = h->xq; a.sx = h->sx; a.xsum = h->xsum; a.logits = h->logits; a.idx = h->idx; a.wts = h->wts;
     a.rows = h->rows; a.meta = h->meta; a.h = h->h; a.hamax = h->hamax; a.part = h->part; a.dn_cnt = h->dn_cnt;
-    a.hq = h->hq; a.hsum = h->hsum; a.shq = h->shq; a.sync = h->sync;
+    a.hq = h->hq; a.hsum = h->hsum; a.shq = h->shq; a.dstate = h->dstate;
     a.dlog = h->dlog; a.dsel = h->dsel;
     a.trace = h->trace; a.trace_n = h->trace_n;
     a.out = out; a.resid = resid; a.err = h->err;
