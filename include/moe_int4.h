@@ -231,10 +231,19 @@ int moe_layer_set_probe(void *handle, int which, cudaEvent_t begin, cudaEvent_t 
  * MMA (mma.sync s8 x u8).  Both give bit-identical int32 dot products.  Needs
  * D % 128 == 0 and I % 64 == 0. */
 #define MOE_OPT_TCGEN05_GEMM 3
+/* Test hook of the failure path, 0 (default) or 1: with 1 the persistent
+ * decode kernel's grid barrier (after gate/up) waits for one arrival more
+ * than there are CTAs, so that bounded wait runs out (one second) and the
+ * launch sets bit 16 in the error word, which moe_layer_device_status
+ * reports (clearing the handle's counters); the kernel then runs to its end
+ * and its output is still the full result.  Used by the tests to exercise
+ * time-out detection without a GPU fault. */
+#define MOE_OPT_DECODE_TEST_WAIT_TIMEOUT 4
 
 /*
  * Set / read a handle option (host).  Not part of the pages' interface: these
- * select between two equivalent launch plans of the same computation.
+ * select between two equivalent launch plans of the same computation (or
+ * turn on the test hook above).
  * Errors: INVALID_ARG (bad handle, unknown option, value out of range).
  */
 int moe_layer_set_option(void *handle, int option, int value);

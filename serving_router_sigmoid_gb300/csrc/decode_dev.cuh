@@ -589,7 +589,7 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
     cta_arrive(&sy->gu_cnt);
     UnitRegs<kDown, CPLD> A2, B2;
     prime<kDown, CPLD>(A2, B2, a, sm.uexp, gpd, dp0, dp1, ex_u, ex);
-    cta_wait(&sy->gu_cnt, G, a.err);
+    cta_wait(&sy->gu_cnt, G + a.wait_extra, a.err);
     // every CTA has read the epoch (before it arrived): advance it
     if (b == 0 && tid == 0) st_relaxed_u32(&a.dstate->epoch, sm.epoch + 1u);
     stamp(a, 7);

@@ -40,6 +40,7 @@ struct LayerArgs {
     int32_t *err;
     int nb_gu, rpi_gu;   // gate/up: row blocks per expert, rows per block
     int nb_dn, rpi_dn;   // down: row blocks per expert, rows per block
+    int wait_extra;      // test hook: arrivals the decode kernel's grid barrier waits for beyond G
     DebugPtrs dbg;
 };
 

@@ -66,6 +66,7 @@ struct Handle {
     bool stream_ok;  // shapes and alignment the streaming kernels cover
     bool single_kernel;  // decode batches run the persistent single-kernel layer
     bool tcgen05_gemm;   // larger batches run the tcgen05 expert GEMMs
+    int test_wait_extra;  // MOE_OPT_DECODE_TEST_WAIT_TIMEOUT
     int dec_grid[moe::kSmallT + 1];  // its grid per token count (0: not available)
     int probe_which;
     cudaEvent_t probe_begin, probe_end;
@@ -206,6 +207,7 @@ int run_layer(Handle *h, const float *x, int T, float *out, const float *resid, 
     a.trace = h->trace; a.trace_n = h->trace_n;
     a.out = out; a.resid = resid; a.err = h->err;
     a.nb_gu = h->nb_gu; a.rpi_gu = h->rpi_gu; a.nb_dn = h->nb_dn; a.rpi_dn = h->rpi_dn;
+    a.wait_extra = h->test_wait_extra;
     a.dbg = dbg;
     const int mch = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8;
     const int mi = moe::mch_index(mch);
@@ -501,6 +503,10 @@ int moe_layer_set_option(void *handle, int option, int value) {
             if (value != 0 && value != 1) return fail(MOE_ERR_INVALID_ARG, "value %d: need 0 or 1", value);
             h->tcgen05_gemm = value != 0;
             return MOE_OK;
+        case MOE_OPT_DECODE_TEST_WAIT_TIMEOUT:
+            if (value != 0 && value != 1) return fail(MOE_ERR_INVALID_ARG, "value %d: need 0 or 1", value);
+            h->test_wait_extra = value;
+            return MOE_OK;
         default:
             return fail(MOE_ERR_INVALID_ARG, "unknown option %d", option);
     }
@@ -515,6 +521,9 @@ int moe_layer_get_option(void *handle, int option, int *value_out) {
             return MOE_OK;
         case MOE_OPT_TCGEN05_GEMM:
             *value_out = h->tcgen05_gemm ? 1 : 0;
+            return MOE_OK;
+        case MOE_OPT_DECODE_TEST_WAIT_TIMEOUT:
+            *value_out = h->test_wait_extra;
             return MOE_OK;
         case MOE_OPT_DECODE_SINGLE_KERNEL_AVAILABLE: {
             int any = 0;

@@ -7,6 +7,8 @@ each other, repeated launches (the kernel's arrival counters must be back at
 zero after every launch), CUDA-graph replay, and a batch at every token count
 the kernel covers.
 """
+import time
+
 import pytest
 import torch
 
@@ -18,6 +20,8 @@ pytestmark = pytest.mark.gpu
 
 SINGLE = 1  # MOE_OPT_DECODE_SINGLE_KERNEL
 AVAILABLE = 2  # MOE_OPT_DECODE_SINGLE_KERNEL_AVAILABLE
+TEST_WAIT_TIMEOUT = 4  # MOE_OPT_DECODE_TEST_WAIT_TIMEOUT
+SYNC_TIMEOUT = 16  # error bit of a wait that ran out of time
 
 DECODE_CASES = [
     dict(D=256, I=128, E=16, K=2, n_shared=1, T=1),
@@ -190,5 +194,38 @@ def test_layer_exact_tie_goes_to_lower_index(moe, single):
             assert row.index(4) < row.index(11)
         ri, rw, _ = oracle.router(x.numpy(), Wr.numpy(), b.numpy(), 3, pair.cfg.routed_scale)
         assert (idx == ri).all()
+    finally:
+        pair.close()
+
+
+@pytest.mark.parametrize("T", [1, 3])
+def test_wait_timeout_is_reported_and_recovered(moe, T):
+    """The test hook makes the grid barrier's bounded wait run out (it waits
+    for one arrival more than there are CTAs): the launch ends after about a
+    second with the time-out bit, which device_status reports, and the full
+    result; the next launches run normally.  No fault, trap or endless loop
+    is involved."""
+    case = dict(D=256, I=128, E=16, K=2, n_shared=1, T=T)
+    pair = _pair(case, 6)
+    try:
+        xd = pair.x.cuda()
+        ref = pair.gpu.forward(xd)
+        torch.cuda.synchronize()
+        assert pair.gpu.device_status() == 0
+        pair.gpu.set_option(TEST_WAIT_TIMEOUT, 1)
+        assert pair.gpu.get_option(TEST_WAIT_TIMEOUT) == 1
+        t0 = time.time()
+        out = pair.gpu.forward(xd)
+        torch.cuda.synchronize()
+        elapsed = time.time() - t0
+        assert pair.gpu.device_status() == SYNC_TIMEOUT
+        assert elapsed > 0.5
+        assert torch.equal(out, ref)
+        pair.gpu.set_option(TEST_WAIT_TIMEOUT, 0)
+        for _ in range(3):
+            out2 = pair.gpu.forward(xd)
+        torch.cuda.synchronize()
+        assert pair.gpu.device_status() == 0
+        assert torch.equal(out2, ref)
     finally:
         pair.close()
