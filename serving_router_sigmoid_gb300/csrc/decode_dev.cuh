@@ -459,8 +459,13 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
     int ex_u = -1;
     DevExpert ex{};
     UnitRegs<kGateUp, CPLG> A, B;
-    const int sp0 = a.n_shared ? (int)((long long)b * I / G) : 0;
-    const int sp1 = a.n_shared ? (int)((long long)(b + 1) * I / G) : 0;
+    // (one token: the shared expert's gate/up streams here, within the
+    // routing's latency; more tokens: it is compute bound in the wide dot
+    // loops and would hold up the union, so it joins the routed entries'
+    // cost-weighted slices instead)
+    const bool sh_early = MCH == 1 && a.n_shared;
+    const int sp0 = sh_early ? (int)((long long)b * I / G) : 0;
+    const int sp1 = sh_early ? (int)((long long)(b + 1) * I / G) : 0;
     prime<kGateUp, CPLG>(A, B, a, sm.sh_uexp, I, sp0, sp1, ex_u, ex);
 
     // router logits of experts b, b + G, ... (the arithmetic of the
@@ -546,8 +551,8 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
         }
     }
 
-    // routed experts' gate/up and all entries' down: cost-weighted
-    // contiguous slices of (entry, row group)
+    // routed experts' gate/up (with the shared expert's for T > 1) and all
+    // entries' down: contiguous slices of (entry, row group)
     constexpr int RPD = UnitShape<kDown, CPLD>::kRows;  // down rows per group
     const int gpd = D / RPD;
     int rp0, rp1, dp0, dp1;
@@ -570,7 +575,7 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
         }
     } else {
         if (tid == 0) {
-            cost_slice<kGateUp>(sm.ubeg, n_r, I, b, G, sm.slice[0], sm.slice[1]);
+            cost_slice<kGateUp>(sm.ubeg, n_u, I, b, G, sm.slice[0], sm.slice[1]);
             cost_slice<kDown>(sm.ubeg, n_u, gpd, b, G, sm.slice[2], sm.slice[3]);
         }
         __syncthreads();
