@@ -466,7 +466,9 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
     const bool sh_early = MCH == 1 && a.n_shared;
     const int sp0 = sh_early ? (int)((long long)b * I / G) : 0;
     const int sp1 = sh_early ? (int)((long long)(b + 1) * I / G) : 0;
-    prime<kGateUp, CPLG>(A, B, a, sm.sh_uexp, I, sp0, sp1, ex_u, ex);
+    // (a router CTA requests them once its logits are out, so that the router
+    // rows have HBM to themselves at the start)
+    if (b >= E) prime<kGateUp, CPLG>(A, B, a, sm.sh_uexp, I, sp0, sp1, ex_u, ex);
 
     // router logits of experts b, b + G, ... (the arithmetic of the
     // four-kernel router), published as data: the slot itself is the flag
@@ -479,6 +481,7 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
                 st_relaxed_u32(dlog + tid * E + e, bits == kLogitEmpty ? 0x7FFFFFFFu : bits);
             }
         }
+        prime<kGateUp, CPLG>(A, B, a, sm.sh_uexp, I, sp0, sp1, ex_u, ex);
     }
     stamp(a, 1);
 
