@@ -59,8 +59,8 @@ HOT_KERNEL_PREFILL = "umma_gemm_kernel<0> (tcgen05 f16-exact gate/up GEMM, SiLU*
 # capture of the current kernel source, or None.  Keyed by workload.
 TRAFFIC = {
     # profiles/launches_glm_moe_layer_decode_b1.md: decode_layer_kernel on the
-    # full workload, 176.7 MB read + 0.72 MB written per launch
-    "glm_moe_layer_decode_b1": 177.4e6,
+    # full workload, 176.7 MB read + 0.57 MB written per launch
+    "glm_moe_layer_decode_b1": 177.3e6,
     # profiles/umma_gemm_prefill_2048.md: umma_gemm_kernel<0> (gate/up),
     # 2.51 GB read + 0.13 GB written
     "glm_moe_layer_prefill_2048": 2.642e9,
