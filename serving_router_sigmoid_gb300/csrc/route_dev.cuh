@@ -22,12 +22,9 @@ namespace moe {
 // product).  D % 8 == 0, D <= 8192, 16-byte aligned rows.  Each thread owns up
 // to four 8-element groups, loaded once into registers before any use.
 // Outputs (each may be null): xq_row / sx_out / xsum_out global; nat_row the
-// natural-order codes; tile the two-plane shared-memory row of the streaming
-// kernels (plane_byte, kdim = D) with tile_sx / tile_xsum.
+// natural-order codes.
 __device__ __forceinline__ void quant_token_perm(const float *__restrict__ xrow, int D, int8_t *__restrict__ xq_row,
-                                                 float *sx_out, int32_t *xsum_out, int8_t *nat_row,
-                                                 int8_t *tile = nullptr, float *tile_sx = nullptr,
-                                                 int *tile_xsum = nullptr) {
+                                                 float *sx_out, int32_t *xsum_out, int8_t *nat_row) {
     __shared__ float red_f[32];
     __shared__ int red_i[32];
     constexpr int G = kMaxDim / (8 * 256);
@@ -63,7 +60,6 @@ __device__ __forceinline__ void quant_token_perm(const float *__restrict__ xrow,
         const uint32_t ev = (q0 & 255) | ((q2 & 255) << 8) | ((q4 & 255) << 16) | ((uint32_t)(q6 & 255) << 24);
         const uint32_t od = (q1 & 255) | ((q3 & 255) << 8) | ((q5 & 255) << 16) | ((uint32_t)(q7 & 255) << 24);
         if (xq_row) *reinterpret_cast<uint2 *>(xq_row + 8 * g) = make_uint2(ev, od);
-        if (tile) *reinterpret_cast<uint2 *>(plane_byte(tile, D, 0, 8 * g)) = make_uint2(ev, od);
         if (nat_row) {
             const uint32_t n0 = (q0 & 255) | ((q1 & 255) << 8) | ((q2 & 255) << 16) | ((uint32_t)(q3 & 255) << 24);
             const uint32_t n1 = (q4 & 255) | ((q5 & 255) << 8) | ((q6 & 255) << 16) | ((uint32_t)(q7 & 255) << 24);
@@ -74,8 +70,6 @@ __device__ __forceinline__ void quant_token_perm(const float *__restrict__ xrow,
     if (threadIdx.x == 0) {
         if (sx_out) *sx_out = s;
         if (xsum_out) *xsum_out = sum;
-        if (tile_sx) *tile_sx = s;
-        if (tile_xsum) *tile_xsum = sum;
     }
 }
 
