@@ -20,14 +20,15 @@
 //      and publishes each as data (the slot itself is the flag).  At one
 //      token every CTA quantises the token into its own tile from the
 //      registers the router loads brought; for T > 1 the last T CTAs
-//      quantise one token each (arrival counter).  Every CTA requests the
-//      first rows of its slice of the shared expert's gate/up, which needs
-//      no routing, and streams that slice once the tokens are quantised.
-//      Meanwhile CTA G-1-t polls token t's logits, selects its top-K and
-//      publishes the selections as data.
+//      quantise one token each (arrival counter).  At one token every CTA
+//      also streams its slice of the shared expert's gate/up, which needs
+//      no routing (a router CTA requests those rows once its logits are
+//      out).  Meanwhile CTA G-1-t polls token t's logits, selects its top-K
+//      and publishes the selections as data.
 //   2. Every CTA polls the published selections and builds the union
 //      tables itself, in shared memory; then it streams its contiguous
-//      slice of the routed experts' gate/up rows (h to L2).
+//      slice of the routed experts' gate/up rows (for T > 1 with the shared
+//      expert's; slices weighted by measured per-group costs; h to L2).
 //   3. A grid-wide arrival barrier; each CTA arrives, then requests its
 //      first down rows, then waits.  The CTA stages the h rows of the
 //      entries in its slice (max|h| of each row by a block reduction of the
