@@ -348,12 +348,21 @@ __device__ __forceinline__ long long group_cost(const int *ubeg, int u) {
     const int M = ubeg[u + 1] - ubeg[u];
     return M <= 1 ? 6 : M <= 2 ? 7 : KIND == kGateUp ? 6 + 2 * M : 7 + 3 * M;
 }
+// Each entry's first group also carries the cost of staging that entry's
+// token rows (one round trip for the quantised tokens of a gate/up entry,
+// about one per h row of a down entry): a CTA whose slice starts k entries
+// pays k stagings more.
+template <int KIND>
+__device__ __forceinline__ long long entry_cost(const int *ubeg, int u) {
+    const int M = ubeg[u + 1] - ubeg[u];
+    return KIND == kGateUp ? 28 : 20 * M;
+}
 template <int KIND>
 __device__ __forceinline__ int group_at_cost(const int *ubeg, int n, int gpe, long long c) {
     long long pre = 0;
     for (int u = 0; u < n; ++u) {
-        const long long w = group_cost<KIND>(ubeg, u), span = (long long)gpe * w;
-        if (c < pre + span) return u * gpe + (int)((c - pre) / w);
+        const long long w = group_cost<KIND>(ubeg, u), ce = entry_cost<KIND>(ubeg, u), span = ce + (long long)gpe * w;
+        if (c < pre + span) return u * gpe + (c - pre < ce ? 0 : (int)((c - pre - ce) / w));
         pre += span;
     }
     return n * gpe;
@@ -361,7 +370,7 @@ __device__ __forceinline__ int group_at_cost(const int *ubeg, int n, int gpe, lo
 template <int KIND>
 __device__ __forceinline__ void cost_slice(const int *ubeg, int n, int gpe, int b, int G, int &p0, int &p1) {
     long long W = 0;
-    for (int u = 0; u < n; ++u) W += (long long)gpe * group_cost<KIND>(ubeg, u);
+    for (int u = 0; u < n; ++u) W += entry_cost<KIND>(ubeg, u) + (long long)gpe * group_cost<KIND>(ubeg, u);
     p0 = group_at_cost<KIND>(ubeg, n, gpe, (long long)b * W / G);
     p1 = group_at_cost<KIND>(ubeg, n, gpe, (long long)(b + 1) * W / G);
 }
