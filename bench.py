@@ -95,6 +95,17 @@ def env_rank():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(value, world, device="cpu"):
+    """The largest of every rank's `value` (the job's time is its slowest
+    rank's); the process group must be up when world > 1."""
+    if world <= 1:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def layer_bytes_per_expert(cfg):
     import synth
     return synth.expert_bytes(cfg)
@@ -365,10 +376,7 @@ def run_ours(args, cfg, stack, rank, world, local):
         torch.distributed.barrier()
     elapsed_ms = ev0.elapsed_time(ev1)
     clk = clocks.stop()
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
 
     tokens = T * K * world
     value = tokens / (elapsed_ms / 1e3)
@@ -451,10 +459,7 @@ def run_ours(args, cfg, stack, rank, world, local):
             a1.record(s)
             s.synchronize()
         e_ms = a0.elapsed_time(a1)
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(e_ms, world, dev)
         e2e = {"value": T * Ke * world / (e_ms / 1e3), "unit": UNIT, "steps": Ke,
                "h2d_bytes_per_step": T * cfg.D * 4, "d2h_bytes_per_step": T * cfg.D * 4,
                "api": "moe_block_forward" if stack else "moe_layer_forward", "graph": False}
