@@ -58,11 +58,12 @@ HOT_KERNEL_PREFILL = "umma_gemm_kernel<0> (tcgen05 f16-exact gate/up GEMM, SiLU*
 # DRAM bytes (read + write) per launch of the dominant kernel from one ncu
 # capture of the current kernel source, or None.  Keyed by workload.
 TRAFFIC = {
-    # profiles/launches_glm_moe_layer_decode_b1.md: decode_layer_kernel on the
-    # full workload, 176.7 MB read + 0.57 MB written per launch
+    # decode_layer_kernel on the full decode batch-1 workload (launch-list
+    # capture with the DRAM byte counters): 176.7 MB read + 0.57 MB written
+    # per launch
     "glm_moe_layer_decode_b1": 177.3e6,
-    # profiles/umma_gemm_prefill_2048.md: umma_gemm_kernel<0> (gate/up),
-    # 2.51 GB read + 0.13 GB written
+    # umma_gemm_kernel<0> (gate/up) at prefill 2048 (full capture of the
+    # 17-expert profiling layout): 2.51 GB read + 0.13 GB written
     "glm_moe_layer_prefill_2048": 2.642e9,
 }
 
@@ -80,6 +81,8 @@ def parse_args():
     p.add_argument("--no-graph", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-secondary", action="store_true",
+                   help="default workload only: skip the verify-8 and prefill-2048 lines timed after it")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU oracle sample budget")
     p.add_argument("--ref-seconds", type=float, default=150.0, help="reference arm time box")
     p.add_argument("--four-kernel", action="store_true",
@@ -244,17 +247,22 @@ def union_sizes(layers, xs):
 
 # ----------------------------------------------------------------- our arm
 
-def run_ours(args, cfg, stack, rank, world, local):
+def run_ours(args, workload, rank, world, local, n_layers=None, steps=None, warmup=None, with_e2e=True,
+             with_cpu=True):
+    """One workload on this rank's GPU; returns rank 0's JSON object (None on
+    the other ranks).  The process group, if any, is already up."""
     import torch
     import serving_router_sigmoid_gb300 as moe
     import synth
 
+    cfg = synth.CONFIGS[WORKLOADS[workload][0]]
+    stack = WORKLOADS[workload][1]
+    steps = args.steps if steps is None else steps
+    warmup = args.warmup if warmup is None else warmup
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-    n_layers = 8 if stack else max(1, args.layers)
+    if n_layers is None:
+        n_layers = 8 if stack else max(1, args.layers)
     t_setup = time.time()
     layers, keep = build_layers(cfg, n_layers, args.light, dev, rank_seed=rank)
     T = cfg.T
@@ -343,14 +351,14 @@ def run_ours(args, cfg, stack, rank, world, local):
     t0 = time.time()
     with torch.cuda.stream(s):
         n_sync = 0
-        while w_done < args.warmup or time.time() - t0 < 0.5:
+        while w_done < warmup or time.time() - t0 < 0.5:
             w_done += launch(w_done, 1 << 30)
             if w_done >= n_sync + 64:
                 n_sync = w_done
                 s.synchronize()
         s.synchronize()
 
-    K = args.steps
+    K = steps
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     probe_ms = []
     if world > 1:
@@ -399,7 +407,7 @@ def run_ours(args, cfg, stack, rank, world, local):
         achieved = step_bytes_layer / (probe_avg_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "kernel": HOT_KERNEL_SINGLE, "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_kind": peak_kind + " HBM copy bandwidth",
-                "traffic": TRAFFIC.get(args.workload), "algorithmic_bytes_per_launch": step_bytes_layer,
+                "traffic": TRAFFIC.get(workload), "algorithmic_bytes_per_launch": step_bytes_layer,
                 "avg_launch_ms": probe_avg_ms, "launches_timed": launches_timed}
     elif args.probe != "gateup":
         roof = {"bound": "hbm", "kernel": args.probe, "achieved": None, "peak": None, "unit": "GB/s",
@@ -409,7 +417,7 @@ def run_ours(args, cfg, stack, rank, world, local):
         achieved = gu_bytes / (probe_avg_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "kernel": HOT_KERNEL_DECODE, "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_kind": peak_kind + " HBM copy bandwidth",
-                "traffic": TRAFFIC.get(args.workload), "algorithmic_bytes_per_launch": gu_bytes,
+                "traffic": TRAFFIC.get(workload), "algorithmic_bytes_per_launch": gu_bytes,
                 "avg_launch_ms": probe_avg_ms, "launches_timed": launches_timed}
     else:
         # int8 ops of the gate/up GEMM: every routed (token, expert) pair and
@@ -422,12 +430,12 @@ def run_ours(args, cfg, stack, rank, world, local):
                 "unit": "TFLOP/s", "frac": achieved / peak,
                 "peak_kind": peak_kind + " dense bf16 (sustained); sm_103a has no int8 tcgen05 kind, so the "
                              "densest tensor rate for these operands is the 16-bit one",
-                "traffic": TRAFFIC.get(args.workload), "algorithmic_ops_per_launch": ops,
+                "traffic": TRAFFIC.get(workload), "algorithmic_ops_per_launch": ops,
                 "avg_launch_ms": probe_avg_ms, "launches_timed": launches_timed}
 
     # end to end through the C ABI: pinned host x -> device, forward, out -> pinned host
     e2e = None
-    if not args.no_e2e:
+    if with_e2e and not args.no_e2e:
         Ke = max(16, min(K, 2000))
         xh = [x.cpu().pin_memory() for x in xs]
         oh = torch.empty((T, cfg.D), dtype=torch.float32).pin_memory()
@@ -465,15 +473,15 @@ def run_ours(args, cfg, stack, rank, world, local):
                "api": "moe_block_forward" if stack else "moe_layer_forward", "graph": False}
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and with_cpu and not args.no_cpu_baseline:
         cpu = cpu_baseline(cfg, stack, args.cpu_seconds, dev)
 
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": warmup,
         "warmup_steps_run": w_done,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int4 weights x int8 activations -> int32, fp32 scales", "data": "synthetic",
-        "config": {"workload": args.workload, "hidden": cfg.D, "moe_intermediate": cfg.I, "experts": cfg.E,
+        "config": {"workload": workload, "hidden": cfg.D, "moe_intermediate": cfg.I, "experts": cfg.E,
                    "top_k": cfg.K, "shared_experts": cfg.n_shared, "tokens_per_step": T,
                    "layers_per_step": len(layers) if stack else 1, "layer_sets_cycled": n_layers,
                    "routed_scale": cfg.routed_scale, "zipf_skew": cfg.skew,
@@ -492,10 +500,11 @@ def run_ours(args, cfg, stack, rank, world, local):
         "clocks": clk,
         "setup_s": round(setup_s, 1),
     }
-    if world > 1:
-        torch.distributed.destroy_process_group()
     for lyr in layers:
         lyr.close()
+    del keep, layers, xs, outs
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
     return line if rank == 0 else None
 
 
@@ -515,33 +524,74 @@ def _oracle_layer_for(cfg, x_np, layer_id, dev):
     return oracle.Layer(cfg.D, cfg.I, cfg.E, cfg.K, cfg.n_shared, cfg.routed_scale, Wr, b, ex)
 
 
+def host_cpu():
+    """(CPU model, uname -m) of this host, as far as the system reports them."""
+    import platform
+    model = None
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for ln in r.stdout.splitlines():
+            if ln.split(":")[0].strip() in ("Model name", "Model"):
+                model = ln.split(":", 1)[1].strip()
+                if not model.isdigit():
+                    break
+    except Exception:
+        pass
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for ln in f:
+                    if ln.lower().startswith("model name"):
+                        model = ln.split(":", 1)[1].strip()
+                        break
+        except Exception:
+            pass
+    return model or "unknown", platform.machine()
+
+
+def _time_oracle(fn, budget_s, max_reps=None):
+    reps, t0 = 0, time.time()
+    while True:
+        fn()
+        reps += 1
+        el = time.time() - t0
+        if el >= budget_s or (max_reps and reps >= max_reps):
+            return reps, el
+
+
 def cpu_baseline(cfg, stack, budget_s, dev="cpu", max_reps=None):
-    """The oracle as it stands on this host's cores, on a bounded sample: a few
-    tokens of the workload (through all 8 layers for the stack) repeated until
-    the budget is used.  Returns the cpu_baseline object."""
+    """The oracle as it stands on this host's cores, on a bounded sample: one
+    token of the workload (through all 8 layers for the stack) repeated until
+    the budget is used, with all cores (OpenMP over output rows) and then with
+    one thread.  Returns the cpu_baseline object."""
     import synth
     import oracle
-    T_s = 1 if not stack else 1
-    x = synth.x_rows(cfg, max(1, T_s), "cpu", "cpu-sample").numpy()
+    x = synth.x_rows(cfg, 1, "cpu", "cpu-sample").numpy()
     n_l = 8 if stack else 1
     Ls = [_oracle_layer_for(cfg, x, l, dev) for l in range(n_l)]
     w = synth.norm_weight(cfg).numpy()
-    reps, t0 = 0, time.time()
-    while True:
+
+    def one():
         if stack:
             y = x.copy()
             for L in Ls:
                 y = L.block_forward(y, w, cfg.eps)
         else:
             Ls[0].forward(x)
-        reps += 1
-        el = time.time() - t0
-        if el >= budget_s or (max_reps and reps >= max_reps):
-            break
-    return {"value": reps * x.shape[0] / el, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+
+    cores = oracle.max_threads()
+    reps, el = _time_oracle(one, budget_s, max_reps)
+    oracle.set_threads(1)
+    try:
+        reps1, el1 = _time_oracle(one, budget_s / 3, max_reps)
+    finally:
+        oracle.set_threads(cores)
+    model, machine = host_cpu()
+    return {"value": reps * x.shape[0] / el, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "value_1thread": reps1 * x.shape[0] / el1, "cpu_model": model, "machine": machine,
             "sample": f"{reps} forward(s) of {x.shape[0]} token through {n_l} GLM-shaped layer(s) "
                       f"({'residual block stack' if stack else 'one MoE layer'}), plain C oracle, "
-                      f"{el:.1f} s wall"}
+                      f"{el:.1f} s wall on {cores} threads; {reps1} forward(s) in {el1:.1f} s on 1 thread"}
 
 
 def run_reference(args, cfg, stack, rank):
@@ -574,7 +624,9 @@ def run_reference(args, cfg, stack, rank):
     value = done / el
     sample = (f"{done} of {args.steps} steps timed (time box {args.ref_seconds:.0f} s); each step 1 token "
               f"through {n_l} GLM-shaped layer(s) of the plain C oracle; warm-up {min(args.warmup, 3)}")
-    cpu = {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle", "sample": sample}
+    model, machine = host_cpu()
+    cpu = {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle", "sample": sample,
+           "cpu_model": model, "machine": machine}
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * el / max(done, 1), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int4 weights x int8 activations -> int32, fp32 scales",
@@ -594,6 +646,27 @@ def _has_cuda():
         return False
 
 
+SECONDARY = ("glm_moe_layer_verify_b8", "glm_moe_layer_prefill_2048")
+SECONDARY_KEYS = ("value", "unit", "ms_per_step", "steps", "warmup", "roofline", "e2e", "clocks", "gpu_launches")
+
+
+def secondary_lines(args, rank, world, local):
+    """The other two single-layer workloads of the metric (verify batch 8 and
+    prefill 2048), timed in the same process after the headline with two
+    resident layer weight sets each (9.7 GB, inputs larger than L2)."""
+    out = {}
+    for wl in SECONDARY:
+        line = run_ours(args, wl, rank, world, local, n_layers=2, steps=max(args.steps, 10),
+                        warmup=max(3, min(args.warmup, 20)), with_cpu=False)
+        if line is None:
+            continue
+        sub = {k: line[k] for k in SECONDARY_KEYS}
+        sub["config"] = {k: line["config"][k] for k in ("tokens_per_step", "zipf_skew", "experts_streamed_per_layer",
+                                                        "layer_sets_cycled", "l2", "cuda_graph")}
+        out[wl] = sub
+    return out
+
+
 def main():
     args = parse_args()
     rank, world, local = env_rank()
@@ -605,7 +678,19 @@ def main():
     else:
         if world != args.gpus:
             print(f"warning: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
-        line = run_ours(args, cfg, stack, rank, world, local)
+        import torch
+        dev = torch.device("cuda", local)
+        torch.cuda.set_device(dev)
+        if world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("nccl", device_id=dev)
+        line = run_ours(args, args.workload, rank, world, local)
+        if world == 1 and not args.no_secondary and args.workload == DEFAULT_WORKLOAD:
+            sec = secondary_lines(args, rank, world, local)
+            if line is not None:
+                line["secondary"] = sec
+        if world > 1:
+            torch.distributed.destroy_process_group()
     if line is not None:
         print(json.dumps(line), flush=True)
 

@@ -194,7 +194,7 @@ int moe_layer_debug(void *handle, const float *x, int n_tokens, float *out,
  * Synchronise `stream`, then read and clear the handle's device error word
  * (set by a kernel that met an input outside the contract, e.g. a token with
  * no finite selection score, or a wait of the persistent decode kernel that
- * ran out of time, bit 16; the handle's arrival counters are then cleared).  *status_out (host) receives 0 or the flag bits.
+ * ran out of time, flag value 16; the handle's arrival counters are then cleared).  *status_out (host) receives 0 or the flag bits.
  * Returns MOE_OK, or MOE_ERR_DEVICE when a flag was set.
  */
 int moe_layer_device_status(void *handle, cudaStream_t stream, int *status_out);
@@ -234,7 +234,7 @@ int moe_layer_set_probe(void *handle, int which, cudaEvent_t begin, cudaEvent_t 
 /* Test hook of the failure path, 0 (default) or 1: with 1 the persistent
  * decode kernel's grid barrier (after gate/up) waits for one arrival more
  * than there are CTAs, so that bounded wait runs out (one second) and the
- * launch sets bit 16 in the error word, which moe_layer_device_status
+ * launch sets the flag value 16 in the error word, which moe_layer_device_status
  * reports (clearing the handle's counters); the kernel then runs to its end
  * and its output is still the full result.  Used by the tests to exercise
  * time-out detection without a GPU fault. */
@@ -271,27 +271,55 @@ int moe_layer_workspace_bytes(const MoeLayerDesc *desc, size_t *bytes_out);
  * every byte of the GPU, a runtime with a fixed, pre-planned memory budget, or
  * a latency-critical loop where cudaMalloc (which can synchronise the device)
  * is not allowed.  It takes no handle and calls no cudaMalloc, cudaFree or
- * other allocating routine.
+ * other allocating routine.  It runs the same kernels with the same launch
+ * plan as moe_layer_forward (the single persistent kernel up to 16 tokens,
+ * the tcgen05 expert GEMMs above), so its output equals that of a handle of
+ * the same layer bit for bit.
  *   desc        host: layer sizes (max_tokens is ignored)
  *   Wr, bias    device: as for moe_layer_create
  *   experts_dev DEVICE array of E + n_shared MoeExpertW (entry E = shared
- *               expert), owned by the caller, 16-byte aligned
+ *               expert), owned by the caller, 16-byte aligned.  As for
+ *               moe_layer_create, no pointer in it may be NULL and every
+ *               gate_q / up_q / down_q must be 16-byte aligned; this call
+ *               cannot read the device table to check that, so the caller
+ *               must (the Python binding checks it before copying the table).
  *   x, out      device [n_tokens, D] fp32, 16-byte aligned, out != x
  * The workspace is one static device array of 8 MiB (every GPU that loads the
- * library holds it until the process exits), which bounds the batch: a batch
- * whose workspace does not fit (for the GLM-5.2 layer, more than ~26 tokens)
- * is rejected with MOE_ERR_SHAPE and a message naming the limit.
+ * library holds it until the process exits); its first 256 bytes hold the
+ * error word, the rest bounds the batch: a batch whose workspace
+ * (moe_layer_workspace_bytes with max_tokens = n_tokens) exceeds
+ * 8 MiB - 256 B is rejected with MOE_ERR_SHAPE and a message naming the
+ * limit.  For the GLM-5.2 layer (D 6144, I 2048, E 256, K 8, one shared
+ * expert) that is at most 23 tokens per call.
  * The first call on a device, with that device current, resolves the array's
- * device address (cudaGetSymbolAddress) and reads the SM count; make that first
- * call before any stream capture.  Every call shares the one array and keeps
- * the previous call's contents (the routing tables, counters and error word are
- * cleared at the start of each call): calls that overlap on the GPU -- on two
- * streams, or two threads, at once -- race and must not be issued.
+ * device address (cudaGetSymbolAddress), reads the SM count and sets the
+ * kernels' attributes for this layer shape (kept for later calls, up to 8
+ * shapes per device); make that first call before any stream capture.  A
+ * set-up that failed is tried again by the next call.  Every call shares the
+ * one array and keeps the previous call's contents (the routing tables and
+ * counters are cleared at the start of each call): calls that overlap on the
+ * GPU -- on two streams, or two threads, at once -- race and must not be
+ * issued.
+ * Device-side flags (the same bits moe_layer_device_status reports) collect
+ * in the array's error word across calls until moe_layer_static_status
+ * reads and clears them.
  * Errors: INVALID_ARG, SHAPE, CUDA.
  */
 int moe_layer_forward_static(const MoeLayerDesc *desc, const float *Wr, const float *bias,
                              const MoeExpertW *experts_dev, const float *x, int n_tokens, float *out,
                              cudaStream_t stream);
+
+/*
+ * Error flags of the allocation-free entry point on the current device (no
+ * counterpart on the pages; it allocates nothing either).  Synchronises
+ * `stream`, then reads and clears the static workspace's error word, which
+ * collects the device-side flags of every moe_layer_forward_static call on
+ * this device since the last read (e.g. a token with no finite selection
+ * score, flag value 1; a bounded wait that ran out of time, flag value 16).
+ * *status_out (host) receives 0 or the flag bits.
+ * Returns MOE_OK, MOE_ERR_DEVICE when a flag was set, or INVALID_ARG / CUDA.
+ */
+int moe_layer_static_status(cudaStream_t stream, int *status_out);
 
 #ifdef __cplusplus
 }

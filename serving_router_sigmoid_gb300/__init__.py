@@ -68,6 +68,7 @@ _SIGS = {
     "moe_layer_get_option": ([_vp, _ci, ctypes.POINTER(_ci)], _ci),
     "moe_layer_workspace_bytes": ([ctypes.POINTER(MoeLayerDesc), ctypes.POINTER(ctypes.c_size_t)], _ci),
     "moe_layer_forward_static": ([ctypes.POINTER(MoeLayerDesc), _vp, _vp, _vp, _vp, _ci, _vp, _vp], _ci),
+    "moe_layer_static_status": ([_vp, ctypes.POINTER(_ci)], _ci),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -248,7 +249,15 @@ def workspace_bytes(D, I, E, K, n_shared, max_tokens, routed_scale=2.5) -> int:
 
 def expert_table_device(experts, device):
     """Device copy of a MoeExpertW array (entry E = shared expert) for
-    moe_layer_forward_static; experts as for MoeLayer."""
+    moe_layer_forward_static; experts as for MoeLayer.  The entry point cannot
+    inspect a device table, so the requirements moe_layer_create checks are
+    checked here, on the host: no missing tensor, 16-byte aligned weights."""
+    for e, ts in enumerate(experts):
+        if len(ts) != 6 or any(t is None for t in ts):
+            raise ValueError(f"expert {e}: need six tensors (gate_q, gate_s, up_q, up_s, down_q, down_s)")
+        for name, t in (("gate_q", ts[0]), ("up_q", ts[2]), ("down_q", ts[4])):
+            if t.data_ptr() % 16:
+                raise ValueError(f"expert {e}: {name} must be 16-byte aligned")
     arr = (MoeExpertW * len(experts))()
     for e, (gq, gs, uq, us, dq, ds) in enumerate(experts):
         arr[e] = MoeExpertW(_ptr(gq), _ptr(uq), _ptr(dq), _ptr(gs), _ptr(us), _ptr(ds))
@@ -260,3 +269,13 @@ def moe_layer_forward_static(D, I, E, K, n_shared, routed_scale, Wr, bias, exper
     desc = MoeLayerDesc(D, I, E, K, n_shared, float(routed_scale), max(1, x.shape[0]))
     _check(_lib.moe_layer_forward_static(ctypes.byref(desc), _ptr(Wr), _ptr(bias), _ptr(experts_dev), _ptr(x),
                                          x.shape[0], _ptr(out), _stream(stream)))
+
+
+def static_status(stream=None) -> int:
+    """Reads and clears the device-side flags that moe_layer_forward_static
+    calls on the current device collected (0 when none)."""
+    v = ctypes.c_int(0)
+    rc = _lib.moe_layer_static_status(_stream(stream), ctypes.byref(v))
+    if rc not in (MOE_OK, MOE_ERR_DEVICE):
+        _check(rc)
+    return int(v.value)

@@ -472,9 +472,14 @@ cudaError_t prepare_expert_kernels(int D, int I, int num_sms, int grid_gu[4], in
         MOE_MCH_SWITCH(mch, MOE_CPL_SWITCH(cd, M_, (fd = down_ptr<C, M_, false>())))
         MOE_MCH_SWITCH(mch, MOE_CPL_SWITCH(cd, M_, (fdf = down_ptr<C, M_, true>())))
         const int smem = mch * I;
+        // the attribute belongs to the instantiation, which layers of other
+        // sizes share: set it to the largest tile any of them can need
+        const int smem_max = mch * kMaxDim;
         cudaError_t ce;
-        if ((ce = cudaFuncSetAttribute(fd, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess) return ce;
-        if ((ce = cudaFuncSetAttribute(fdf, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess) return ce;
+        if ((ce = cudaFuncSetAttribute(fd, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max)) != cudaSuccess)
+            return ce;
+        if ((ce = cudaFuncSetAttribute(fdf, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max)) != cudaSuccess)
+            return ce;
         int og = 0, od = 0;
         if ((ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&og, fg, 256, 0)) != cudaSuccess) return ce;
         if ((ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&od, fd, 256, smem)) != cudaSuccess) return ce;

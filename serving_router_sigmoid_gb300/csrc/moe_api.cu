@@ -2,6 +2,7 @@
 // validation, the handle with its device workspace, and the launch sequence of
 // one layer forward.  Every compute step runs in this library's kernels.
 #include <cstdarg>
+#include <cstddef>
 #include <cstdio>
 #include <cstring>
 #include <functional>
@@ -566,26 +567,94 @@ int moe_layer_set_probe(void *handle, int which, cudaEvent_t begin, cudaEvent_t 
 // library holds it until the process exits.  Host code cannot pass the
 // array's name to a kernel (on the host it only stands for the symbol), so
 // its device address is looked up once per device with cudaGetSymbolAddress.
+// The first 256 bytes hold the error word, at a fixed place so that
+// moe_layer_static_status finds it whatever the last call's sizes were; the
+// layer workspace follows.
 namespace {
 
 constexpr size_t kStaticScratchBytes = (size_t)8 << 20;  // 8 MiB
+constexpr size_t kStaticErrBytes = 256;                  // error word (+ padding)
 __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
+// The caller's device table of MoeExpertW is read by the kernels as
+// moe::DevExpert: both must have the same layout.
+static_assert(sizeof(MoeExpertW) == sizeof(moe::DevExpert), "expert table layout");
+static_assert(offsetof(MoeExpertW, gate_q) == offsetof(moe::DevExpert, gq), "expert table layout");
+static_assert(offsetof(MoeExpertW, up_q) == offsetof(moe::DevExpert, uq), "expert table layout");
+static_assert(offsetof(MoeExpertW, down_q) == offsetof(moe::DevExpert, dq), "expert table layout");
+static_assert(offsetof(MoeExpertW, gate_s) == offsetof(moe::DevExpert, gs), "expert table layout");
+static_assert(offsetof(MoeExpertW, up_s) == offsetof(moe::DevExpert, us), "expert table layout");
+static_assert(offsetof(MoeExpertW, down_s) == offsetof(moe::DevExpert, ds), "expert table layout");
+
 constexpr int kMaxDevices = 64;
+constexpr int kStaticPlans = 8;  // launch plans kept per device (distinct layer shapes)
+
+// Grids of one layer shape, as moe_layer_create computes them.
+struct StaticPlan {
+    bool used;
+    int D, I, E, K, n_shared;
+    int grid_gu[4], grid_dn[4];
+    int dec_grid[moe::kSmallT + 1];
+};
+
 struct StaticDeviceState {
-    std::once_flag once;
-    cudaError_t status;
+    bool ready;     // scratch address and SM count resolved
     void *scratch;  // device address of g_static_scratch on this device
     int num_sms;
+    int next;       // plan slot replaced next when all are used
+    StaticPlan plans[kStaticPlans];
 };
+std::mutex g_static_mu;
 StaticDeviceState g_static_dev[kMaxDevices];
 
-// Once per device, with that device current: resolve the scratch address and
-// the launch shapes.  No allocation happens here.
-void static_setup(StaticDeviceState *st, int dev) {
-    st->status = cudaGetSymbolAddress(&st->scratch, g_static_scratch);
-    if (st->status == cudaSuccess)
-        st->status = cudaDeviceGetAttribute(&st->num_sms, cudaDevAttrMultiProcessorCount, dev);
+// With the device current and g_static_mu held: resolve the scratch address
+// and the SM count once per device.  A failure is not remembered, so a later
+// call tries again.  No allocation happens here.
+cudaError_t static_ready(StaticDeviceState &st, int dev) {
+    if (st.ready) return cudaSuccess;
+    void *p = nullptr;
+    int nsm = 0;
+    cudaError_t ce = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (ce == cudaSuccess) ce = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    if (ce != cudaSuccess) {
+        cudaGetLastError();
+        return ce;
+    }
+    st.scratch = p;
+    st.num_sms = nsm;
+    st.ready = true;
+    return cudaSuccess;
+}
+
+// With g_static_mu held: the launch plan of this layer shape, computed (kernel
+// attributes, occupancy) on its first use and kept for later calls.
+cudaError_t static_plan(StaticDeviceState &st, const MoeLayerDesc &d, int dev, const StaticPlan **out) {
+    for (int i = 0; i < kStaticPlans; ++i) {
+        const StaticPlan &p = st.plans[i];
+        if (p.used && p.D == d.D && p.I == d.I && p.E == d.E && p.K == d.K && p.n_shared == d.n_shared) {
+            *out = &p;
+            return cudaSuccess;
+        }
+    }
+    Handle tmp;
+    std::memset(&tmp, 0, sizeof tmp);
+    tmp.device = dev;
+    tmp.d = d;
+    tmp.d.max_tokens = moe::kSmallT;  // decode grids for every decode-sized batch
+    tmp.S = d.K + d.n_shared;
+    tmp.num_sms = st.num_sms;
+    cudaError_t ce = moe::prepare_expert_kernels(d.D, d.I, st.num_sms, tmp.grid_gu, tmp.grid_dn);
+    if (ce == cudaSuccess) ce = prepare_decode(&tmp);
+    if (ce != cudaSuccess) return ce;
+    StaticPlan &p = st.plans[st.next];
+    st.next = (st.next + 1) % kStaticPlans;
+    p.used = true;
+    p.D = d.D; p.I = d.I; p.E = d.E; p.K = d.K; p.n_shared = d.n_shared;
+    std::memcpy(p.grid_gu, tmp.grid_gu, sizeof p.grid_gu);
+    std::memcpy(p.grid_dn, tmp.grid_dn, sizeof p.grid_dn);
+    std::memcpy(p.dec_grid, tmp.dec_grid, sizeof p.dec_grid);
+    *out = &p;
+    return cudaSuccess;
 }
 
 }  // namespace
@@ -600,11 +669,11 @@ extern "C" int moe_layer_forward_static(const MoeLayerDesc *desc, const float *W
     MoeLayerDesc d = *desc;
     d.max_tokens = n_tokens;
     const size_t need = layout(d, nullptr);
-    if (need > kStaticScratchBytes)
+    if (need > kStaticScratchBytes - kStaticErrBytes)
         return fail(MOE_ERR_SHAPE,
                     "n_tokens=%d needs %zu bytes of workspace; the static workspace holds %zu bytes "
                     "(use moe_layer_create/moe_layer_forward for larger batches)",
-                    n_tokens, need, kStaticScratchBytes);
+                    n_tokens, need, kStaticScratchBytes - kStaticErrBytes);
     if (!Wr || !bias || !experts_dev || !x || !out) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
     if (!aligned16(Wr) || !aligned16(x) || !aligned16(out) || !aligned16(experts_dev))
         return fail(MOE_ERR_INVALID_ARG, "Wr, x, out and experts_dev must be 16-byte aligned");
@@ -613,13 +682,23 @@ extern "C" int moe_layer_forward_static(const MoeLayerDesc *desc, const float *W
     cudaError_t ce = cudaGetDevice(&dev);
     if (ce != cudaSuccess) return cuda_fail(ce, "cudaGetDevice");
     if (dev < 0 || dev >= kMaxDevices) return fail(MOE_ERR_INVALID_ARG, "device %d out of range", dev);
-    StaticDeviceState &st = g_static_dev[dev];
-    std::call_once(st.once, static_setup, &st, dev);
-    if (st.status != cudaSuccess) return cuda_fail(st.status, "static workspace set-up");
 
     // a handle that lives on the stack and points into the static workspace
     Handle h;
     std::memset(&h, 0, sizeof h);
+    {
+        std::lock_guard<std::mutex> lk(g_static_mu);
+        StaticDeviceState &st = g_static_dev[dev];
+        if ((ce = static_ready(st, dev)) != cudaSuccess) return cuda_fail(ce, "static workspace set-up");
+        const StaticPlan *plan = nullptr;
+        if ((ce = static_plan(st, d, dev, &plan)) != cudaSuccess) return cuda_fail(ce, "kernel attributes");
+        h.ws = static_cast<char *>(st.scratch) + kStaticErrBytes;
+        h.num_sms = st.num_sms;
+        std::memcpy(h.grid_gu, plan->grid_gu, sizeof h.grid_gu);
+        std::memcpy(h.grid_dn, plan->grid_dn, sizeof h.grid_dn);
+        std::memcpy(h.dec_grid, plan->dec_grid, sizeof h.dec_grid);
+        h.err = static_cast<int32_t *>(st.scratch);
+    }
     h.magic = kMagic;
     h.device = dev;
     h.d = d;
@@ -627,24 +706,46 @@ extern "C" int moe_layer_forward_static(const MoeLayerDesc *desc, const float *W
     h.Wr = Wr;
     h.bias = bias;
     h.experts = reinterpret_cast<moe::DevExpert *>(const_cast<MoeExpertW *>(experts_dev));
-    h.ws = st.scratch;
     h.ws_bytes = need;
+    int32_t *err = h.err;
     layout(d, &h);
+    h.err = err;  // the fixed error word, not the layout's
     h.rpi_gu = kRpiGu;
     h.nb_gu = (d.I + kRpiGu - 1) / kRpiGu;
     h.rpi_dn = kRpiDn;
     h.nb_dn = (d.D + kRpiDn - 1) / kRpiDn;
-    h.num_sms = st.num_sms;
     h.stream_ok = moe::stream_supported(d.D, d.I);
-    if ((ce = moe::prepare_expert_kernels(d.D, d.I, st.num_sms, h.grid_gu, h.grid_dn)) != cudaSuccess ||
-        (ce = prepare_decode(&h)) != cudaSuccess)
-        return cuda_fail(ce, "kernel attributes");
-    // the arrival counters, routing tables and error word must start at zero;
-    // everything else is written before it is read
+    h.single_kernel = true;
+    h.tcgen05_gemm = true;
+    // the arrival counters and routing tables must start at zero (their place
+    // moves with the sizes); everything else is written before it is read.
+    // The error word keeps its flags until moe_layer_static_status reads them.
     if ((ce = cudaMemsetAsync(h.meta, 0, sizeof(moe::RouteMeta), stream)) != cudaSuccess ||
         (ce = cudaMemsetAsync(h.dn_cnt, 0, 4 * (size_t)((d.D + 15) / 16), stream)) != cudaSuccess ||
-        (ce = reset_decode_state(&h, stream)) != cudaSuccess ||
-        (ce = cudaMemsetAsync(h.err, 0, 4, stream)) != cudaSuccess)
+        (ce = reset_decode_state(&h, stream)) != cudaSuccess)
         return cuda_fail(ce, "static workspace clear");
     return run_layer(&h, x, n_tokens, out, nullptr, moe::DebugPtrs{}, stream);
+}
+
+extern "C" int moe_layer_static_status(cudaStream_t stream, int *status_out) {
+    if (!status_out) return fail(MOE_ERR_INVALID_ARG, "status_out is NULL");
+    int dev = -1;
+    cudaError_t ce = cudaGetDevice(&dev);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(MOE_ERR_INVALID_ARG, "device %d out of range", dev);
+    void *scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_static_mu);
+        StaticDeviceState &st = g_static_dev[dev];
+        if ((ce = static_ready(st, dev)) != cudaSuccess) return cuda_fail(ce, "static workspace set-up");
+        scratch = st.scratch;
+    }
+    int v = 0;
+    ce = cudaStreamSynchronize(stream);
+    if (ce == cudaSuccess) ce = cudaMemcpy(&v, scratch, 4, cudaMemcpyDeviceToHost);
+    if (ce == cudaSuccess) ce = cudaMemsetAsync(scratch, 0, 4, stream);
+    if (ce == cudaSuccess) ce = cudaStreamSynchronize(stream);
+    if (ce != cudaSuccess) return cuda_fail(ce, "static status");
+    *status_out = v;
+    return v ? fail(MOE_ERR_DEVICE, "device error flags 0x%x", v) : MOE_OK;
 }

@@ -129,13 +129,21 @@ def check_layer(pair, sample=None, x=None):
     assert np.abs(hq_g.astype(np.int32) - hq_o.astype(np.int32)).max() <= 1
     assert mism <= 1e-4 * hq_g.size, f"{mism} of {hq_g.size} hq codes differ"
     np.testing.assert_allclose(g["sh"][tok], od["sh"], rtol=1e-6, atol=0)
-    # down dots bit-exact against the naive integer dot on the GPU's own hq
-    for j, t in enumerate(tok):
-        for s in range(cfg.S):
-            e = cfg.E if s == cfg.K else int(g["idx"][t, s])
-            dq = unpack_np(pair.oracle_expert(e).dq, cfg.I).astype(np.int32)
-            ad = dq @ g["hq"][t, s].astype(np.int32)
-            np.testing.assert_array_equal(g["down_acc"][t, s], ad)
+    # down dots bit-exact against the plain integer dot of the oracle's
+    # unpacked down weights with the GPU's own hq, one expert at a time (every
+    # (token, slot) row of that expert in one product; the int4 x int8
+    # products and all their partial sums are integers far below 2^53, so a
+    # float64 matrix product of them is exact whatever its summation order)
+    eid = np.empty((len(tok), cfg.S), np.int64)
+    eid[:, :cfg.K] = g["idx"][tok]
+    if cfg.n_shared:
+        eid[:, cfg.K] = cfg.E
+    hq_rows, dn_rows = g["hq"][tok], g["down_acc"][tok]
+    for e in np.unique(eid):
+        sel = eid == e
+        dq = unpack_np(pair.oracle_expert(int(e)).dq, cfg.I).astype(np.float64)
+        ad = hq_rows[sel].astype(np.float64) @ dq.T
+        np.testing.assert_array_equal(dn_rows[sel], ad.astype(np.int64))
     r, m = assert_output_close(got[tok], ref)
     return r, m, mism
 
@@ -222,8 +230,11 @@ def test_layer_rejects_bad_arguments(moe):
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name,sample", [("glm_decode_b1", None), ("glm_verify_b8", None),
-                                         ("glm_prefill_2048", [0, 1, 511, 1024, 2046, 2047])])
+                                         ("glm_prefill_2048", None)])
 def test_glm_layer_parity(moe, name, sample):
+    """The GLM-shaped layer at decode batch 1, verify batch 8 and prefill 2048
+    tokens (Zipf-skewed routing: the hottest expert gets ~300 tokens, several
+    tcgen05 token blocks), every token compared with the oracle."""
     cfg = synth.CONFIGS[name]
     pair = LayerPair(cfg, wdev="cuda")
     try:
