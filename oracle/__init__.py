@@ -78,6 +78,10 @@ def lib():
         L.orc_layer_forward.restype = ci
         L.orc_block_forward.argtypes = [ctypes.POINTER(_Layer), vp, vp, cf, ci]
         L.orc_block_forward.restype = ci
+        L.orc_fp8_e4m3_decode.argtypes = [ctypes.c_uint8]
+        L.orc_fp8_e4m3_decode.restype = cf
+        L.orc_fp8_block_dequant.argtypes = [vp, vp, vp, i64, i64]
+        L.orc_fp8_block_to_int4.argtypes = [vp, vp, vp, vp, i64, i64]
         L.orc_set_threads.argtypes = [ci]
         L.orc_max_threads.restype = ci
         _lib = L
@@ -108,6 +112,36 @@ def pack_int4(w):
     q4 = np.empty((O, (I + 1) // 2), np.uint8)
     s = np.empty(O, np.float32)
     lib().orc_pack_int4(_p(w), _p(q4), _p(s), O, I)
+    return q4, s
+
+
+def fp8_e4m3_decode(b):
+    """uint8 array of FP8 E4M3 codes -> fp32 values (same shape)."""
+    b = np.asarray(b, dtype=np.uint8)
+    f = lib().orc_fp8_e4m3_decode
+    return np.array([f(int(v)) for v in b.reshape(-1)], np.float32).reshape(b.shape)
+
+
+def fp8_block_dequant(w8, scale_inv):
+    """w8 [O, I] uint8 E4M3 codes, scale_inv [ceil(O/128), ceil(I/128)] fp32 -> fp32 [O, I]."""
+    w8 = _c(w8, np.uint8)
+    O, I = w8.shape
+    si = _c(scale_inv, np.float32)
+    assert si.shape == ((O + 127) // 128, (I + 127) // 128)
+    w = np.empty((O, I), np.float32)
+    lib().orc_fp8_block_dequant(_p(w8), _p(si), _p(w), O, I)
+    return w
+
+
+def fp8_block_to_int4(w8, scale_inv):
+    """The converter step: block dequantisation then int4 packing -> (q4, scale)."""
+    w8 = _c(w8, np.uint8)
+    O, I = w8.shape
+    si = _c(scale_inv, np.float32)
+    assert si.shape == ((O + 127) // 128, (I + 127) // 128)
+    q4 = np.empty((O, (I + 1) // 2), np.uint8)
+    s = np.empty(O, np.float32)
+    lib().orc_fp8_block_to_int4(_p(w8), _p(si), _p(q4), _p(s), O, I)
     return q4, s
 
 

@@ -86,6 +86,45 @@ void orc_pack_int4(const float *w, uint8_t *q4, float *scale, int64_t O, int64_t
     }
 }
 
+/* ---------------------------------------------------------------------------
+ * FP8 checkpoint decoding.  [A] §06 "FP8 block scale 解码" and the model
+ * config (quant_method fp8, fmt e4m3, weight_block_size [128, 128]); [B] §06.
+ * The checkpoint stores each weight as one FP8 E4M3 byte and one fp32
+ * scale_inv per 128 x 128 block; the converter widens the bytes to fp32 and
+ * multiplies element (o, i) by scale_inv[o / 128][i / 128] (an fp32 product),
+ * then packs the result to int4 with the row packer below.
+ *
+ * E4M3 ("fn" variant, the only one with 448 as its largest value): bit 7 is
+ * the sign, bits 6..3 the exponent e (bias 7), bits 2..0 the mantissa m.
+ * e > 0: (1 + m/8) * 2^(e-7); e == 0: (m/8) * 2^-6 (subnormal); the codes
+ * S.1111.111 are NaN and there is no infinity.  Written from that definition.
+ * ------------------------------------------------------------------------- */
+float orc_fp8_e4m3_decode(uint8_t b) {
+    const int neg = b >> 7, e = (b >> 3) & 15, m = b & 7;
+    if (e == 15 && m == 7) return NAN;
+    /* both cases are an integer times a power of two: exact in fp32 */
+    const float v = e == 0 ? ldexpf((float)m, -9) : ldexpf((float)(8 + m), e - 10);
+    return neg ? -v : v;
+}
+
+void orc_fp8_block_dequant(const uint8_t *w8, const float *scale_inv, float *w, int64_t O, int64_t I) {
+    const int64_t nbi = (I + 127) / 128;  /* scale blocks per row of blocks */
+#pragma omp parallel for schedule(static)
+    for (int64_t o = 0; o < O; o++)
+        for (int64_t i = 0; i < I; i++)
+            w[o * I + i] = orc_fp8_e4m3_decode(w8[o * I + i]) * scale_inv[(o / 128) * nbi + i / 128];
+}
+
+/* The converter's whole step for one FP8 matrix: block dequantisation, then
+ * the int4 row packer ([A] §06: dequant, then quant_int4 / pack_int4). */
+void orc_fp8_block_to_int4(const uint8_t *w8, const float *scale_inv, uint8_t *q4, float *scale, int64_t O,
+                           int64_t I) {
+    float *w = (float *)malloc(sizeof(float) * (size_t)(O * I) + 4);
+    orc_fp8_block_dequant(w8, scale_inv, w, O, I);
+    orc_pack_int4(w, q4, scale, O, I);
+    free(w);
+}
+
 /* Inverse of the nibble layout: value = nibble - 8.  [A] §06 worked example. */
 static inline int nibble_value(const uint8_t *row, int64_t i) {
     uint8_t b = row[i >> 1];

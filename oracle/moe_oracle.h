@@ -8,8 +8,10 @@
  *
  * Sources (the only authority on what the layer computes):
  *   [A] reader.mx, "惊呆了！25GB 内存上运行 GLM 5.2 744B 模型":
+ *       §02 model config (FP8 e4m3 checkpoint, 128 x 128 weight blocks),
  *       §04 手写的基础数学 (rmsnorm, siluf, layer order),
- *       §06 从 FP8 到 int4 (per-row int4 packer, nibble layout, worked example),
+ *       §06 从 FP8 到 int4 (FP8 block-scale decoding, per-row int4 packer,
+ *           nibble layout, worked example),
  *       §11 MoE 路由与专家执行 (sigmoid+bias top-K router, expert union, SwiGLU),
  *       §12 AVX2 整数 kernel (per-row int8 activation quantiser, integer dot).
  *   [B] besthub.dev, "Running 744B MoE on 25GB RAM: Int4, Disk Streaming & MLA
@@ -68,6 +70,14 @@ int   orc_max_threads(void);
 
 void  orc_pack_int4(const float *w, uint8_t *q4, float *scale, int64_t O, int64_t I);
 void  orc_unpack_int4(const uint8_t *q4, int8_t *v, int64_t O, int64_t I);
+/* FP8 E4M3 weights with one fp32 scale_inv per 128 x 128 block (the
+ * checkpoint format, [A] §06): decode one byte; dequantise a matrix
+ * w8 [O, I] with scale_inv [ceil(O/128), ceil(I/128)] to fp32; or dequantise
+ * and pack to int4 in one call (q4 / scale as orc_pack_int4). */
+float orc_fp8_e4m3_decode(uint8_t b);
+void  orc_fp8_block_dequant(const uint8_t *w8, const float *scale_inv, float *w, int64_t O, int64_t I);
+void  orc_fp8_block_to_int4(const uint8_t *w8, const float *scale_inv, uint8_t *q4, float *scale, int64_t O,
+                            int64_t I);
 float orc_qrow_i8(const float *x, int8_t *q, int64_t n);
 void  orc_quant_act(const float *x, int8_t *xq, float *sx, int64_t T, int64_t D);
 int32_t orc_dot_i4_i8(const uint8_t *q4row, const int8_t *x, int64_t n);

@@ -389,3 +389,95 @@ def test_block_is_residual_of_layer_on_rmsnorm():
     np.testing.assert_array_equal(got, ref)
     # rmsnorm makes the block invariant to the scale of x up to the residual
     assert np.abs(got - x).max() > 0
+
+
+# ------------------------------------------------------ FP8 checkpoint step --
+# reader.mx §06 "FP8 block scale 解码": E4M3 bytes widened to fp32 times the
+# fp32 scale_inv of their 128 x 128 block, then the int4 row packer.
+
+def _read_fp8_example():
+    vals = {}
+    with open(os.path.join(GOLDEN, "fp8_block_example.txt")) as f:
+        for line in f:
+            if line.startswith("#") or ":" not in line:
+                continue
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.split()
+    codes = np.array([int(s, 16) for s in vals["fp8_codes"]], np.uint8)
+    return (codes, np.float32(vals["scale_inv"][0]), np.float32(vals["row_scale"][0]),
+            np.array([int(s, 16) for s in vals["int4_bytes"]], np.uint8))
+
+
+def test_fp8_decode_matches_torch_float8_e4m3fn_on_every_code():
+    """All 256 codes against torch's own float8_e4m3fn type (an independent
+    implementation of the format); NaN codes are NaN on both sides."""
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.fp8_e4m3_decode(codes)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).float().numpy()
+    np.testing.assert_array_equal(np.isnan(got), np.isnan(ref))
+    assert np.isnan(got).sum() == 2  # S.1111.111 only: the fn variant has no infinities
+    ok = ~np.isnan(ref)
+    np.testing.assert_array_equal(got[ok], ref[ok])
+    np.testing.assert_array_equal(np.signbit(got[ok]), np.signbit(ref[ok]))
+
+
+def test_fp8_decode_closed_forms():
+    cases = {0x00: 0.0, 0x38: 1.0, 0x7E: 448.0, 0xFE: -448.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9,
+             0x08: 2.0 ** -6, 0x3F: 1.875, 0x40: 2.0, 0x4E: 7.0, 0xB8: -1.0}
+    for code, v in cases.items():
+        assert oracle.fp8_e4m3_decode(np.array([code], np.uint8))[0] == np.float32(v), hex(code)
+
+
+def test_fp8_block_dequant_power_of_two_scales_pin_the_block_index():
+    """Ragged shape (partial last blocks on both axes); every block gets its own
+    power-of-two scale, so each product is exact and equals the decoded value
+    times that block's power of two: a wrong block size, a transposed block
+    index or a wrong row of blocks fails."""
+    rng = np.random.default_rng(3)
+    O, I = 300, 260
+    codes = rng.integers(0, 256, size=(O, I), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x11  # no NaN codes
+    nbo, nbi = (O + 127) // 128, (I + 127) // 128
+    k = np.arange(nbo * nbi).reshape(nbo, nbi) - 4
+    si = np.ldexp(np.float32(1.0), k).astype(np.float32)
+    w = oracle.fp8_block_dequant(codes, si)
+    dec = oracle.fp8_e4m3_decode(codes).astype(np.float64)
+    kk = k[np.arange(O)[:, None] // 128, np.arange(I)[None, :] // 128]
+    np.testing.assert_array_equal(w.astype(np.float64), np.ldexp(dec, kk))
+
+
+def test_fp8_block_dequant_general_scales_against_torch():
+    """Arbitrary fp32 scales: each element is one fp32 product, the same as
+    torch's widening of float8_e4m3fn times the block-repeated scale."""
+    import torch
+    rng = np.random.default_rng(4)
+    O, I = 257, 384
+    codes = rng.integers(0, 256, size=(O, I), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x22
+    si = rng.uniform(1e-4, 1e-2, size=((O + 127) // 128, (I + 127) // 128)).astype(np.float32)
+    w = oracle.fp8_block_dequant(codes, si)
+    wt = torch.from_numpy(codes).view(torch.float8_e4m3fn).float()
+    st = torch.from_numpy(si).repeat_interleave(128, 0).repeat_interleave(128, 1)[:O, :I]
+    np.testing.assert_array_equal(w, (wt * st).numpy())
+
+
+def test_fp8_to_int4_hand_worked_row():
+    codes, si, s_ref, b_ref = _read_fp8_example()
+    q4, s = oracle.fp8_block_to_int4(codes[None, :], np.array([[si]], np.float32))
+    assert s[0] == s_ref
+    np.testing.assert_array_equal(q4[0], b_ref)
+
+
+def test_fp8_to_int4_is_dequant_then_pack():
+    rng = np.random.default_rng(5)
+    O, I = 129, 1001
+    codes = rng.integers(0, 256, size=(O, I), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x33
+    codes[7] = 0  # an all-zero row takes the 1e-8 floor
+    si = rng.uniform(1e-3, 1e-1, size=((O + 127) // 128, (I + 127) // 128)).astype(np.float32)
+    q4, s = oracle.fp8_block_to_int4(codes, si)
+    q4b, sb = _numpy_converter(oracle.fp8_block_dequant(codes, si))
+    np.testing.assert_array_equal(q4, q4b)
+    np.testing.assert_array_equal(s, sb)
+    assert s[7] == np.float32(1e-8) and (q4[7] == 0x88).all()
