@@ -48,6 +48,8 @@ WORKLOADS = {
     "glm_moe_layer_prefill_2048": ("glm_prefill_2048", False),
     "glm_moe_stack8_decode_b1": ("glm_stack8_b1", True),
     "glm_moe_stack8_decode_b8": ("glm_stack8_b8", True),
+    # the checkpoint converter step (not a layer forward): GB/s, not tokens/s
+    "glm_fp8_to_int4": (None, False),
 }
 DEFAULT_WORKLOAD = "glm_moe_layer_decode_b1"
 # Dominant kernel per path: decode batches (<= 16 tokens) stream the weights
@@ -646,6 +648,51 @@ def _has_cuda():
         return False
 
 
+def run_fp8_converter(args, local, n_experts=64, steps=20, warmup=5):
+    """The checkpoint converter step (FP8 E4M3 with 128 x 128 block scales ->
+    packed int4 + row scales) on the stacked gate matrices of n_experts
+    GLM-shaped experts: [n_experts * 2048, 6144] codes (805 MB at 64, far
+    larger than L2).  HBM-bound: algorithmic bytes = codes read + packed bytes
+    written + scales, per launch."""
+    import torch
+    import serving_router_sigmoid_gb300 as moe
+    import synth
+    dev = torch.device("cuda", local)
+    O, I = n_experts * 2048, 6144
+    codes, si = synth.fp8_checkpoint_matrix(O, I, seed=77, device=dev)
+    q4 = torch.empty((O, I // 2), dtype=torch.uint8, device=dev)
+    sc = torch.empty(O, dtype=torch.float32, device=dev)
+    s = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(s):
+        for _ in range(warmup):
+            moe.moe_fp8_block_to_int4(codes, si, q4, sc, stream=s)
+        s.synchronize()
+        clocks = ClockSampler(local)
+        clocks.start()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(steps):
+            moe.moe_fp8_block_to_int4(codes, si, q4, sc, stream=s)
+        e1.record(s)
+        s.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / steps
+    nbytes = O * I + O * (I // 2) + 4 * O + 4 * si.numel()
+    peak, peak_kind = measured_peak("hbm_gbs")
+    achieved = nbytes / (ms / 1e3) / 1e9
+    del codes, si, q4, sc
+    torch.cuda.empty_cache()
+    return {"metric": "FP8 E4M3 block-scaled -> int4 converter throughput", "value": achieved, "unit": "GB/s",
+            "ms_per_step": ms, "steps": steps, "warmup": warmup,
+            "config": {"rows": O, "cols": I, "matrices": f"{n_experts} stacked GLM gate matrices",
+                       "l2": "inputs larger than L2 (805 MB of codes per launch)"},
+            "roofline": {"bound": "hbm", "kernel": "fp8_to_int4_kernel<12>", "achieved": achieved, "peak": peak,
+                         "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind + " HBM copy bandwidth",
+                         "traffic": TRAFFIC.get("glm_fp8_to_int4"), "algorithmic_bytes_per_launch": nbytes,
+                         "avg_launch_ms": ms, "launches_timed": steps},
+            "gpu_launches": steps, "clocks": clk}
+
+
 SECONDARY = ("glm_moe_layer_verify_b8", "glm_moe_layer_prefill_2048")
 SECONDARY_KEYS = ("value", "unit", "ms_per_step", "steps", "warmup", "roofline", "e2e", "clocks", "gpu_launches")
 
@@ -664,6 +711,8 @@ def secondary_lines(args, rank, world, local):
         sub["config"] = {k: line["config"][k] for k in ("tokens_per_step", "zipf_skew", "experts_streamed_per_layer",
                                                         "layer_sets_cycled", "l2", "cuda_graph")}
         out[wl] = sub
+    if rank == 0:
+        out["glm_fp8_to_int4"] = run_fp8_converter(args, local)
     return out
 
 
@@ -671,6 +720,14 @@ def main():
     args = parse_args()
     rank, world, local = env_rank()
     import synth
+    if args.workload == "glm_fp8_to_int4":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the layer forward only"}))
+            return
+        import torch
+        torch.cuda.set_device(local)
+        print(json.dumps(run_fp8_converter(args, local, steps=args.steps, warmup=max(3, args.warmup))), flush=True)
+        return
     cfg = synth.CONFIGS[WORKLOADS[args.workload][0]]
     stack = WORKLOADS[args.workload][1]
     if args.impl == "reference":

@@ -73,6 +73,27 @@ int moe_pack_int4(const float *w, uint8_t *q4, float *scale, int64_t O, int64_t 
                   cudaStream_t stream);
 
 /*
+ * The checkpoint converter's step: an FP8 weight matrix to the packed int4
+ * layout.  reader.mx article §02 (checkpoint config: fmt e4m3,
+ * weight_block_size [128, 128]) and §06 (FP8 block-scale decoding, then the
+ * per-row int4 packer); besthub.dev §06.
+ *   w8        [O, I] uint8 FP8 E4M3 codes, row-major ("fn" variant: sign,
+ *             4 exponent bits with bias 7, 3 mantissa bits, no infinities)
+ *   scale_inv [ceil(O/128), ceil(I/128)] fp32, row-major: the factor of the
+ *             128 x 128 block that holds element (o, i)
+ *   q4, scale as moe_pack_int4 (outputs)
+ * Computes w = e4m3(w8[o, i]) * scale_inv[o/128][i/128] (one fp32 product)
+ * and packs w exactly as moe_pack_int4 does: byte-exact with packing the
+ * dequantised fp32 matrix, without ever forming it (one read of w8, one write
+ * of q4).  Fastest when I % 16 == 0, I <= 8192, w8 16-byte and q4 8-byte
+ * aligned; any shape and alignment is accepted.  The NaN codes (0x7F, 0xFF)
+ * are outside the contract.
+ * Errors: INVALID_ARG for NULL pointers, SHAPE for O < 0, I < 0 or O*I >= 2^62.
+ */
+int moe_fp8_block_to_int4(const uint8_t *w8, const float *scale_inv, uint8_t *q4, float *scale, int64_t O,
+                          int64_t I, cudaStream_t stream);
+
+/*
  * Per-token int8 activation quantiser.
  * reader.mx article §12 (qrow_i8); besthub.dev §12.
  *   x  [n_tokens, D] fp32 row-major;  xq [n_tokens, D] int8 out (natural

@@ -54,6 +54,7 @@ _SIGS = {
     "moe_last_error": ([], ctypes.c_char_p),
     "moe_pack_int4": ([_vp, _vp, _vp, _i64, _i64, _vp], _ci),
     "moe_quant_act_int8": ([_vp, _vp, _vp, _ci, _ci, _vp], _ci),
+    "moe_fp8_block_to_int4": ([_vp, _vp, _vp, _vp, _i64, _i64, _vp], _ci),
     "moe_router_topk": ([_vp, _vp, _vp, _ci, _ci, _ci, _ci, _cf, _vp, _vp, _vp], _ci),
     "moe_layer_create": ([ctypes.POINTER(MoeLayerDesc), _vp, _vp, ctypes.POINTER(MoeExpertW),
                           ctypes.POINTER(_vp)], _ci),
@@ -129,6 +130,23 @@ def moe_router_topk(x, Wr, bias, K, routed_scale, idx, w, stream=None):
     E = Wr.shape[0]
     _check(_lib.moe_router_topk(_ptr(x), _ptr(Wr), _ptr(bias), T, D, E, K, float(routed_scale),
                                 _ptr(idx), _ptr(w), _stream(stream)))
+
+
+def moe_fp8_block_to_int4(w8, scale_inv, q4, scale, stream=None):
+    """w8 [O, I] uint8 E4M3 codes, scale_inv [ceil(O/128), ceil(I/128)] fp32 -> q4, scale (outputs)."""
+    O, I = w8.shape
+    if tuple(scale_inv.shape) != ((O + 127) // 128, (I + 127) // 128):
+        raise ValueError("scale_inv must be [ceil(O/128), ceil(I/128)]")
+    _check(_lib.moe_fp8_block_to_int4(_ptr(w8), _ptr(scale_inv), _ptr(q4), _ptr(scale), O, I, _stream(stream)))
+
+
+def fp8_block_to_int4(w8, scale_inv, stream=None):
+    """Allocating convenience wrapper of moe_fp8_block_to_int4 -> (q4, scale)."""
+    O, I = w8.shape
+    q4 = torch.empty((O, (I + 1) // 2), dtype=torch.uint8, device=w8.device)
+    s = torch.empty(O, dtype=torch.float32, device=w8.device)
+    moe_fp8_block_to_int4(w8, scale_inv, q4, s, stream)
+    return q4, s
 
 
 def pack_int4(w, stream=None):

@@ -1,0 +1,184 @@
+// k_fp8.cu -- the checkpoint converter's step on the GPU: an FP8 E4M3 weight
+// matrix with one fp32 scale_inv per 128 x 128 block, dequantised and packed
+// to the int4 layout with one fp32 scale per row, in one pass over HBM.
+//
+// Sources: reader.mx "惊呆了！25GB 内存上运行 GLM 5.2 744B 模型" §02 (the
+// checkpoint config: quant_method fp8, fmt e4m3, weight_block_size
+// [128, 128]) and §06 从 FP8 到 int4 (FP8 block-scale decoding: the bytes
+// widened to fp32 times the block's scale_inv; then the per-row int4 packer:
+// s = max(amax / 7, 1e-8), nearest integer of w / s with ties to even, clamped
+// to [-8, 7], stored +8 as nibbles, element 2j low); besthub.dev "Running 744B
+// MoE on 25GB RAM" §06.
+//
+// Design (GB300).  The step is HBM-bound: 1 byte read and half a byte written
+// per weight.  One warp owns one row at a time; a row of up to 8192 codes is
+// read once into registers with 16-byte loads (all of a lane's loads issued
+// before any use), so the amax pass and the packing pass read no memory
+// twice and no fp32 copy of the matrix exists.  A 16-byte chunk lies inside
+// one 128-column block, so each chunk needs one scale.  E4M3 is sign-magnitude
+// with a monotone encoding, so the largest |value| of a chunk is the one of its
+// largest 7-bit magnitude code, and (rounding being monotone) the chunk's
+// largest |w| is that value times the block scale: the amax pass costs a few
+// byte-max instructions per chunk.  The widening uses the hardware e4m3x2 ->
+// f16x2 conversion (exact: every E4M3 value is an f16 value), then f16 -> f32
+// (exact).  Rows that are not a multiple of 16 codes, longer than 8192 or
+// unaligned take a plain per-element path with the same arithmetic.
+#include "layer_args.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kWarpsPerCta = 8;
+constexpr int kMaxCpl = 16;  // 16-byte chunks per lane: rows of up to 32 * 16 * 16 = 8192 codes
+
+// Two E4M3 codes (low byte -> .x) widened to fp32, exactly.
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two) {
+    uint32_t h;
+    asm("{\n .reg .b16 lo;\n cvt.u16.u32 lo, %1;\n cvt.rn.f16x2.e4m3x2 %0, lo;\n}" : "=r"(h) : "r"(two));
+    float2 r;
+    asm("{\n .reg .f16 a, b;\n mov.b32 {a, b}, %2;\n cvt.f32.f16 %0, a;\n cvt.f32.f16 %1, b;\n}"
+        : "=f"(r.x), "=f"(r.y)
+        : "r"(h));
+    return r;
+}
+
+// The packer's code of one dequantised value: nearest integer of w / s (IEEE
+// division, ties to even), clamped to [-8, 7], plus 8.
+__device__ __forceinline__ uint32_t nibble_of(float w, float s) {
+    const int v = __float2int_rn(__fdiv_rn(w, s));
+    return (uint32_t)(min(7, max(-8, v)) + 8);
+}
+
+// One word of four codes at block scale sc -> the two packed bytes of its four
+// elements (low 16 bits of the result).
+__device__ __forceinline__ uint32_t pack_word(uint32_t w, float sc, float s) {
+    const float2 a = e4m3x2_to_f32x2(w & 0xFFFFu), b = e4m3x2_to_f32x2(w >> 16);
+    const uint32_t n0 = nibble_of(__fmul_rn(a.x, sc), s), n1 = nibble_of(__fmul_rn(a.y, sc), s);
+    const uint32_t n2 = nibble_of(__fmul_rn(b.x, sc), s), n3 = nibble_of(__fmul_rn(b.y, sc), s);
+    return n0 | (n1 << 4) | (n2 << 8) | (n3 << 12);
+}
+
+// Largest magnitude code (0..127) among the 16 codes of a chunk.
+__device__ __forceinline__ uint32_t max_mag_code(int4 c) {
+    const uint32_t m = 0x7F7F7F7Fu;
+    uint32_t v = __vmaxu4(__vmaxu4((uint32_t)c.x & m, (uint32_t)c.y & m), __vmaxu4((uint32_t)c.z & m, (uint32_t)c.w & m));
+    v = __vmaxu4(v, v >> 16);
+    v = __vmaxu4(v, v >> 8);
+    return v & 0xFFu;
+}
+
+__device__ __forceinline__ float row_scale(float amax) {
+    float s = __fdiv_rn(amax, 7.f);
+    return s < 1e-8f ? 1e-8f : s;
+}
+
+// Rows of I = 16 * nch codes (nch <= 32 * CPL), 16-byte aligned rows.
+template <int CPL>
+__global__ void __launch_bounds__(32 * kWarpsPerCta) fp8_to_int4_kernel(const uint8_t *__restrict__ w8,
+                                                                         const float *__restrict__ si,
+                                                                         uint8_t *__restrict__ q4,
+                                                                         float *__restrict__ scale, long long O,
+                                                                         int I) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nch = I >> 4, nbi = (I + 127) >> 7;
+    const long long stride = (long long)gridDim.x * kWarpsPerCta;
+    for (long long o = (long long)blockIdx.x * kWarpsPerCta + warp; o < O; o += stride) {
+        const uint8_t *row = w8 + o * I;
+        const float *srow = si + (o >> 7) * nbi;
+        int4 raw[CPL];
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            const int c = lane + 32 * j;
+            raw[j] = c < nch ? ld_stream16(row + 16 * c) : make_int4(0, 0, 0, 0);
+        }
+        float sc[CPL];
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            const int c = lane + 32 * j;
+            sc[j] = c < nch ? __ldg(srow + (c >> 3)) : 0.f;
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            const float v = e4m3x2_to_f32x2(max_mag_code(raw[j])).x;
+            amax = fmaxf(amax, fabsf(__fmul_rn(v, sc[j])));
+        }
+        amax = warp_max_f(amax);
+        const float s = row_scale(amax);
+        if (lane == 0) scale[o] = s;
+        uint8_t *qrow = q4 + o * (I >> 1);
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            const int c = lane + 32 * j;
+            if (c < nch) {
+                const uint32_t p0 = pack_word((uint32_t)raw[j].x, sc[j], s), p1 = pack_word((uint32_t)raw[j].y, sc[j], s);
+                const uint32_t p2 = pack_word((uint32_t)raw[j].z, sc[j], s), p3 = pack_word((uint32_t)raw[j].w, sc[j], s);
+                *reinterpret_cast<uint2 *>(qrow + 8 * c) = make_uint2(p0 | (p1 << 16), p2 | (p3 << 16));
+            }
+        }
+    }
+}
+
+// Any shape and alignment: per element, reading the row twice.
+__global__ void __launch_bounds__(32 * kWarpsPerCta) fp8_to_int4_any_kernel(const uint8_t *__restrict__ w8,
+                                                                             const float *__restrict__ si,
+                                                                             uint8_t *__restrict__ q4,
+                                                                             float *__restrict__ scale, long long O,
+                                                                             long long I) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long nbi = (I + 127) >> 7, nb = (I + 1) >> 1;
+    const long long stride = (long long)gridDim.x * kWarpsPerCta;
+    for (long long o = (long long)blockIdx.x * kWarpsPerCta + warp; o < O; o += stride) {
+        const uint8_t *row = w8 + o * I;
+        const float *srow = si + (o >> 7) * nbi;
+        float amax = 0.f;
+        for (long long i = lane; i < I; i += 32)
+            amax = fmaxf(amax, fabsf(__fmul_rn(e4m3x2_to_f32x2(row[i]).x, __ldg(srow + (i >> 7)))));
+        amax = warp_max_f(amax);
+        const float s = row_scale(amax);
+        if (lane == 0) scale[o] = s;
+        for (long long j = lane; j < nb; j += 32) {
+            const long long i = 2 * j;
+            const uint32_t lo = nibble_of(__fmul_rn(e4m3x2_to_f32x2(row[i]).x, __ldg(srow + (i >> 7))), s);
+            const uint32_t hi =
+                i + 1 < I ? nibble_of(__fmul_rn(e4m3x2_to_f32x2(row[i + 1]).x, __ldg(srow + ((i + 1) >> 7))), s)
+                          : 8u;
+            q4[o * nb + j] = (uint8_t)(lo | (hi << 4));
+        }
+    }
+}
+
+template <int CPL>
+cudaError_t launch_fast(const uint8_t *w8, const float *si, uint8_t *q4, float *scale, int64_t O, int64_t I,
+                        int grid, cudaStream_t s) {
+    fp8_to_int4_kernel<CPL><<<grid, 32 * kWarpsPerCta, 0, s>>>(w8, si, q4, scale, O, (int)I);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fp8_to_int4(const uint8_t *w8, const float *si, uint8_t *q4, float *scale, int64_t O, int64_t I,
+                               cudaStream_t s) {
+    int dev = 0, nsm = 0;
+    cudaError_t ce = cudaGetDevice(&dev);
+    if (ce == cudaSuccess) ce = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    if (ce != cudaSuccess) return ce;
+    // a persistent grid: rows are handed out by a grid-stride loop
+    const int64_t ctas = (O + kWarpsPerCta - 1) / kWarpsPerCta;
+    const int per_sm = 8;
+    const int grid = (int)(ctas < (int64_t)nsm * per_sm ? ctas : (int64_t)nsm * per_sm);
+    const bool fast = I > 0 && I % 16 == 0 && I <= 512 * kMaxCpl &&
+                      (reinterpret_cast<uintptr_t>(w8) & 15u) == 0 && (reinterpret_cast<uintptr_t>(q4) & 7u) == 0;
+    if (fast) {
+        const int64_t cpl = (I / 16 + 31) / 32;
+        if (cpl <= 4) return launch_fast<4>(w8, si, q4, scale, O, I, grid, s);
+        if (cpl <= 8) return launch_fast<8>(w8, si, q4, scale, O, I, grid, s);
+        if (cpl <= 12) return launch_fast<12>(w8, si, q4, scale, O, I, grid, s);
+        return launch_fast<16>(w8, si, q4, scale, O, I, grid, s);
+    }
+    fp8_to_int4_any_kernel<<<grid, 32 * kWarpsPerCta, 0, s>>>(w8, si, q4, scale, O, I);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -64,6 +64,9 @@ cudaError_t launch_quant_natural(const float *x, int8_t *xq, float *sx, int T, i
                                  cudaStream_t s);
 cudaError_t launch_pack_int4(const float *w, uint8_t *q4, float *scale, int64_t O, int64_t I,
                              cudaStream_t s);
+// FP8 E4M3 matrix with 128 x 128 block scales -> packed int4 + row scales.
+cudaError_t launch_fp8_to_int4(const uint8_t *w8, const float *scale_inv, uint8_t *q4, float *scale, int64_t O,
+                               int64_t I, cudaStream_t s);
 cudaError_t launch_gateup_stream(const LayerArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_down_stream(const LayerArgs &a, int grid, cudaStream_t s);
 bool stream_supported(int D, int I);

@@ -314,6 +314,16 @@ int moe_pack_int4(const float *w, uint8_t *q4, float *scale, int64_t O, int64_t 
     return ce == cudaSuccess ? MOE_OK : cuda_fail(ce, "pack_int4 launch");
 }
 
+int moe_fp8_block_to_int4(const uint8_t *w8, const float *scale_inv, uint8_t *q4, float *scale, int64_t O,
+                          int64_t I, cudaStream_t stream) {
+    if (O < 0 || I < 0) return fail(MOE_ERR_SHAPE, "O=%lld I=%lld must be >= 0", (long long)O, (long long)I);
+    if (O == 0) return MOE_OK;
+    if (I > 0 && O > ((int64_t)1 << 62) / I) return fail(MOE_ERR_SHAPE, "O*I too large");
+    if (!w8 || !scale_inv || !q4 || !scale) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+    cudaError_t ce = moe::launch_fp8_to_int4(w8, scale_inv, q4, scale, O, I, stream);
+    return ce == cudaSuccess ? MOE_OK : cuda_fail(ce, "fp8_to_int4 launch");
+}
+
 int moe_quant_act_int8(const float *x, int8_t *xq, float *sx, int n_tokens, int D, cudaStream_t stream) {
     if (n_tokens < 0 || D < 1) return fail(MOE_ERR_SHAPE, "n_tokens=%d D=%d", n_tokens, D);
     if (n_tokens == 0) return MOE_OK;

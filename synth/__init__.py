@@ -143,3 +143,21 @@ def expert_bytes(cfg: LayerCfg) -> int:
     gu = cfg.I * ((cfg.D + 1) // 2) + cfg.I * 4
     dn = cfg.D * ((cfg.I + 1) // 2) + cfg.D * 4
     return 2 * gu + dn
+
+
+def fp8_checkpoint_matrix(O: int, I: int, seed, device="cpu", std: float = 0.02):
+    """An FP8 E4M3 weight matrix as a block-scaled checkpoint stores it:
+    w ~ N(0, std) fp32, one scale_inv per 128 x 128 block = block amax / 448
+    (the largest E4M3 value), codes = w / scale_inv rounded to E4M3 by torch's
+    float8_e4m3fn cast.  Returns (codes [O, I] uint8, scale_inv fp32
+    [ceil(O/128), ceil(I/128)]).  Input generation only: the converter under
+    test decodes these codes, nothing here packs to int4."""
+    w = normal((O, I), std, device, "fp8-ckpt", seed)
+    bo, bi = (O + 127) // 128, (I + 127) // 128
+    pad = torch.zeros((bo * 128, bi * 128), dtype=torch.float32, device=device)
+    pad[:O, :I] = w.abs()
+    amax = pad.view(bo, 128, bi, 128).amax(dim=(1, 3))
+    si = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax)).float()
+    full = si.repeat_interleave(128, 0).repeat_interleave(128, 1)[:O, :I]
+    codes = (w / full).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes.contiguous(), si.contiguous()

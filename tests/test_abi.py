@@ -48,6 +48,9 @@ def test_host_validation_without_gpu(lib):
     assert lib.moe_pack_int4(None, None, None, 0, 5, None) == moe.MOE_OK  # empty: nothing to do
     assert lib.moe_pack_int4(None, None, None, 3, 5, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_quant_act_int8(None, None, None, 2, 0, None) == moe.MOE_ERR_SHAPE
+    assert lib.moe_fp8_block_to_int4(None, None, None, None, -1, 16, None) == moe.MOE_ERR_SHAPE
+    assert lib.moe_fp8_block_to_int4(None, None, None, None, 0, 16, None) == moe.MOE_OK
+    assert lib.moe_fp8_block_to_int4(None, None, None, None, 2, 16, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_router_topk(None, None, None, 1, 64, 16, 17, 2.5, None, None, None) == moe.MOE_ERR_SHAPE
     for bad in (dict(D=100), dict(I=0), dict(E=0), dict(E=600), dict(K=9, E=8), dict(n_shared=2),
                 dict(max_tokens=0)):

@@ -105,9 +105,35 @@ def check_layer(pair, sample=None, x=None):
     OL = pair.oracle_layer(xs)
     ref, od = OL.forward(xs, debug=True)
 
-    # routing: identical expert ids in selection order, weights to rounding
-    np.testing.assert_array_equal(g["idx"][tok], od["idx"])
-    np.testing.assert_allclose(g["w"][tok], od["w"], rtol=2e-6, atol=0)
+    # routing.  The set of experts of each token is identical (the inputs keep
+    # a margin of >= 1e-5 between the K-th and (K+1)-th score).  The selection
+    # order is identical except inside runs of consecutive picks whose oracle
+    # scores c = sigmoid(logit) + bias lie within 1e-5 of each other: there it
+    # follows the last bits of the logits, which the GPU sums in another fp32
+    # order, and both orders are correct.  Every per-slot array is compared
+    # after mapping each oracle slot to the GPU slot holding the same expert.
+    gi, oi = g["idx"][tok], od["idx"]
+    np.testing.assert_array_equal(np.sort(gi, 1), np.sort(oi, 1))
+    _, _, p_or = oracle.router(xs, pair.Wr.numpy(), pair.bias.numpy(), cfg.K, cfg.routed_scale)
+    c_or = (p_or + pair.bias.numpy()[None, :]).astype(np.float32)
+    c_pick = np.take_along_axis(c_or, oi.astype(np.int64), 1)
+    run = np.concatenate([np.zeros((len(tok), 1), np.int64),
+                          np.cumsum(np.abs(np.diff(c_pick, axis=1)) >= 1e-5, axis=1)], axis=1)
+    perm = np.empty((len(tok), cfg.S), np.int64)
+    for j in range(len(tok)):
+        pos = {int(e): k for k, e in enumerate(gi[j])}
+        perm[j, :cfg.K] = [pos[int(e)] for e in oi[j]]
+        # the GPU slot of every pick lies inside the pick's run of near ties
+        assert all(run[j, perm[j, k]] == run[j, k] for k in range(cfg.K)), (j, gi[j], oi[j])
+    if cfg.n_shared:
+        perm[:, cfg.K] = cfg.K
+    n_swapped = int((perm[:, :cfg.K] != np.arange(cfg.K)[None, :]).any(axis=1).sum())
+
+    def by_oracle_slot(a, slots=cfg.S):
+        p = perm[:, :slots].reshape(perm.shape[0], slots, *([1] * (a.ndim - 2)))
+        return np.take_along_axis(a, p, 1)
+
+    np.testing.assert_allclose(by_oracle_slot(g["w"][tok], cfg.K), od["w"], rtol=2e-6, atol=0)
     # int8 activations bit-exact
     np.testing.assert_array_equal(g["xq"][tok], od["xq"])
     np.testing.assert_array_equal(g["sx"][tok], od["sx"])
@@ -122,13 +148,15 @@ def check_layer(pair, sample=None, x=None):
     if sample is None:
         assert set(routed.tolist()) == set(od["uniq"].tolist())
     # exact int32 dot products
-    np.testing.assert_array_equal(g["gate_acc"][tok], od["gate_acc"])
-    np.testing.assert_array_equal(g["up_acc"][tok], od["up_acc"])
-    hq_g, hq_o = g["hq"][tok], od["hq"]
+    np.testing.assert_array_equal(by_oracle_slot(g["gate_acc"][tok]), od["gate_acc"])
+    np.testing.assert_array_equal(by_oracle_slot(g["up_acc"][tok]), od["up_acc"])
+    hq_g, hq_o = by_oracle_slot(g["hq"][tok]), od["hq"]
     mism = int(np.count_nonzero(hq_g != hq_o))
     assert np.abs(hq_g.astype(np.int32) - hq_o.astype(np.int32)).max() <= 1
     assert mism <= 1e-4 * hq_g.size, f"{mism} of {hq_g.size} hq codes differ"
-    np.testing.assert_allclose(g["sh"][tok], od["sh"], rtol=1e-6, atol=0)
+    np.testing.assert_allclose(by_oracle_slot(g["sh"][tok]), od["sh"], rtol=1e-6, atol=0)
+    if n_swapped:
+        print(f"{n_swapped} token(s) with near-tied picks in another order")
     # down dots bit-exact against the plain integer dot of the oracle's
     # unpacked down weights with the GPU's own hq, one expert at a time (every
     # (token, slot) row of that expert in one product; the int4 x int8
