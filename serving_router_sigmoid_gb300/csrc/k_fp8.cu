@@ -21,7 +21,8 @@
 // largest |w| is that value times the block scale: the amax pass costs a few
 // byte-max instructions per chunk.  The widening uses the hardware e4m3x2 ->
 // f16x2 conversion (exact: every E4M3 value is an f16 value), then f16 -> f32
-// (exact).  Rows that are not a multiple of 16 codes, longer than 8192 or
+// (exact).  The division of the packer is replaced, where that provably gives
+// the same code, by a product with the row's reciprocal (nibble_fast).  Rows that are not a multiple of 16 codes, longer than 8192 or
 // unaligned take a plain per-element path with the same arithmetic.
 #include "layer_args.cuh"
 
@@ -50,12 +51,31 @@ __device__ __forceinline__ uint32_t nibble_of(float w, float s) {
     return (uint32_t)(min(7, max(-8, v)) + 8);
 }
 
-// One word of four codes at block scale sc -> the two packed bytes of its four
-// elements (low 16 bits of the result).
-__device__ __forceinline__ uint32_t pack_word(uint32_t w, float sc, float s) {
+// The same code without the division where that is provably safe.  With
+// inv = fl(1/s) and g = fl(sc * inv), y = fl(v * g) differs from the packer's
+// quotient fl(fl(v * sc) / s) by at most five roundings of relative size
+// 2^-24 of a quotient whose magnitude is at most 7 (|w| <= amax, s >= amax/7
+// rounded): less than 2^-18.  So when y lies farther than 2^-17 from every
+// half-integer, both round to the same integer; otherwise (ties and near
+// ties) the quotient is formed exactly as the packer forms it.  Rounding y to
+// an integer: adding M = 1.5 * 2^23 + 8 rounds at integer granularity with
+// ties to even (M is even) and leaves 8 + nearest(y) in the low four bits of
+// the sum (|nearest(y)| <= 7, so no borrow or carry leaves the nibble).
+__device__ __forceinline__ uint32_t nibble_fast(float v, float g, float sc, float s) {
+    constexpr float kM = 12582920.f;  // 1.5 * 2^23 + 8
+    const float y = __fmul_rn(v, g);
+    const float z = __fadd_rn(y, kM);
+    const float r = __fsub_rn(y, __fsub_rn(z, kM));  // y - nearest(y), exact
+    if (fabsf(r) < 0.5f - 7.62939453125e-06f) return __float_as_uint(z) & 15u;  // 2^-17 from any half
+    return nibble_of(__fmul_rn(v, sc), s);
+}
+
+// One word of four codes at block scale sc (g = fl(sc * fl(1/s))) -> the two
+// packed bytes of its four elements (low 16 bits of the result).
+__device__ __forceinline__ uint32_t pack_word(uint32_t w, float sc, float g, float s) {
     const float2 a = e4m3x2_to_f32x2(w & 0xFFFFu), b = e4m3x2_to_f32x2(w >> 16);
-    const uint32_t n0 = nibble_of(__fmul_rn(a.x, sc), s), n1 = nibble_of(__fmul_rn(a.y, sc), s);
-    const uint32_t n2 = nibble_of(__fmul_rn(b.x, sc), s), n3 = nibble_of(__fmul_rn(b.y, sc), s);
+    const uint32_t n0 = nibble_fast(a.x, g, sc, s), n1 = nibble_fast(a.y, g, sc, s);
+    const uint32_t n2 = nibble_fast(b.x, g, sc, s), n3 = nibble_fast(b.y, g, sc, s);
     return n0 | (n1 << 4) | (n2 << 8) | (n3 << 12);
 }
 
@@ -108,12 +128,14 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) fp8_to_int4_kernel(const ui
         const float s = row_scale(amax);
         if (lane == 0) scale[o] = s;
         uint8_t *qrow = q4 + o * (I >> 1);
+        const float inv = __fdiv_rn(1.f, s);
 #pragma unroll
         for (int j = 0; j < CPL; ++j) {
             const int c = lane + 32 * j;
             if (c < nch) {
-                const uint32_t p0 = pack_word((uint32_t)raw[j].x, sc[j], s), p1 = pack_word((uint32_t)raw[j].y, sc[j], s);
-                const uint32_t p2 = pack_word((uint32_t)raw[j].z, sc[j], s), p3 = pack_word((uint32_t)raw[j].w, sc[j], s);
+                const float g = __fmul_rn(sc[j], inv), scj = sc[j];
+                const uint32_t p0 = pack_word((uint32_t)raw[j].x, scj, g, s), p1 = pack_word((uint32_t)raw[j].y, scj, g, s);
+                const uint32_t p2 = pack_word((uint32_t)raw[j].z, scj, g, s), p3 = pack_word((uint32_t)raw[j].w, scj, g, s);
                 *reinterpret_cast<uint2 *>(qrow + 8 * c) = make_uint2(p0 | (p1 << 16), p2 | (p3 << 16));
             }
         }

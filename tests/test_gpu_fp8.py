@@ -87,3 +87,21 @@ def test_argument_errors(moe):
     assert lib.moe_fp8_block_to_int4(None, None, None, None, -1, 16, None) == moe.MOE_ERR_SHAPE
     assert lib.moe_fp8_block_to_int4(None, None, None, None, 0, 16, None) == moe.MOE_OK
     assert lib.moe_fp8_block_to_int4(None, None, None, None, 2, 16, None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_near_ties_take_the_exact_quotient(moe):
+    """Columns 0..127 hold +-7 at scale_inv 0.5 (row scale s = 0.5); columns
+    128..255 hold 1.5, 2.5, -2.5, 0.5, 3.5, -3.5, 0, -1.5 at a scale_inv a few
+    ulps away from 0.5, so their quotients w / s sit within a few ulps of
+    half-integers (where a product with the reciprocal may round otherwise
+    than the packer's division): still byte-exact."""
+    nb = 9
+    blk0 = np.tile(np.array([0x4E, 0xCE], np.uint8), (nb * 128, 64))
+    blk1 = np.tile(np.array([0x3C, 0x42, 0xC2, 0x30, 0x46, 0xC6, 0x00, 0xBC], np.uint8), (nb * 128, 16))
+    codes = np.concatenate([blk0, blk1], axis=1)
+    si = np.empty((nb, 2), np.float32)
+    si[:, 0] = 0.5
+    si[:, 1] = (np.float32(0.5) * (1 + (np.arange(nb) - 4) * np.float32(2.0 ** -21))).astype(np.float32)
+    rq, _ = oracle.fp8_block_to_int4(codes, si)
+    assert len({bytes(rq[128 * j, 64:68]) for j in range(nb)}) > 1  # the near ties round both ways
+    _check(moe, torch.from_numpy(codes), torch.from_numpy(si))
