@@ -311,7 +311,7 @@ int moe_layer_workspace_bytes(const MoeLayerDesc *desc, size_t *bytes_out);
  * (moe_layer_workspace_bytes with max_tokens = n_tokens) exceeds
  * 8 MiB - 256 B is rejected with MOE_ERR_SHAPE and a message naming the
  * limit.  For the GLM-5.2 layer (D 6144, I 2048, E 256, K 8, one shared
- * expert) that is at most 23 tokens per call.
+ * expert) that is at most 18 tokens per call.
  * The first call on a device, with that device current, resolves the array's
  * device address (cudaGetSymbolAddress), reads the SM count and sets the
  * kernels' attributes for this layer shape (kept for later calls, up to 8

@@ -19,6 +19,8 @@
 // of the 128-element chunk.  Tiles are ordered (expert, weight block, token
 // block) so the token blocks of one weight block run back to back and share
 // it through L2.  A persistent grid walks the tiles.
+#include <cuda_fp16.h>
+
 #include "layer_args.cuh"
 
 namespace moe {
@@ -315,6 +317,12 @@ __global__ void __launch_bounds__(256) requant_h_kernel(LayerArgs a) {
         const uint32_t ev = (q0 & 255) | ((q2 & 255) << 8) | ((q4 & 255) << 16) | ((uint32_t)(q6 & 255) << 24);
         const uint32_t od = (q1 & 255) | ((q3 & 255) << 8) | ((q5 & 255) << 16) | ((uint32_t)(q7 & 255) << 24);
         *reinterpret_cast<uint2 *>(a.hq + (size_t)r * I + 8 * gi) = make_uint2(ev, od);
+        if (a.xf) {  // the tcgen05 GEMM's operand: the same codes as f16 integers, same order
+            auto h2 = [](int lo, int hi) {
+                return (uint32_t)__half_as_ushort(__int2half_rn(lo)) | ((uint32_t)__half_as_ushort(__int2half_rn(hi)) << 16);
+            };
+            *reinterpret_cast<uint4 *>(a.xf + (size_t)r * I + 8 * gi) = make_uint4(h2(q0, q2), h2(q4, q6), h2(q1, q3), h2(q5, q7));
+        }
         if (a.dbg.hq) {
             const uint32_t n0 = (q0 & 255) | ((q1 & 255) << 8) | ((q2 & 255) << 16) | ((uint32_t)(q3 & 255) << 24);
             const uint32_t n1 = (q4 & 255) | ((q5 & 255) << 8) | ((q6 & 255) << 16) | ((uint32_t)(q7 & 255) << 24);

@@ -20,32 +20,42 @@
 // waste at most 15 token columns.  For gate/up the 128 rows are 64 gate rows
 // interleaved with the same 64 up rows, so one lane shuffle pairs g and u in
 // the epilogue.  K runs in stages of 64.
-//  - One CTA per SM, 25 warps: 4 epilogue warps (TMEM lanes 0..127), two
-//    groups of 8 converter warps (even and odd stages), 1 MMA warp, 4 load
-//    warps.
+//  - The activation operand is not converted here: a small kernel before the
+//    GEMM writes every grouped row of the batch (gate/up: the token's int8
+//    codes; down: the requantised h codes) as f16 integers, once, and one
+//    producer thread moves each stage's token tile into shared memory with
+//    TMA tile loads (boxes of 32 rows x 64 f16 = 128 bytes per row, 128-byte
+//    swizzle: the K-major layout the MMA reads).  Rows past the tile's tokens
+//    belong to the next entry (or lie past the tensor and read as zeros):
+//    their accumulator columns are computed and ignored.
+//  - One CTA per SM, 26 warps: 4 epilogue warps (TMEM lanes 0..127), two
+//    groups of 8 converter warps (even and odd stages), 1 MMA warp, 4 weight
+//    load warps, 1 activation TMA warp.
 //  - The load warps copy the weight rows of 4 stages at a time into a
 //    4-slot raw ring with 16-byte cp.async (32 rows per warp, 8 lanes per
 //    128-byte row, so every warp instruction is fully coalesced); each
-//    lane's copies arrive on the slot's barrier when they land.
-//    Converter thread c of a group owns fixed 16-byte chunks of each of its
-//    stages (one weight chunk, up to two activation chunks); it copies its
-//    activation chunks itself with cp.async 6 stages ahead, so no other
-//    thread waits on them, then expands both operands to f16 (a byte permute
-//    into 0x64xx patterns and one f16x2 subtraction per pair) into the
-//    128-byte-swizzled K-major layout the MMA reads, and its warp arrives on
-//    the stage's barrier.  The packed weight nibbles
-//    come out in the order e0 e2 e4 e6 e1 e3 e5 e7 of each 8-group, which is
-//    exactly the even/odd order in which the activations are stored, so both
-//    operands see the same permutation of K.
-//  - The MMA thread issues four K=16 MMAs per stage and commits them to the
-//    stage's "empty" barrier; after a tile's last stage to an accumulator
-//    barrier.  Two 128-column TMEM accumulators let the epilogue of one tile
-//    overlap the MMAs of the next.
+//    lane's copies arrive on the slot's barrier when they land.  Converter
+//    thread c of a group owns one fixed 16-byte chunk of each of its stages,
+//    expands it to f16 (a byte permute into 0x64xx patterns and one f16x2
+//    subtraction per pair) and stores it into TMEM (the MMA's A operand); its
+//    warp then arrives on the stage's barrier.  The packed weight nibbles come
+//    out in the order e0 e2 e4 e6 e1 e3 e5 e7 of each 8-group, which is
+//    exactly the even/odd order in which the activation rows are stored, so
+//    both operands see the same permutation of K.
+//  - The MMA thread waits for a stage's weights (converter barrier) and its
+//    token tile (TMA transaction barrier), issues four K=16 MMAs and commits
+//    them to the stage's "empty" barrier; after a tile's last stage to an
+//    accumulator barrier.  Two 128-column TMEM accumulators let the epilogue
+//    of one tile overlap the MMAs of the next.
 //  - Epilogue: tcgen05.ld 32 columns at a time; gate/up: h = silu(g)*u, max|h|
 //    per token row; down: y = (acc*sh)*sd into the per-slot partial rows.
 // Every barrier wait is bounded (one second of %globaltimer); a time-out sets
 // kErrSyncTimeout and an abort flag every role polls, the MMA thread drains
-// its outstanding MMAs (bounded) and the TMEM is freed before the CTA exits.
+// its outstanding MMAs (bounded), the copy issuers wait (bounded) for their
+// copies in flight, and the TMEM is freed before the CTA exits.
+#include <cuda.h>
+#include <cuda_fp16.h>
+
 #include "layer_args.cuh"
 
 namespace moe {
@@ -53,34 +63,34 @@ namespace moe {
 namespace {
 
 constexpr int kGU = 0, kDN = 1;
-constexpr int kThreads = 800;             // 25 warps
+constexpr int kThreads = 832;             // 26 warps
 constexpr int kConv0 = 128;               // first converter thread: two groups of 8 warps
 constexpr int kMmaWarp = 20;
-constexpr int kLoadWarp0 = 21;            // four load warps
+constexpr int kLoadWarp0 = 21;            // four weight load warps
 constexpr int kLoadWarps = 4;
+constexpr int kTmaWarp = 25;              // activation tiles
 constexpr int kBKs = 64;                  // K elements per stage
 constexpr int kTok = 128;                 // token columns per tile at most
-constexpr int kSt = 5;                    // operand stages (weights in TMEM, activations in shared memory)
+constexpr int kBoxRows = 32;              // token rows per TMA box
+constexpr int kSt = 6;                    // operand stages (weights in TMEM, activations in shared memory)
 constexpr int kRA = 4;                    // weight raw ring: slots of up to 4 stages (128 bytes per row)
-constexpr int kRB = 6;                    // activation raw ring (stages of lookahead)
 constexpr uint32_t kBF16 = kTok * 128;    // 128 tokens x 64 f16
 constexpr uint32_t kARowPitch = 144;      // raw weight row pitch: 128 bytes + 16 of padding
 // raw weight row r sits at r * pitch (+64 for the second 64-row half), so the
 // 16-byte reads of 8 consecutive tile rows fall in 8 different bank groups
 __device__ __forceinline__ uint32_t raw_row_off(int r) { return (uint32_t)r * kARowPitch + (r >= 64 ? 64u : 0u); }
 constexpr uint32_t kARaw = 128 * kARowPitch + 64;  // 128 rows x up to 4 stages of 64 int4
-constexpr uint32_t kBRaw = kTok * 64;     // 128 tokens x 64 int8
 constexpr uint32_t kOffB = 0;
 constexpr uint32_t kOffRA = kOffB + kSt * kBF16;
-constexpr uint32_t kOffRB = kOffRA + kRA * kARaw;
-constexpr uint32_t kDyn = kOffRB + kRB * kBRaw;  // 200 KB
+constexpr uint32_t kDyn = kOffRA + kRA * kARaw;  // 170 KB
 constexpr size_t kSmemBytes = kDyn + 1024;       // + alignment to 1024 bytes
 constexpr uint32_t kTmemCols = 512;       // accumulators [0, 256), weight stages [256, 256 + 32 kSt)
 constexpr uint32_t kTmemA = 2 * kTok;     // first weight-stage column
 constexpr uint32_t kAcolStage = 32;       // columns per weight stage: 64 f16 as 32 pairs
+static_assert(kTmemA + kSt * kAcolStage <= kTmemCols, "TMEM columns");
 
 struct UmmaSmem {
-    uint64_t full[kSt], empty[kSt], acc_full[2], acc_empty[2], drain;
+    uint64_t full[kSt], bfull[kSt], empty[kSt], acc_full[2], acc_empty[2], drain;
     uint64_t raw_full[kRA], raw_empty[kRA];
     uint32_t tmem;
     int abort;
@@ -158,9 +168,6 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t *b) {
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // tcgen05 shared-memory descriptor: K-major, 128-byte swizzle, 8-row atoms
 // 1024 bytes apart; the atom base is 1024-byte aligned and the start address
@@ -172,11 +179,6 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
 // Instruction descriptor of kind::f16: f16 A and B, K-major, fp32 D, M = 128.
 __device__ __forceinline__ uint32_t idesc_f16(int n) {
     return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
-}
-// Byte offset of 16-byte chunk c (K positions 8c..8c+7) of row r in a
-// 128-byte-swizzled tile.
-__device__ __forceinline__ uint32_t sw_off(int r, int c) {
-    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
 __device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
@@ -191,10 +193,14 @@ __device__ __forceinline__ uint4 w4_to_f16(uint32_t w) {
     return make_uint4(hsub2(__byte_perm(lo, m, 0x4140), k), hsub2(__byte_perm(lo, m, 0x4342), k),
                       hsub2(__byte_perm(hi, m, 0x4140), k), hsub2(__byte_perm(hi, m, 0x4342), k));
 }
-// Four int8 activations -> two f16 pairs, the byte order kept.
-__device__ __forceinline__ uint2 x8_to_f16(uint32_t x) {
-    const uint32_t u = x ^ 0x80808080u, m = 0x64646464u, k = 0x64806480u;
-    return make_uint2(hsub2(__byte_perm(u, m, 0x4140), k), hsub2(__byte_perm(u, m, 0x4342), k));
+// TMA tile load of a 2D f16 tensor (box of the map) into shared memory,
+// completing on the barrier's transaction count.  c0 = element column (a
+// multiple of 64 here: 128-byte aligned), c1 = row.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(su32(bar))
+        : "memory");
 }
 
 struct Tile {
@@ -220,7 +226,7 @@ __device__ __forceinline__ Tile tile_of(const LayerArgs &a, const UmmaSmem &sm, 
 }
 
 template <int KIND>
-__global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(LayerArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, LayerArgs a) {
     extern __shared__ uint8_t dyn_raw[];
     __shared__ UmmaSmem sm;
     uint8_t *dyn = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dyn_raw) + 1023) & ~uintptr_t(1023));
@@ -244,7 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(LayerArgs a) {
         sm.tp[nu] = run;
         sm.abort = 0;
         for (int s = 0; s < kSt; ++s) {
-            mb_init(&sm.full[s], 8);
+            mb_init(&sm.full[s], 8);   // the 8 converter warps of the stage's group
+            mb_init(&sm.bfull[s], 1);  // the TMA issuer's arrival, plus the tile's bytes
             mb_init(&sm.empty[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
@@ -269,118 +276,47 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(LayerArgs a) {
     const uint32_t tmem = sm.tmem;
     const int n_tiles = sm.tp[nu];
     const int n_my = b < n_tiles ? (n_tiles - b + G - 1) / G : 0;
+    const int n_stages = n_my * kst;
 
     if (tid >= kConv0 && tid < kConv0 + 512) {
         // ------------------------------------------------------ converters
         const int grp = (tid - kConv0) >> 8;      // this group converts stages i = grp (mod 2)
         const int ct = (tid - kConv0) & 255;
-        // weights: the warp writes its TMEM lane quarter (warp % 4); tile row
+        // the warp writes its TMEM lane quarter (warp % 4); tile row
         // m = 32 * quarter + lane, 16-byte half ah = converter warp / 4; raw
         // row ra holds tile row m (gate/up rows interleave: m = 2i gate, 2i+1 up)
         const int cw = ct >> 5, m = 32 * (warp & 3) + lane, ah = cw >> 2;
         const int ra = KIND == kGU ? ((m & 1) * 64 + (m >> 1)) : m;
-        const int bj = ct >> 2, bq = ct & 3;      // activation chunks: token rows bj, bj + 64, quarter bq
         const int lch = ch == 4 ? 2 : ch == 2 ? 1 : 0;
-        const int n_stages = n_my * kst;
-        // activation copies run kRB stages (kRB / 2 of this group's) ahead in
-        // this thread's own cp.async groups; the source rows of its two token
-        // columns are looked up once per tile
-        int bi = grp, bti = 0, bks = grp;  // issue front: stage, its tile and stage in the tile
-        while (bks >= kst) { bks -= kst; ++bti; }
-        int b_ti = -1, b_npad = 0, b_nvalid = 0;
-        const int8_t *b_src[2] = {nullptr, nullptr};
-        auto issue_b = [&]() {
-            if (bi < n_stages) {
-                if (bti != b_ti) {
-                    b_ti = bti;
-                    const Tile bt = tile_of(a, sm, nu, nwb, b + bti * G);
-                    b_npad = bt.npad;
-                    b_nvalid = bt.nvalid;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int j = bj + 64 * h;
-                        const bool ok = j < bt.nvalid;
-                        if (KIND == kGU) {
-                            const int tok = ok ? a.rows[bt.r0 + j] / S : 0;
-                            b_src[h] = a.xq + (size_t)tok * kdim;
-                        } else {
-                            b_src[h] = a.hq + (size_t)(ok ? bt.r0 + j : 0) * kdim;
-                        }
-                    }
-                }
-                const uint32_t slot = sbase + kOffRB + (uint32_t)(bi % kRB) * kBRaw;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int j = bj + 64 * h;
-                    if (j < b_npad)
-                        cp_async16(slot + j * 64 + bq * 16, b_src[h] + bks * 64 + bq * 16, j < b_nvalid ? 16u : 0u);
-                }
-            }
-            cp_async_commit();
-            bi += 2;
-            bks += 2;
-            while (bks >= kst) { bks -= kst; ++bti; }
-        };
-        for (int k2 = 0; k2 < kRB / 2; ++k2) issue_b();  // prologue: this group's first kRB / 2 stages
-        int c_ti = -1, c_npad = 0;
-        int ti = 0, ks = grp;  // the stage being converted: its tile and stage in the tile
-        while (ks >= kst) { ks -= kst; ++ti; }
-        int fs = grp, use3 = 0, bslot = grp;  // f16 slot (i % kSt) and use (i / kSt); raw activation slot (i % kRB)
+        int fs = grp, use3 = 0;  // TMEM stage slot (i % kSt) and its use (i / kSt)
         for (int i = grp; i < n_stages; i += 2) {
-            cp_async_wait<kRB / 2 - 1>();  // this thread's copies of stage i have landed
             const int q = i >> lch, within = i & (ch - 1), rs = q & (kRA - 1);
             bool ok = true;
             if (within < 2) ok = mb_wait(&sm.raw_full[rs], (uint32_t)((q / kRA) & 1), abort, a.err);
             if (ok && i >= kSt) ok = mb_wait(&sm.empty[fs], (uint32_t)((use3 - 1) & 1), abort, a.err);
             if (__any_sync(0xffffffffu, !ok)) break;  // the whole warp leaves together
-            if (ti != c_ti) {
-                c_ti = ti;
-                c_npad = tile_of(a, sm, nu, nwb, b + ti * G).npad;
-            }
-            // weights: 4 packed words -> 16 f16 pairs of tile row m, to TMEM
+            // 4 packed words -> 16 f16 pairs of tile row m, to TMEM
             const uint4 w = *reinterpret_cast<const uint4 *>(dyn + kOffRA + (uint32_t)rs * kARaw + raw_row_off(ra) +
                                                              within * 32 + ah * 16);
             if (within + 2 >= ch) {  // this group's last stage of the slot: one arrival per warp
                 __syncwarp();
                 if (lane == 0) mb_arrive(&sm.raw_empty[rs]);
             }
-            {
-                const uint4 p0 = w4_to_f16(w.x), p1 = w4_to_f16(w.y), p2 = w4_to_f16(w.z), p3 = w4_to_f16(w.w);
-                const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kTmemA + (uint32_t)fs * kAcolStage +
-                                    (uint32_t)ah * 16;
-                asm volatile(
-                    "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(ta),
-                    "r"(p0.x), "r"(p0.y), "r"(p0.z), "r"(p0.w), "r"(p1.x), "r"(p1.y), "r"(p1.z), "r"(p1.w), "r"(p2.x),
-                    "r"(p2.y), "r"(p2.z), "r"(p2.w), "r"(p3.x), "r"(p3.y), "r"(p3.z), "r"(p3.w)
-                    : "memory");
-            }
-            // activations: per token row 16 bytes = two 8-groups -> two f16 chunks
-            uint8_t *fb = dyn + kOffB + (uint32_t)fs * kBF16;
-            const uint8_t *rb = dyn + kOffRB + (uint32_t)bslot * kBRaw;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int j = bj + 64 * h;
-                if (j >= c_npad) continue;
-                const uint4 x = *reinterpret_cast<const uint4 *>(rb + j * 64 + bq * 16);
-                const uint2 g0a = x8_to_f16(x.x), g0b = x8_to_f16(x.y), g1a = x8_to_f16(x.z), g1b = x8_to_f16(x.w);
-                *reinterpret_cast<uint4 *>(fb + sw_off(j, 2 * bq)) = make_uint4(g0a.x, g0a.y, g0b.x, g0b.y);
-                *reinterpret_cast<uint4 *>(fb + sw_off(j, 2 * bq + 1)) = make_uint4(g1a.x, g1a.y, g1b.x, g1b.y);
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // activations: to the MMA's proxy
-            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");    // weights: in TMEM
+            const uint4 p0 = w4_to_f16(w.x), p1 = w4_to_f16(w.y), p2 = w4_to_f16(w.z), p3 = w4_to_f16(w.w);
+            const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kTmemA + (uint32_t)fs * kAcolStage +
+                                (uint32_t)ah * 16;
+            asm volatile(
+                "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(ta),
+                "r"(p0.x), "r"(p0.y), "r"(p0.z), "r"(p0.w), "r"(p1.x), "r"(p1.y), "r"(p1.z), "r"(p1.w), "r"(p2.x),
+                "r"(p2.y), "r"(p2.z), "r"(p2.w), "r"(p3.x), "r"(p3.y), "r"(p3.z), "r"(p3.w)
+                : "memory");
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
             if (lane == 0) mb_arrive(&sm.full[fs]);
-            issue_b();
-            // next stage of this group: i + 2
-            ks += 2;
-            while (ks >= kst) { ks -= kst; ++ti; }
             fs += 2;
             if (fs >= kSt) { fs -= kSt; ++use3; }
-            bslot += 2;
-            if (bslot >= kRB) bslot -= kRB;
         }
-        cp_async_wait<0>();
     } else if (warp == kMmaWarp) {
         // ----------------------------------------------------------- MMA
         if (lane == 0) {
@@ -394,7 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(LayerArgs a) {
                 bool ok = true;
                 for (int ks = 0; ks < kst; ++ks) {
                     const int i = ti * kst + ks, fs = i % kSt;
-                    if (!mb_wait(&sm.full[fs], (uint32_t)((i / kSt) & 1), abort, a.err)) {
+                    const uint32_t ph = (uint32_t)((i / kSt) & 1);
+                    if (!mb_wait(&sm.full[fs], ph, abort, a.err) || !mb_wait(&sm.bfull[fs], ph, abort, a.err)) {
                         ok = false;
                         break;
                     }
@@ -429,6 +366,36 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(LayerArgs a) {
                 }
         }
         __syncwarp();
+    } else if (warp == kTmaWarp) {
+        // -------------------------------------------- activation tiles (TMA)
+        if (lane == 0) {
+            int issued = 0, t_ti = -1, nbox = 0, r0 = 0;
+            for (int i = 0; i < n_stages && !*abort; ++i) {
+                const int ti = i / kst, ks = i - ti * kst, fs = i % kSt;
+                if (ti != t_ti) {
+                    t_ti = ti;
+                    const Tile x = tile_of(a, sm, nu, nwb, b + ti * G);
+                    nbox = (x.npad + kBoxRows - 1) / kBoxRows;
+                    r0 = x.r0;
+                }
+                // the slot is free once the MMAs that read it have completed
+                if (i >= kSt && !mb_wait(&sm.empty[fs], (uint32_t)(((i / kSt) - 1) & 1), abort, a.err)) break;
+                mb_expect_tx(&sm.bfull[fs], (uint32_t)nbox * kBoxRows * 128u);
+                const uint32_t dst = sbase + kOffB + (uint32_t)fs * kBF16;
+                for (int bx = 0; bx < nbox; ++bx)
+                    tma_load_2d(dst + (uint32_t)bx * kBoxRows * 128u, &xmap, ks * kBKs, r0 + kBoxRows * bx, &sm.bfull[fs]);
+                issued = i + 1;
+            }
+            // tiles still in flight land before the CTA may leave (bounded)
+            const unsigned long long t0 = global_ns();
+            for (int i = issued - kSt < 0 ? 0 : issued - kSt; i < issued; ++i)
+                while (!mb_try(&sm.bfull[i % kSt], (uint32_t)((i / kSt) & 1)))
+                    if (global_ns() - t0 > kWaitNs) {
+                        atomicOr(a.err, kErrSyncTimeout);
+                        break;
+                    }
+        }
+        __syncwarp();
     } else if (warp >= kLoadWarp0 && warp < kLoadWarp0 + kLoadWarps) {
         // ------------------------------------------------------ weight loads
         // slot q of the raw ring: 128 weight rows x ch stages (ch * 32 bytes
@@ -436,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(LayerArgs a) {
         // 32w .. 32w+31, lane l the 16-byte pieces l, l + 32, ... of them
         // (row = piece / 8, column piece % 8)
         const int lw = warp - kLoadWarp0;
-        const int n_q = n_my * kst / ch;
+        const int n_q = n_stages / ch;
         int l_ti = -1, issued = 0;
         const uint8_t *r0p = nullptr, *r1p = nullptr;  // first rows of the two 64-row halves
         for (int q = 0; q < n_q; ++q) {
@@ -565,21 +532,96 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(LayerArgs a) {
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
 }
 
+// The activation operand of the gate/up GEMM: grouped row r = the int8 codes
+// of its token (even/odd order kept) as f16 integers (exact).
+__global__ void __launch_bounds__(256) act_rows_f16_kernel(const int8_t *__restrict__ xq,
+                                                           const int32_t *__restrict__ rows, int S, int D,
+                                                           __half *__restrict__ xf) {
+    const int r = blockIdx.x;
+    const int tok = rows[r] / S;
+    const int8_t *src = xq + (size_t)tok * D;
+    __half *dst = xf + (size_t)r * D;
+    for (int g = threadIdx.x; g < (D >> 3); g += blockDim.x) {
+        const uint2 v = __ldg(reinterpret_cast<const uint2 *>(src + 8 * g));
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t word = k < 2 ? v.x : v.y, sh = 16 * (k & 1);
+            const int lo = (int)(int8_t)((word >> sh) & 0xFFu), hi = (int)(int8_t)((word >> (sh + 8)) & 0xFFu);
+            o[k] = (uint32_t)__half_as_ushort(__int2half_rn(lo)) | ((uint32_t)__half_as_ushort(__int2half_rn(hi)) << 16);
+        }
+        *reinterpret_cast<uint4 *>(dst + 8 * g) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
 template <int KIND>
-cudaError_t launch_u(const LayerArgs &a, int num_sms, cudaStream_t s) {
+cudaError_t launch_u(const LayerArgs &a, const CUtensorMap &map, int num_sms, cudaStream_t s) {
     auto fn = umma_gemm_kernel<KIND>;
     cudaError_t ce = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (ce != cudaSuccess) return ce;
-    fn<<<num_sms, kThreads, kSmemBytes, s>>>(a);
+    fn<<<num_sms, kThreads, kSmemBytes, s>>>(map, a);
     return cudaGetLastError();
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library).
+cudaError_t encode_fn(EncodeTiledFn *out) {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        cudaError_t ce = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+        if (ce != cudaSuccess) return ce;
+        if (q != cudaDriverEntryPointSuccess || !p) return cudaErrorNotSupported;
+        fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    *out = fn;
+    return cudaSuccess;
+}
+
+// Map of a row-major f16 matrix [rows, cols] (16-byte aligned base, cols a
+// multiple of 64): boxes of kBoxRows rows x 64 columns (128 bytes), 128-byte
+// swizzle; rows past the matrix read as zeros.
+cudaError_t encode_rows_f16(void *base, int rows, int cols, CUtensorMap *map) {
+    EncodeTiledFn fn = nullptr;
+    cudaError_t ce = encode_fn(&fn);
+    if (ce != cudaSuccess) return ce;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kBKs, (cuuint32_t)kBoxRows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 }  // namespace
 
 bool umma_supported(int D, int I) { return D % 128 == 0 && I % 64 == 0 && D <= kMaxDim && I <= kMaxDim; }
 
-cudaError_t launch_umma_gateup(const LayerArgs &a, int num_sms, cudaStream_t s) { return launch_u<kGU>(a, num_sms, s); }
+cudaError_t umma_encode_maps(void *xf, int rows, int D, int I, UmmaMaps *maps) {
+    if ((reinterpret_cast<uintptr_t>(xf) & 15u) || rows < 1) return cudaErrorInvalidValue;
+    cudaError_t ce = encode_rows_f16(xf, rows, D, &maps->gu);
+    if (ce == cudaSuccess) ce = encode_rows_f16(xf, rows, I, &maps->dn);
+    return ce;
+}
 
-cudaError_t launch_umma_down(const LayerArgs &a, int num_sms, cudaStream_t s) { return launch_u<kDN>(a, num_sms, s); }
+cudaError_t launch_act_rows_f16(const LayerArgs &a, cudaStream_t s) {
+    act_rows_f16_kernel<<<a.T * a.S, 256, 0, s>>>(a.xq, a.rows, a.S, a.D, reinterpret_cast<__half *>(a.xf));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_umma_gateup(const LayerArgs &a, const UmmaMaps &maps, int num_sms, cudaStream_t s) {
+    return launch_u<kGU>(a, maps.gu, num_sms, s);
+}
+
+cudaError_t launch_umma_down(const LayerArgs &a, const UmmaMaps &maps, int num_sms, cudaStream_t s) {
+    return launch_u<kDN>(a, maps.dn, num_sms, s);
+}
 
 }  // namespace moe

@@ -2,6 +2,8 @@
 // host launch code.  Internal.
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace moe {
@@ -25,6 +27,8 @@ struct LayerArgs {
     uint32_t *hamax;     // [Tmax * S] bits of max|h| per grouped row
     float *part;         // [Tmax * S, D] expert outputs y by entry id
     int8_t *hq;          // [Tmax * S, I] requantised h (even/odd layout), by grouped row
+    uint16_t *xf;        // [Tmax * S, max(D, I)] f16 activation operand rows of the tcgen05 GEMMs, by grouped row
+                         // (gate/up: the token's codes, D per row; down: the requantised h, I per row), or null
     int32_t *hsum;       // [Tmax * S] code sums of hq rows
     float *shq;          // [Tmax * S] scales of hq rows
     int32_t *dn_cnt;     // [nb_dn] arrival counters of the fused reduce
@@ -78,10 +82,18 @@ cudaError_t launch_grouped_gateup(const LayerArgs &a, int num_sms, cudaStream_t 
 cudaError_t launch_requant_h(const LayerArgs &a, cudaStream_t s);
 cudaError_t launch_grouped_down(const LayerArgs &a, int num_sms, cudaStream_t s);
 bool grouped_supported(int D, int I);
-// Tensor-core (tcgen05, f16-exact) expert GEMMs of large batches.
+// Tensor-core (tcgen05, f16-exact) expert GEMMs of large batches.  Their
+// activation operand is the f16 row buffer xf, read through TMA tensor maps
+// (gate/up: rows of D columns; down: rows of I columns), encoded once per
+// workspace.
+struct UmmaMaps {
+    CUtensorMap gu, dn;
+};
 bool umma_supported(int D, int I);
-cudaError_t launch_umma_gateup(const LayerArgs &a, int num_sms, cudaStream_t s);
-cudaError_t launch_umma_down(const LayerArgs &a, int num_sms, cudaStream_t s);
+cudaError_t umma_encode_maps(void *xf, int rows, int D, int I, UmmaMaps *maps);
+cudaError_t launch_act_rows_f16(const LayerArgs &a, cudaStream_t s);
+cudaError_t launch_umma_gateup(const LayerArgs &a, const UmmaMaps &maps, int num_sms, cudaStream_t s);
+cudaError_t launch_umma_down(const LayerArgs &a, const UmmaMaps &maps, int num_sms, cudaStream_t s);
 // Occupancy-derived grid sizes and kernel attributes (call once per device).
 cudaError_t prepare_expert_kernels(int D, int I, int num_sms, int grid_gu[4], int grid_dn[4]);
 int mch_index(int mch);

@@ -53,6 +53,9 @@ struct Handle {
     uint32_t *hamax;
     float *part;
     int8_t *hq;
+    uint16_t *xf;  // f16 operand rows of the tcgen05 GEMMs
+    moe::UmmaMaps maps;  // their TMA tensor maps
+    bool maps_ok;
     int32_t *hsum;
     float *shq;
     int32_t *dn_cnt;
@@ -100,6 +103,8 @@ size_t layout(const MoeLayerDesc &d, Handle *h) {
     const size_t o_hamax = take(4 * T * S);
     const size_t o_part = take(4 * T * S * D);
     const size_t o_hq = take(T * S * I);
+    // the tcgen05 GEMMs' f16 operand rows: only batches above the decode sizes use them
+    const size_t o_xf = take(T > (size_t)moe::kSmallT ? 2 * T * S * (D > I ? D : I) : 0);
     const size_t o_hsum = take(4 * T * S);
     const size_t o_shq = take(4 * T * S);
     const size_t o_cnt = take(4 * nb_dn);
@@ -122,6 +127,7 @@ size_t layout(const MoeLayerDesc &d, Handle *h) {
         h->hamax = reinterpret_cast<uint32_t *>(b + o_hamax);
         h->part = reinterpret_cast<float *>(b + o_part);
         h->hq = reinterpret_cast<int8_t *>(b + o_hq);
+        h->xf = reinterpret_cast<uint16_t *>(b + o_xf);
         h->hsum = reinterpret_cast<int32_t *>(b + o_hsum);
         h->shq = reinterpret_cast<float *>(b + o_shq);
         h->dn_cnt = reinterpret_cast<int32_t *>(b + o_cnt);
@@ -243,18 +249,22 @@ int run_layer(Handle *h, const float *x, int T, float *out, const float *resid, 
 
     // larger batches with tile-aligned shapes: tensor-core grouped GEMMs
     // (tcgen05 with f16-exact operands; the legacy integer MMA on request)
-    const bool umma = h->tcgen05_gemm && moe::umma_supported(a.D, a.I);
+    const bool umma = h->tcgen05_gemm && h->maps_ok && moe::umma_supported(a.D, a.I);
     if (!small && (umma || moe::grouped_supported(a.D, a.I))) {
+        if (umma) {
+            a.xf = h->xf;
+            if ((ce = moe::launch_act_rows_f16(a, s)) != cudaSuccess) return cuda_fail(ce, "operand rows launch");
+        }
         if (h->probe_which == MOE_PROBE_GATE_UP && (ce = record(h->probe_begin, s)) != cudaSuccess)
             return cuda_fail(ce, "probe record");
-        ce = umma ? moe::launch_umma_gateup(a, h->num_sms, s) : moe::launch_grouped_gateup(a, h->num_sms, s);
+        ce = umma ? moe::launch_umma_gateup(a, h->maps, h->num_sms, s) : moe::launch_grouped_gateup(a, h->num_sms, s);
         if (ce != cudaSuccess) return cuda_fail(ce, "gateup launch");
         if (h->probe_which == MOE_PROBE_GATE_UP && (ce = record(h->probe_end, s)) != cudaSuccess)
             return cuda_fail(ce, "probe record");
         if (h->probe_which == MOE_PROBE_DOWN && (ce = record(h->probe_begin, s)) != cudaSuccess)
             return cuda_fail(ce, "probe record");
         if ((ce = moe::launch_requant_h(a, s)) != cudaSuccess) return cuda_fail(ce, "requant launch");
-        ce = umma ? moe::launch_umma_down(a, h->num_sms, s) : moe::launch_grouped_down(a, h->num_sms, s);
+        ce = umma ? moe::launch_umma_down(a, h->maps, h->num_sms, s) : moe::launch_grouped_down(a, h->num_sms, s);
         if (ce != cudaSuccess) return cuda_fail(ce, "down launch");
         if ((ce = moe::launch_reduce(a, s)) != cudaSuccess) return cuda_fail(ce, "reduce launch");
         if (h->probe_which == MOE_PROBE_DOWN && (ce = record(h->probe_end, s)) != cudaSuccess)
@@ -398,6 +408,8 @@ int moe_layer_create(const MoeLayerDesc *desc, const float *Wr, const float *bia
         return fail(MOE_ERR_NOMEM, "workspace of %zu bytes: %s", h->ws_bytes, cudaGetErrorString(ce));
     }
     layout(*desc, h);
+    h->maps_ok = moe::umma_supported(desc->D, desc->I) &&
+                 moe::umma_encode_maps(h->xf, desc->max_tokens * h->S, desc->D, desc->I, &h->maps) == cudaSuccess;
     if ((ce = cudaMalloc(&h->experts, sizeof(moe::DevExpert) * ne)) != cudaSuccess) {
         cudaGetLastError();
         cudaFree(h->ws);
@@ -720,6 +732,8 @@ extern "C" int moe_layer_forward_static(const MoeLayerDesc *desc, const float *W
     int32_t *err = h.err;
     layout(d, &h);
     h.err = err;  // the fixed error word, not the layout's
+    h.maps_ok = n_tokens > moe::kSmallT && moe::umma_supported(d.D, d.I) &&
+                moe::umma_encode_maps(h.xf, n_tokens * (d.K + d.n_shared), d.D, d.I, &h.maps) == cudaSuccess;
     h.rpi_gu = kRpiGu;
     h.nb_gu = (d.I + kRpiGu - 1) / kRpiGu;
     h.rpi_dn = kRpiDn;

@@ -68,5 +68,6 @@ def test_workspace_size_glm_decode():
     n1 = moe.workspace_bytes(6144, 2048, 256, 8, 1, 1)
     n2048 = moe.workspace_bytes(6144, 2048, 256, 8, 1, 2048)
     assert n1 < 4 << 20
-    # h (fp32) and expert outputs (fp32) per (token, slot) dominate: 9 * (2048 + 6144) * 4 B per token
-    assert abs(n2048 - 2048 * 9 * (2048 + 6144) * 4) < 0.2 * n2048
+    # h (fp32), expert outputs (fp32) and the tcgen05 GEMMs' f16 operand rows
+    # per (token, slot) dominate: 9 * ((2048 + 6144) * 4 + 6144 * 2) B per token
+    assert abs(n2048 - 2048 * 9 * ((2048 + 6144) * 4 + 6144 * 2)) < 0.2 * n2048
