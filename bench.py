@@ -83,6 +83,8 @@ def parse_args():
     p.add_argument("--no-graph", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--fp8-experts", type=int, default=64,
+                   help="glm_fp8_to_int4: stacked gate matrices converted per launch")
     p.add_argument("--no-secondary", action="store_true",
                    help="default workload only: skip the verify-8 and prefill-2048 lines timed after it")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU oracle sample budget")
@@ -660,6 +662,7 @@ def run_fp8_converter(args, local, n_experts=64, steps=20, warmup=5):
     dev = torch.device("cuda", local)
     O, I = n_experts * 2048, 6144
     codes, si = synth.fp8_checkpoint_matrix(O, I, seed=77, device=dev)
+    torch.cuda.empty_cache()  # the generator's fp32 temporaries
     q4 = torch.empty((O, I // 2), dtype=torch.uint8, device=dev)
     sc = torch.empty(O, dtype=torch.float32, device=dev)
     s = torch.cuda.Stream(device=dev)
@@ -685,7 +688,7 @@ def run_fp8_converter(args, local, n_experts=64, steps=20, warmup=5):
     return {"metric": "FP8 E4M3 block-scaled -> int4 converter throughput", "value": achieved, "unit": "GB/s",
             "ms_per_step": ms, "steps": steps, "warmup": warmup,
             "config": {"rows": O, "cols": I, "matrices": f"{n_experts} stacked GLM gate matrices",
-                       "l2": "inputs larger than L2 (805 MB of codes per launch)"},
+                       "l2": "inputs larger than L2 (%.0f MB of codes per launch)" % (O * I / 1e6)},
             "roofline": {"bound": "hbm", "kernel": "fp8_to_int4_kernel<12>", "achieved": achieved, "peak": peak,
                          "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind + " HBM copy bandwidth",
                          "traffic": TRAFFIC.get("glm_fp8_to_int4"), "algorithmic_bytes_per_launch": nbytes,
@@ -726,7 +729,8 @@ def main():
             return
         import torch
         torch.cuda.set_device(local)
-        print(json.dumps(run_fp8_converter(args, local, steps=args.steps, warmup=max(3, args.warmup))), flush=True)
+        print(json.dumps(run_fp8_converter(args, local, n_experts=args.fp8_experts, steps=args.steps,
+                                           warmup=max(3, args.warmup))), flush=True)
         return
     cfg = synth.CONFIGS[WORKLOADS[args.workload][0]]
     stack = WORKLOADS[args.workload][1]

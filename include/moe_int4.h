@@ -248,10 +248,16 @@ int moe_layer_set_probe(void *handle, int which, cudaEvent_t begin, cudaEvent_t 
 #define MOE_OPT_DECODE_SINGLE_KERNEL_AVAILABLE 2
 /* 1 (default): batches of more than 16 tokens run their expert GEMMs on the
  * tcgen05 tensor cores (kind::f16 with the int4 / int8 values carried exactly,
- * fp32 accumulation, which is exact for these sizes); 0: on the legacy integer
- * MMA (mma.sync s8 x u8).  Both give bit-identical int32 dot products.  Needs
- * D % 128 == 0 and I % 64 == 0. */
+ * fp32 accumulation, which is exact for these sizes; the activation tiles
+ * arrive by TMA from f16 operand rows the library writes once per batch); 0:
+ * on the legacy integer MMA (mma.sync s8 x u8).  Both give bit-identical
+ * int32 dot products.  Needs D % 128 == 0 and I % 64 == 0. */
 #define MOE_OPT_TCGEN05_GEMM 3
+/* read-only: 1 when the tcgen05 expert GEMMs can run for this handle (tile-
+ * aligned sizes, max_tokens > 16, and the TMA tensor maps of their activation
+ * operand encoded at create); otherwise batches above 16 tokens run on the
+ * legacy integer MMA whatever MOE_OPT_TCGEN05_GEMM says. */
+#define MOE_OPT_TCGEN05_GEMM_AVAILABLE 5
 /* Test hook of the failure path, 0 (default) or 1: with 1 the persistent
  * decode kernel's grid barrier (after gate/up) waits for one arrival more
  * than there are CTAs, so that bounded wait runs out (one second) and the

@@ -548,6 +548,9 @@ int moe_layer_get_option(void *handle, int option, int *value_out) {
         case MOE_OPT_DECODE_TEST_WAIT_TIMEOUT:
             *value_out = h->test_wait_extra;
             return MOE_OK;
+        case MOE_OPT_TCGEN05_GEMM_AVAILABLE:
+            *value_out = h->maps_ok && moe::umma_supported(h->d.D, h->d.I) ? 1 : 0;
+            return MOE_OK;
         case MOE_OPT_DECODE_SINGLE_KERNEL_AVAILABLE: {
             int any = 0;
             for (int T = 1; T <= moe::kSmallT; ++T) any |= h->dec_grid[T] > 0;

@@ -18,6 +18,7 @@ from _layers import LayerPair
 pytestmark = pytest.mark.gpu
 
 TCGEN05 = 3  # MOE_OPT_TCGEN05_GEMM
+TCGEN05_AVAILABLE = 5  # MOE_OPT_TCGEN05_GEMM_AVAILABLE
 
 CASES = [
     dict(D=256, I=128, E=16, K=2, n_shared=1, T=17),
@@ -43,6 +44,7 @@ def test_tcgen05_and_legacy_mma_bit_identical(moe, case):
     pair = LayerPair(cfg, wdev="cpu")
     try:
         xd = pair.x.cuda()
+        assert pair.gpu.get_option(TCGEN05_AVAILABLE) == 1
         want = dict(gate_acc=True, up_acc=True, hq=True, down_acc=True)
         outs, dbgs = [], []
         for opt in (1, 0):
@@ -83,6 +85,7 @@ def test_saturated_dots_exact(moe):
     x = torch.ones((T, D), dtype=torch.float32)
     layer = moe.MoeLayer(D, I, E, K, 1, 2.5, T, Wr.to(dev), bias.to(dev), experts_gpu)
     try:
+        assert layer.get_option(TCGEN05_AVAILABLE) == 1
         out = torch.empty((T, D), device=dev)
         dbg = layer.moe_layer_debug(x.to(dev), out, idx=True, gate_acc=True, up_acc=True, down_acc=True, hq=True)
         torch.cuda.synchronize()
