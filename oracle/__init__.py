@@ -47,7 +47,7 @@ class _Layer(ctypes.Structure):
                 ("K", ctypes.c_int), ("n_shared", ctypes.c_int),
                 ("routed_scale", ctypes.c_float),
                 ("Wr", ctypes.c_void_p), ("bias", ctypes.c_void_p),
-                ("experts", ctypes.POINTER(_Expert))]
+                ("experts", ctypes.POINTER(_Expert)), ("top_p", ctypes.c_float)]
 
 
 class _Debug(ctypes.Structure):
@@ -71,6 +71,8 @@ def lib():
         L.orc_dot_i4_i8.restype = ctypes.c_int32
         L.orc_router.argtypes = [vp, vp, vp, ci, ci, ci, ci, cf, vp, vp, vp]
         L.orc_router_gap_f64.argtypes = [vp, vp, vp, ci, ci, ci, ci, vp]
+        L.orc_topp_keff.argtypes = [vp, ci, cf]
+        L.orc_topp_keff.restype = ci
         L.orc_union.argtypes = [vp, ci, ci, ci, vp]
         L.orc_union.restype = ci
         L.orc_rmsnorm.argtypes = [vp, vp, vp, ci, cf]
@@ -201,6 +203,14 @@ def router_gap_f64(x, Wr, bias, K):
     return gap
 
 
+def topp_keff(w, top_p):
+    """w [K] or [T, K] routing weights in selection order -> keff (int or [T])."""
+    w = _c(w, np.float32)
+    if w.ndim == 1:
+        return int(lib().orc_topp_keff(_p(w), w.shape[0], float(top_p)))
+    return np.array([lib().orc_topp_keff(_p(np.ascontiguousarray(r)), w.shape[1], float(top_p)) for r in w], np.int32)
+
+
 def union(idx, E):
     idx = _c(idx, np.int32)
     T, K = idx.shape
@@ -238,9 +248,10 @@ def pack_expert(gate, up, down) -> PackedExpert:
 class Layer:
     """Keeps the numpy buffers alive for the ctypes layer description."""
 
-    def __init__(self, D, I, E, K, n_shared, routed_scale, Wr, bias, experts):
+    def __init__(self, D, I, E, K, n_shared, routed_scale, Wr, bias, experts, top_p=0.0):
         """experts: dict or list, index -> PackedExpert (shared expert at index E).
-        Missing entries are passed as NULL and must not be selected."""
+        Missing entries are passed as NULL and must not be selected.  top_p in
+        (0, 1) turns on adaptive expert top-p (dropped selections: id -1)."""
         self.D, self.I, self.E, self.K, self.n_shared = D, I, E, K, n_shared
         self.Wr = _c(Wr, np.float32)
         self.bias = _c(bias, np.float32)
@@ -251,7 +262,8 @@ class Layer:
                 continue
             arr[e] = _Expert(_p(px.gq), _p(px.uq), _p(px.dq), _p(px.gs), _p(px.us), _p(px.ds))
         self._arr = arr
-        self._c = _Layer(D, I, E, K, n_shared, float(routed_scale), _p(self.Wr), _p(self.bias), arr)
+        self.top_p = float(top_p)
+        self._c = _Layer(D, I, E, K, n_shared, float(routed_scale), _p(self.Wr), _p(self.bias), arr, self.top_p)
 
     def forward(self, x, debug: bool = False):
         x = _c(x, np.float32)

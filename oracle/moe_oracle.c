@@ -252,6 +252,27 @@ void orc_router_gap_f64(const float *x, const float *Wr, const float *bias, int 
     }
 }
 
+/* Adaptive expert top-p.  [C] 使用方法 item 4 (--topp: adaptive expert top-p,
+ * fewer expert reads) and [A] §11 (the union runs over the first keff[s]
+ * selections of token s; how keff is chosen is not shown).  Reading: keff is
+ * the length of the shortest prefix of the token's selections, in selection
+ * order, whose routing weights sum to at least top_p times the sum of all K
+ * weights (sums in fp32, left to right; the bound one fp32 product), and at
+ * least 1.  top_p <= 0 or >= 1 keeps all K.  The kept selections keep their
+ * weights (no renormalisation), as [A]'s weighted add uses w unchanged. */
+int orc_topp_keff(const float *w, int K, float top_p) {
+    if (!(top_p > 0.f && top_p < 1.f)) return K;
+    float total = 0.f;
+    for (int k = 0; k < K; k++) total += w[k];
+    const float bound = top_p * total;
+    float run = 0.f;
+    for (int k = 0; k < K; k++) {
+        run += w[k];
+        if (run >= bound) return k + 1;
+    }
+    return K;
+}
+
 /* Union of the routed experts over a batch in first-appearance order over
  * (token, slot).  [A] §11 (each expert's weights are read once per batch),
  * [B] §11.  Returns the number of distinct experts. */
@@ -317,7 +338,8 @@ static void expert_row(const OrcExpert *ex, int D, int I, const int8_t *xq, floa
  * The layer.  [A] §11 and §12, [B] §11:
  *   xq, sx = per-token int8 quantisation of x;
  *   router on the fp32 x (not on xq);
- *   union of the selected experts; for each union expert, in union order,
+ *   adaptive top-p: each token keeps its first keff selections (orc_topp_keff);
+ *   union of the kept experts; for each union expert, in union order,
  *   every (token, slot) routed to it runs the expert and adds w * y into
  *   out[token] (fp32, one rounding for the product, one for the sum);
  *   then the shared expert adds its y with weight 1.
@@ -338,6 +360,14 @@ int orc_layer_forward(const OrcLayer *L, const float *x, int T, float *out, OrcD
 
     orc_quant_act(x, xq, sx, T, D);
     orc_router(x, L->Wr, L->bias, T, D, E, K, L->routed_scale, idx, w, NULL);
+    /* adaptive top-p: selections past keff are dropped (id -1, weight 0) */
+    for (int t = 0; t < T; t++) {
+        const int keff = orc_topp_keff(w + (int64_t)t * K, K, L->top_p);
+        for (int k = keff; k < K; k++) {
+            idx[(int64_t)t * K + k] = -1;
+            w[(int64_t)t * K + k] = 0.f;
+        }
+    }
     const int nu = orc_union(idx, T, K, E, uniq);
     memset(out, 0, sizeof(float) * (size_t)T * D);
 

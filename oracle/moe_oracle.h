@@ -12,10 +12,13 @@
  *       §04 手写的基础数学 (rmsnorm, siluf, layer order),
  *       §06 从 FP8 到 int4 (FP8 block-scale decoding, per-row int4 packer,
  *           nibble layout, worked example),
- *       §11 MoE 路由与专家执行 (sigmoid+bias top-K router, expert union, SwiGLU),
+ *       §11 MoE 路由与专家执行 (sigmoid+bias top-K router, expert union over the
+ *           first keff[s] selections of each token, SwiGLU),
  *       §12 AVX2 整数 kernel (per-row int8 activation quantiser, integer dot).
  *   [B] besthub.dev, "Running 744B MoE on 25GB RAM: Int4, Disk Streaming & MLA
  *       Compression", §06, §11, §12 (summaries of the same steps).
+ *   [C] aimsg.uk, "低配电脑也能跑GLM 5.2", 使用方法 item 4 (--topp, adaptive
+ *       expert top-p) and 性能数据 (--topp 0.7).
  *
  * Precision: the pages fix fp32 arithmetic (float, expf, lrintf); the oracle
  * follows it.  Integer dot products are exact int32.  The router's double
@@ -44,6 +47,7 @@ typedef struct {
     const float *Wr;   /* [E, D] fp32 router weight, out-major */
     const float *bias; /* [E] fp32 correction bias */
     const OrcExpert *experts;
+    float top_p;       /* adaptive expert top-p in (0, 1); 0 or >= 1: plain top-K */
 } OrcLayer;
 
 /* Optional per-(token, slot) intermediates; every pointer may be NULL.
@@ -85,6 +89,7 @@ void  orc_router(const float *x, const float *Wr, const float *bias, int T, int 
                  int K, float routed_scale, int32_t *idx, float *w, float *p_out);
 void  orc_router_gap_f64(const float *x, const float *Wr, const float *bias, int T, int D,
                          int E, int K, double *gap);
+int   orc_topp_keff(const float *w, int K, float top_p);
 int   orc_union(const int32_t *idx, int T, int K, int E, int32_t *uniq);
 void  orc_rmsnorm(const float *x, const float *w, float *out, int D, float eps);
 int   orc_layer_forward(const OrcLayer *L, const float *x, int T, float *out, OrcDebug *dbg);

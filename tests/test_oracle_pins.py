@@ -481,3 +481,78 @@ def test_fp8_to_int4_is_dequant_then_pack():
     np.testing.assert_array_equal(q4, q4b)
     np.testing.assert_array_equal(s, sb)
     assert s[7] == np.float32(1e-8) and (q4[7] == 0x88).all()
+
+
+# ------------------------------------------------------ adaptive expert top-p --
+# aimsg.uk "低配电脑也能跑GLM 5.2" 使用方法 item 4 (--topp) and reader.mx §11
+# (the union over the first keff[s] selections); the rule itself is a reading
+# (the shortest selection-order prefix whose weights reach top_p of the sum).
+
+def test_topp_keff_hand_example():
+    w = np.array([0.5, 0.25, 0.125, 0.125], np.float32)  # dyadic: every sum exact
+    for p, want in ((0.1, 1), (0.5, 1), (0.5000001, 2), (0.7, 2), (0.75, 2), (0.76, 3), (0.875, 3),
+                    (0.9, 4), (0.999, 4)):
+        assert oracle.topp_keff(w, p) == want, (p, want)
+    # weights in selection order need not be sorted: the prefix is by position
+    assert oracle.topp_keff(np.array([0.125, 0.5, 0.25, 0.125], np.float32), 0.6) == 2
+
+
+def test_topp_disabled_keeps_every_selection():
+    w = np.random.default_rng(30).uniform(0.01, 2.5, 8).astype(np.float32)
+    for p in (0.0, -1.0, 1.0, 1.5):
+        assert oracle.topp_keff(w, p) == 8
+    w[5:] = 0.0  # trailing zero weights still count as selections when disabled
+    assert oracle.topp_keff(w, 1.0) == 8
+
+
+def test_topp_keff_brute_force_and_monotone():
+    rng = np.random.default_rng(31)
+    W = rng.uniform(0.0, 2.5, size=(200, 8)).astype(np.float32)
+    ps = np.linspace(0.05, 0.95, 19).astype(np.float32)
+    prev = np.ones(200, np.int32)
+    for p in ps:
+        k = oracle.topp_keff(W, p)
+        # brute force: prefix sums left to right in float32, first reaching p * total
+        for t in range(200):
+            run, tot = np.float32(0), np.float32(0)
+            for v in W[t]:
+                tot = np.float32(tot + v)
+            bound = np.float32(p * tot)
+            want = 8
+            for j, v in enumerate(W[t]):
+                run = np.float32(run + v)
+                if run >= bound:
+                    want = j + 1
+                    break
+            assert k[t] == want
+        assert (k >= prev).all()
+        prev = k
+
+
+def test_topp_layer_drops_the_tail_selections_only():
+    """With top-p the layer output equals the plain top-K output minus the
+    dropped selections' weighted expert outputs (up to fp32 sum order); the
+    dropped slots are marked id -1 / weight 0, the kept ones are untouched,
+    and the union shrinks as top_p falls."""
+    D, I, E, K = 256, 128, 16, 4
+    L, Wr, b, packed = _make_layer(D, I, E, K, 1, seed=32)
+    x = np.random.default_rng(33).standard_normal((12, D)).astype(np.float32)
+    full, dfull = L.forward(x, debug=True)
+    prev_nu = len(dfull["uniq"])
+    for p in (0.9, 0.7, 0.5, 0.2):
+        Lp = oracle.Layer(D, I, E, K, 1, 2.5, Wr, b, packed, top_p=p)
+        out, d = Lp.forward(x, debug=True)
+        keff = oracle.topp_keff(dfull["w"], p)
+        expect = full.astype(np.float64).copy()
+        for t in range(12):
+            np.testing.assert_array_equal(d["idx"][t, :keff[t]], dfull["idx"][t, :keff[t]])
+            np.testing.assert_array_equal(d["w"][t, :keff[t]], dfull["w"][t, :keff[t]])
+            assert (d["idx"][t, keff[t]:] == -1).all() and (d["w"][t, keff[t]:] == 0).all()
+            for k in range(keff[t], K):
+                expect[t] -= float(dfull["w"][t, k]) * dfull["y"][t, k].astype(np.float64)
+        np.testing.assert_allclose(out, expect, rtol=0, atol=1e-5 * np.abs(full).max())
+        kept = set(d["idx"][d["idx"] >= 0].tolist())
+        assert set(d["uniq"].tolist()) == kept
+        assert len(d["uniq"]) <= prev_nu
+        prev_nu = len(d["uniq"])
+    assert prev_nu < len(dfull["uniq"])
