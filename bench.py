@@ -83,6 +83,8 @@ def parse_args():
     p.add_argument("--no-graph", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--top-p", type=float, default=0.0,
+                   help="adaptive expert top-p in (0, 1) (0: plain top-K, the headline)")
     p.add_argument("--fp8-experts", type=int, default=64,
                    help="glm_fp8_to_int4: stacked gate matrices converted per launch")
     p.add_argument("--no-secondary", action="store_true",
@@ -210,7 +212,7 @@ def measured_peak(kind="hbm_gbs"):
 
 # ------------------------------------------------------------ layer set-up
 
-def build_layers(cfg, n_layers, light, dev, rank_seed=0):
+def build_layers(cfg, n_layers, light, dev, rank_seed=0, top_p=0.0):
     """n_layers resident GLM-shaped layers, weights drawn on the GPU from the
     seeded generator and packed by the library's own int4 packer."""
     import torch
@@ -232,7 +234,7 @@ def build_layers(cfg, n_layers, light, dev, rank_seed=0):
             del g, u, d
         table = [phys[e if e < n_phys or e == cfg.E else e % n_phys] for e in range(cfg.E)] + [phys[cfg.E]]
         layers.append(moe.MoeLayer(cfg.D, cfg.I, cfg.E, cfg.K, cfg.n_shared, cfg.routed_scale, max(cfg.T, 1),
-                                   Wr, bias, table))
+                                   Wr, bias, table, top_p))
         keep.append((Wr, bias, phys))
     torch.cuda.synchronize()
     return layers, keep
@@ -252,7 +254,7 @@ def union_sizes(layers, xs):
 # ----------------------------------------------------------------- our arm
 
 def run_ours(args, workload, rank, world, local, n_layers=None, steps=None, warmup=None, with_e2e=True,
-             with_cpu=True):
+             with_cpu=True, top_p=None):
     """One workload on this rank's GPU; returns rank 0's JSON object (None on
     the other ranks).  The process group, if any, is already up."""
     import torch
@@ -268,7 +270,8 @@ def run_ours(args, workload, rank, world, local, n_layers=None, steps=None, warm
     if n_layers is None:
         n_layers = 8 if stack else max(1, args.layers)
     t_setup = time.time()
-    layers, keep = build_layers(cfg, n_layers, args.light, dev, rank_seed=rank)
+    top_p = args.top_p if top_p is None else top_p
+    layers, keep = build_layers(cfg, n_layers, args.light, dev, rank_seed=rank, top_p=top_p)
     T = cfg.T
     for lyr in layers:
         if args.four_kernel:
@@ -488,7 +491,7 @@ def run_ours(args, workload, rank, world, local, n_layers=None, steps=None, warm
         "config": {"workload": workload, "hidden": cfg.D, "moe_intermediate": cfg.I, "experts": cfg.E,
                    "top_k": cfg.K, "shared_experts": cfg.n_shared, "tokens_per_step": T,
                    "layers_per_step": len(layers) if stack else 1, "layer_sets_cycled": n_layers,
-                   "routed_scale": cfg.routed_scale, "zipf_skew": cfg.skew,
+                   "routed_scale": cfg.routed_scale, "zipf_skew": cfg.skew, "top_p": top_p,
                    "experts_streamed_per_layer": u1_mean, "cuda_graph": use_graph,
                    "steps_per_graph": n_layers if run_graph is not None else 1, "light": args.light,
                    "decode_plan": ("single persistent kernel" if single else "four kernels") if T <= 16 else None,
@@ -703,17 +706,20 @@ SECONDARY_KEYS = ("value", "unit", "ms_per_step", "steps", "warmup", "roofline",
 def secondary_lines(args, rank, world, local):
     """The other two single-layer workloads of the metric (verify batch 8 and
     prefill 2048), timed in the same process after the headline with two
-    resident layer weight sets each (9.7 GB, inputs larger than L2)."""
+    resident layer weight sets each (9.7 GB, inputs larger than L2); the
+    headline workload again with adaptive expert top-p 0.7; and the FP8 ->
+    int4 converter step."""
     out = {}
-    for wl in SECONDARY:
-        line = run_ours(args, wl, rank, world, local, n_layers=2, steps=max(args.steps, 10),
-                        warmup=max(3, min(args.warmup, 20)), with_cpu=False)
+    runs = [(wl, 0.0, 2) for wl in SECONDARY] + [(DEFAULT_WORKLOAD, 0.7, 8)]
+    for wl, tp, nl in runs:
+        line = run_ours(args, wl, rank, world, local, n_layers=nl, steps=max(args.steps, 10),
+                        warmup=max(3, min(args.warmup, 20)), with_cpu=False, top_p=tp)
         if line is None:
             continue
         sub = {k: line[k] for k in SECONDARY_KEYS}
         sub["config"] = {k: line["config"][k] for k in ("tokens_per_step", "zipf_skew", "experts_streamed_per_layer",
-                                                        "layer_sets_cycled", "l2", "cuda_graph")}
-        out[wl] = sub
+                                                        "layer_sets_cycled", "l2", "cuda_graph", "top_p")}
+        out[wl if tp == 0.0 else f"{wl}_topp{tp}"] = sub
     if rank == 0:
         out["glm_fp8_to_int4"] = run_fp8_converter(args, local)
     return out

@@ -132,6 +132,15 @@ typedef struct {
     int n_shared;       /* 0 or 1 always-on shared experts, same I as routed */
     float routed_scale; /* routed_scaling_factor (2.5) */
     int max_tokens;     /* largest n_tokens any forward will pass; >= 1 */
+    float top_p;        /* adaptive expert top-p (aimsg.uk article, --topp; reader.mx
+                         * article §11 runs the union over each token's first keff
+                         * selections).  In (0, 1): each token keeps the shortest
+                         * prefix of its K selections, in selection order, whose
+                         * weights reach top_p times the sum of all K (fp32 sums in
+                         * order, at least one), with unchanged weights; the others
+                         * are dropped (no expert read, no term in the sum; in
+                         * moe_layer_debug their idx is -1 and w 0).  0 (or any value
+                         * outside (0, 1)): plain top-K.  NaN: INVALID_ARG. */
 } MoeLayerDesc;
 
 /* One expert's packed weights (device pointers, as moe_pack_int4 writes them):

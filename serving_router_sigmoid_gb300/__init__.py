@@ -34,7 +34,8 @@ if not os.path.exists(LIB_PATH):
 
 class MoeLayerDesc(ctypes.Structure):
     _fields_ = [("D", ctypes.c_int), ("I", ctypes.c_int), ("E", ctypes.c_int), ("K", ctypes.c_int),
-                ("n_shared", ctypes.c_int), ("routed_scale", ctypes.c_float), ("max_tokens", ctypes.c_int)]
+                ("n_shared", ctypes.c_int), ("routed_scale", ctypes.c_float), ("max_tokens", ctypes.c_int),
+                ("top_p", ctypes.c_float)]
 
 
 class MoeExpertW(ctypes.Structure):
@@ -166,12 +167,13 @@ class MoeLayer:
     of CUDA tensors as moe_pack_int4 writes them; entry E is the shared expert.
     """
 
-    def __init__(self, D, I, E, K, n_shared, routed_scale, max_tokens, Wr, bias, experts):
+    def __init__(self, D, I, E, K, n_shared, routed_scale, max_tokens, Wr, bias, experts, top_p=0.0):
         self.D, self.I, self.E, self.K, self.n_shared = D, I, E, K, n_shared
         self.S = K + n_shared
         self.max_tokens = max_tokens
+        self.top_p = float(top_p)
         self._keep = (Wr, bias, list(experts))
-        desc = MoeLayerDesc(D, I, E, K, n_shared, float(routed_scale), max_tokens)
+        desc = MoeLayerDesc(D, I, E, K, n_shared, float(routed_scale), max_tokens, self.top_p)
         arr = (MoeExpertW * (E + n_shared))()
         for e, (gq, gs, uq, us, dq, ds) in enumerate(experts):
             arr[e] = MoeExpertW(_ptr(gq), _ptr(uq), _ptr(dq), _ptr(gs), _ptr(us), _ptr(ds))
@@ -260,7 +262,7 @@ class MoeLayer:
 
 
 def workspace_bytes(D, I, E, K, n_shared, max_tokens, routed_scale=2.5) -> int:
-    desc = MoeLayerDesc(D, I, E, K, n_shared, float(routed_scale), max_tokens)
+    desc = MoeLayerDesc(D, I, E, K, n_shared, float(routed_scale), max_tokens, 0.0)
     n = ctypes.c_size_t(0)
     _check(_lib.moe_layer_workspace_bytes(ctypes.byref(desc), ctypes.byref(n)))
     return int(n.value)
@@ -283,9 +285,10 @@ def expert_table_device(experts, device):
     return torch.frombuffer(bytearray(bytes(arr)), dtype=torch.uint8).to(device)
 
 
-def moe_layer_forward_static(D, I, E, K, n_shared, routed_scale, Wr, bias, experts_dev, x, out, stream=None):
+def moe_layer_forward_static(D, I, E, K, n_shared, routed_scale, Wr, bias, experts_dev, x, out, stream=None,
+                             top_p=0.0):
     """The allocation-free forward: experts_dev from expert_table_device."""
-    desc = MoeLayerDesc(D, I, E, K, n_shared, float(routed_scale), max(1, x.shape[0]))
+    desc = MoeLayerDesc(D, I, E, K, n_shared, float(routed_scale), max(1, x.shape[0]), float(top_p))
     _check(_lib.moe_layer_forward_static(ctypes.byref(desc), _ptr(Wr), _ptr(bias), _ptr(experts_dev), _ptr(x),
                                          x.shape[0], _ptr(out), _stream(stream)))
 

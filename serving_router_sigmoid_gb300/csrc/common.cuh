@@ -21,6 +21,10 @@ constexpr int kErrRouteCount = 2;    // routing table inconsistent
 constexpr int kErrTooManyRows = 8;   // an expert had more rows than the streaming tile
 constexpr int kErrSyncTimeout = 16;  // a wait of the persistent decode kernel ran out of time
 
+// Expert id of a selection that adaptive top-p dropped (no expert: its slot
+// is skipped by the union and the weighted sum).
+constexpr int kDroppedSel = -1;
+
 struct DevExpert {
     const uint8_t *gq, *uq, *dq;
     const float *gs, *us, *ds;

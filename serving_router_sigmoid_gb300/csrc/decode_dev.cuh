@@ -381,25 +381,31 @@ __device__ __forceinline__ void cost_slice(const int *ubeg, int n, int gpe, int 
 // expert-grouped order (rows of one expert keep (token, slot) order).  The
 // first selection of each expert also ranks its expert among the distinct
 // ones: the union is in ascending expert id, the shared expert last.
-__device__ __forceinline__ void build_union(DecodeSmem &sm, int T, int K, int S, int E, int n_shared) {
+// Selections that adaptive top-p dropped (kDroppedSel) take no row; the
+// shared expert's rows follow the kept ones.  Returns the kept count.
+__device__ __forceinline__ int build_union(DecodeSmem &sm, int T, int K, int S, int E, int n_shared) {
     const int n = T * K, tid = threadIdx.x;
     int e = -1, less = 0;
-    bool first = true;
+    bool first = false;
     if (tid == 0) sm.nu = 0;
     if (tid < n) {
         e = sm.idx[tid];
-        for (int j = 0; j < n; ++j) {
-            const int ej = sm.idx[j];
-            less += ej < e;
-            if (ej == e && j < tid) {
-                ++less;
-                first = false;
+        if (e != kDroppedSel) {
+            first = true;
+            for (int j = 0; j < n; ++j) {
+                const int ej = sm.idx[j];
+                if (ej == kDroppedSel) continue;
+                less += ej < e;
+                if (ej == e && j < tid) {
+                    ++less;
+                    first = false;
+                }
             }
+            sm.rows[less] = (tid / K) * S + (tid % K);
         }
-        sm.rows[less] = (tid / K) * S + (tid % K);
         sm.first[tid] = first;
     }
-    __syncthreads();
+    const int n_kept = __syncthreads_count(tid < n && e != kDroppedSel);
     if (tid < n && first) {
         int upos = 0;
         for (int j = 0; j < n; ++j) upos += sm.first[j] && sm.idx[j] < e;
@@ -407,16 +413,18 @@ __device__ __forceinline__ void build_union(DecodeSmem &sm, int T, int K, int S,
         sm.ubeg[upos] = less;
         atomicAdd(&sm.nu, 1);
     }
+    if (n_shared && tid < T) sm.rows[n_kept + tid] = tid * S + K;
     __syncthreads();
     if (tid == 0) {
         const int nr = sm.nu;
-        sm.ubeg[nr] = n;
+        sm.ubeg[nr] = n_kept;
         if (n_shared) {
             sm.uexp[nr] = E;
-            sm.ubeg[nr + 1] = n + T;
+            sm.ubeg[nr + 1] = n_kept + T;
         }
     }
     __syncthreads();
+    return n_kept;
 }
 
 template <int CPLG, int CPLD, int MCH>
@@ -473,7 +481,9 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
     // routing's latency; more tokens: it is compute bound in the wide dot
     // loops and would hold up the union, so it joins the routed entries'
     // cost-weighted slices instead)
-    const bool sh_early = MCH == 1 && a.n_shared;
+    // (with adaptive top-p the shared rows follow the kept selections, whose
+    // count the routing decides: the shared expert then joins the slices)
+    const bool sh_early = MCH == 1 && a.n_shared && !(a.top_p > 0.f && a.top_p < 1.f);
     const int sp0 = sh_early ? (int)((long long)b * I / G) : 0;
     const int sp1 = sh_early ? (int)((long long)(b + 1) * I / G) : 0;
     // (a router CTA requests them once its logits are out, so that the router
@@ -514,7 +524,7 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
     // publishes them as data, while the other CTAs stream the shared expert
     if (tq < T)
         topk_small_cta<true>(dlog + (size_t)tq * E, a.bias, 1, E, K, a.routed_scale, nullptr, nullptr,
-                             dsel + (size_t)tq * K, a.err, sm.tk, sm.tkp);
+                             dsel + (size_t)tq * K, a.err, sm.tk, sm.tkp, a.top_p);
 
     // shared expert gate/up, once the quantised tokens are in
     if (MCH > 1) cta_wait(&sy->quant_cnt, T, a.err);
@@ -533,7 +543,7 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
                 const unsigned long long v = ld_relaxed_u64(dsel + i);
                 const int e = (int)(v >> 32);
                 miss |= v == kSelEmpty;
-                sm.idx[i] = (e >= 0 && e < E) ? e : 0;
+                sm.idx[i] = v == kSelEmpty ? 0 : e == kDroppedSel ? kDroppedSel : (e >= 0 && e < E) ? e : 0;
                 sm.w[i] = v == kSelEmpty ? 0.f : __uint_as_float((uint32_t)v);
             }
             if (!__syncthreads_or(miss)) break;
@@ -546,7 +556,7 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
         }
     }
     stamp(a, 4);
-    build_union(sm, T, K, S, E, a.n_shared);
+    const int n_kept = build_union(sm, T, K, S, E, a.n_shared);
     stamp(a, 5);
     const int n_r = sm.nu, n_u = n_r + a.n_shared;
     if (b == 0) {  // the tables for the debug entry point and other readers
@@ -554,7 +564,7 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
             a.idx[i] = sm.idx[i];
             a.wts[i] = sm.w[i];
         }
-        for (int i = tid; i < n_sel + a.n_shared * T; i += blockDim.x) a.rows[i] = sm.rows[i];
+        for (int i = tid; i < n_kept + a.n_shared * T; i += blockDim.x) a.rows[i] = sm.rows[i];
         for (int i = tid; i < n_u; i += blockDim.x) a.meta->uexp[i] = sm.uexp[i];
         for (int i = tid; i <= n_u; i += blockDim.x) a.meta->ubeg[i] = sm.ubeg[i];
         if (tid == 0) {
@@ -666,7 +676,7 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int k = 0; k < kMaxK; ++k) {
-                if (k < K) {
+                if (k < K && sm.idx[t * K + k] != kDroppedSel) {  // a dropped slot has no expert output
                     const float wk = sm.w[t * K + k];
                     acc.x = __fadd_rn(acc.x, __fmul_rn(wk, y[k].x));
                     acc.y = __fadd_rn(acc.y, __fmul_rn(wk, y[k].y));

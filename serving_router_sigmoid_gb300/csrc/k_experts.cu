@@ -274,8 +274,9 @@ __global__ void __launch_bounds__(256) down_kernel(LayerArgs a) {
                     const int t = i / nrow, o = o0 + (i - t * nrow);
                     const float *pt = a.part + (size_t)t * S * D + o;
                     float acc = 0.f;
-                    for (int k = 0; k < K; ++k)
-                        acc = __fadd_rn(acc, __fmul_rn(__ldcg(a.wts + t * K + k), __ldcg(pt + (size_t)k * D)));
+                    for (int k = 0; k < K; ++k)  // a slot top-p dropped has no expert output
+                        if (__ldcg(a.idx + t * K + k) != kDroppedSel)
+                            acc = __fadd_rn(acc, __fmul_rn(__ldcg(a.wts + t * K + k), __ldcg(pt + (size_t)k * D)));
                     if (a.n_shared) acc = __fadd_rn(acc, __ldcg(pt + (size_t)K * D));
                     if (a.resid) acc = __fadd_rn(__ldcg(a.resid + (size_t)t * D + o), acc);
                     a.out[(size_t)t * D + o] = acc;
@@ -288,7 +289,8 @@ __global__ void __launch_bounds__(256) down_kernel(LayerArgs a) {
 
 // ---------------------------------------------------------------- reduce
 
-// out[t] = (resid[t] +) sum_k w[t,k] * y[t,k] + y[t,shared], slots in order.
+// out[t] = (resid[t] +) sum_k w[t,k] * y[t,k] + y[t,shared], slots in order
+// (slots adaptive top-p dropped are skipped).
 // Every slot's value is loaded before the first add (K <= kMaxK).
 __global__ void __launch_bounds__(256) reduce_kernel(LayerArgs a) {
     const int t = blockIdx.y;
@@ -298,17 +300,21 @@ __global__ void __launch_bounds__(256) reduce_kernel(LayerArgs a) {
     const float *pt = a.part + (size_t)t * S * D + o;
     float4 y[kMaxK + 1];
     float wk[kMaxK];
+    bool kept[kMaxK];  // a slot top-p dropped has no expert output
 #pragma unroll
     for (int k = 0; k <= kMaxK; ++k) {
         if (k < S) y[k] = *reinterpret_cast<const float4 *>(pt + (size_t)k * D);
-        if (k < K && k < kMaxK) wk[k] = a.wts[t * K + k];
+        if (k < K && k < kMaxK) {
+            wk[k] = a.wts[t * K + k];
+            kept[k] = a.idx[t * K + k] != kDroppedSel;
+        }
     }
     float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
     if (a.resid) r = *reinterpret_cast<const float4 *>(a.resid + (size_t)t * D + o);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < kMaxK; ++k) {
-        if (k < K) {
+        if (k < K && kept[k]) {
             acc.x = __fadd_rn(acc.x, __fmul_rn(wk[k], y[k].x));
             acc.y = __fadd_rn(acc.y, __fmul_rn(wk[k], y[k].y));
             acc.z = __fadd_rn(acc.z, __fmul_rn(wk[k], y[k].z));

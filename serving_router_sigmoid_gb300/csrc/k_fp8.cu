@@ -11,19 +11,23 @@
 // MoE on 25GB RAM" §06.
 //
 // Design (GB300).  The step is HBM-bound: 1 byte read and half a byte written
-// per weight.  One warp owns one row at a time; a row of up to 8192 codes is
-// read once into registers with 16-byte loads (all of a lane's loads issued
-// before any use), so the amax pass and the packing pass read no memory
-// twice and no fp32 copy of the matrix exists.  A 16-byte chunk lies inside
-// one 128-column block, so each chunk needs one scale.  E4M3 is sign-magnitude
-// with a monotone encoding, so the largest |value| of a chunk is the one of its
-// largest 7-bit magnitude code, and (rounding being monotone) the chunk's
-// largest |w| is that value times the block scale: the amax pass costs a few
-// byte-max instructions per chunk.  The widening uses the hardware e4m3x2 ->
-// f16x2 conversion (exact: every E4M3 value is an f16 value), then f16 -> f32
-// (exact).  The division of the packer is replaced, where that provably gives
-// the same code, by a product with the row's reciprocal (nibble_fast).  Rows that are not a multiple of 16 codes, longer than 8192 or
-// unaligned take a plain per-element path with the same arithmetic.
+// per weight.  One warp owns one row at a time.  The amax pass issues all of a
+// lane's 16-byte loads of the row at once (rows of up to 8192 codes) and keeps
+// nothing but the running maximum; the packing pass walks the row's chunks
+// again, one at a time, from L1, so the code and the register footprint stay
+// small (an unrolled packing pass overflowed the instruction cache and halved
+// the occupancy) and no fp32 copy of the matrix exists.  A 16-byte chunk lies
+// inside one 128-column block, so each chunk needs one scale.  E4M3 is
+// sign-magnitude with a monotone encoding, so the largest |value| of a chunk
+// is the one of its largest 7-bit magnitude code, and (rounding being
+// monotone) the chunk's largest |w| is that value times the block scale: the
+// amax pass costs a few byte-max instructions per chunk.  The widening uses
+// the hardware e4m3x2 -> f16x2 conversion (exact: every E4M3 value is an f16
+// value), then f16 -> f32 (exact).  The packer's division is replaced, where
+// that provably gives the same code, by a product with the row's reciprocal
+// (nibble_fast); a chunk with a quotient near a tie is redone exactly.  Rows
+// that are not a multiple of 16 codes, longer than 8192 or unaligned take a
+// plain per-element path with the packer's arithmetic.
 #include "layer_args.cuh"
 
 namespace moe {
@@ -51,38 +55,58 @@ __device__ __forceinline__ uint32_t nibble_of(float w, float s) {
     return (uint32_t)(min(7, max(-8, v)) + 8);
 }
 
-// The same code without the division where that is provably safe.  With
-// inv = fl(1/s) and g = fl(sc * inv), y = fl(v * g) differs from the packer's
-// quotient fl(fl(v * sc) / s) by at most five roundings of relative size
-// 2^-24 of a quotient whose magnitude is at most 7 (|w| <= amax, s >= amax/7
-// rounded): less than 2^-18.  So when y lies farther than 2^-17 from every
-// half-integer, both round to the same integer; otherwise (ties and near
-// ties) the quotient is formed exactly as the packer forms it.  Rounding y to
-// an integer: adding M = 1.5 * 2^23 + 8 rounds at integer granularity with
-// ties to even (M is even) and leaves 8 + nearest(y) in the low four bits of
-// the sum (|nearest(y)| <= 7, so no borrow or carry leaves the nibble).
-__device__ __forceinline__ uint32_t nibble_fast(float v, float g, float sc, float s) {
+// The same code without the division, where that provably gives the same
+// result.  With inv = fl(1/s) and g = fl(sc * inv), y = fl(v * g) differs
+// from the packer's quotient fl(fl(v * sc) / s) by at most five roundings of
+// relative size 2^-24 of a quotient whose magnitude is at most 7 (|w| <= amax,
+// s >= amax/7 rounded): less than 2^-18.  So when y lies farther than 2^-17
+// from every half-integer, both round to the same integer.  Rounding y to an
+// integer: adding M = 1.5 * 2^23 + 8 rounds at integer granularity with ties
+// to even (M is even) and leaves 8 + nearest(y) in the low four bits of the
+// sum (|nearest(y)| <= 7, so no borrow or carry leaves the nibble).  `near`
+// is set when y lies within 2^-17 of a half-integer: the caller then forms
+// the quotient exactly as the packer does.
+__device__ __forceinline__ uint32_t nibble_fast(float v, float g, bool &near) {
     constexpr float kM = 12582920.f;  // 1.5 * 2^23 + 8
     const float y = __fmul_rn(v, g);
     const float z = __fadd_rn(y, kM);
     const float r = __fsub_rn(y, __fsub_rn(z, kM));  // y - nearest(y), exact
-    if (fabsf(r) < 0.5f - 7.62939453125e-06f) return __float_as_uint(z) & 15u;  // 2^-17 from any half
-    return nibble_of(__fmul_rn(v, sc), s);
+    near |= fabsf(r) >= 0.5f - 7.62939453125e-06f;
+    return __float_as_uint(z) & 15u;
 }
 
-// One word of four codes at block scale sc (g = fl(sc * fl(1/s))) -> the two
-// packed bytes of its four elements (low 16 bits of the result).
-__device__ __forceinline__ uint32_t pack_word(uint32_t w, float sc, float g, float s) {
-    const float2 a = e4m3x2_to_f32x2(w & 0xFFFFu), b = e4m3x2_to_f32x2(w >> 16);
-    const uint32_t n0 = nibble_fast(a.x, g, sc, s), n1 = nibble_fast(a.y, g, sc, s);
-    const uint32_t n2 = nibble_fast(b.x, g, sc, s), n3 = nibble_fast(b.y, g, sc, s);
-    return n0 | (n1 << 4) | (n2 << 8) | (n3 << 12);
+// Packed bytes of one 16-code chunk (4 words, element 2j low nibble).
+__device__ __forceinline__ uint2 pack_chunk_fast(uint4 c, float g, bool &near) {
+    uint32_t out[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t w0 = h ? c.z : c.x, w1 = h ? c.w : c.y;
+        const float2 a = e4m3x2_to_f32x2(w0 & 0xFFFFu), b = e4m3x2_to_f32x2(w0 >> 16);
+        const float2 d = e4m3x2_to_f32x2(w1 & 0xFFFFu), e = e4m3x2_to_f32x2(w1 >> 16);
+        out[h] = nibble_fast(a.x, g, near) | (nibble_fast(a.y, g, near) << 4) | (nibble_fast(b.x, g, near) << 8) |
+                 (nibble_fast(b.y, g, near) << 12) | (nibble_fast(d.x, g, near) << 16) |
+                 (nibble_fast(d.y, g, near) << 20) | (nibble_fast(e.x, g, near) << 24) |
+                 (nibble_fast(e.y, g, near) << 28);
+    }
+    return make_uint2(out[0], out[1]);
+}
+
+// The packer's arithmetic for a whole chunk (rare: a quotient near a tie).
+__device__ __noinline__ uint2 pack_chunk_exact(uint4 c, float sc, float s) {
+    uint32_t out[2] = {0u, 0u};
+    const uint32_t wd[4] = {c.x, c.y, c.z, c.w};
+    for (int q = 0; q < 8; ++q) {
+        const float2 v = e4m3x2_to_f32x2((wd[q >> 1] >> (16 * (q & 1))) & 0xFFFFu);
+        const uint32_t pair = nibble_of(__fmul_rn(v.x, sc), s) | (nibble_of(__fmul_rn(v.y, sc), s) << 4);
+        out[q >> 2] |= pair << (8 * (q & 3));
+    }
+    return make_uint2(out[0], out[1]);
 }
 
 // Largest magnitude code (0..127) among the 16 codes of a chunk.
-__device__ __forceinline__ uint32_t max_mag_code(int4 c) {
+__device__ __forceinline__ uint32_t max_mag_code(uint4 c) {
     const uint32_t m = 0x7F7F7F7Fu;
-    uint32_t v = __vmaxu4(__vmaxu4((uint32_t)c.x & m, (uint32_t)c.y & m), __vmaxu4((uint32_t)c.z & m, (uint32_t)c.w & m));
+    uint32_t v = __vmaxu4(__vmaxu4(c.x & m, c.y & m), __vmaxu4(c.z & m, c.w & m));
     v = __vmaxu4(v, v >> 16);
     v = __vmaxu4(v, v >> 8);
     return v & 0xFFu;
@@ -93,7 +117,10 @@ __device__ __forceinline__ float row_scale(float amax) {
     return s < 1e-8f ? 1e-8f : s;
 }
 
-// Rows of I = 16 * nch codes (nch <= 32 * CPL), 16-byte aligned rows.
+// Rows of I = 16 * nch codes (nch <= 32 * CPL), 16-byte aligned rows.  The
+// amax pass issues all of a lane's 16-byte loads of the row at once (they
+// stay in L1); the packing pass reloads one chunk at a time, which keeps the
+// loop small and the registers few.
 template <int CPL>
 __global__ void __launch_bounds__(32 * kWarpsPerCta) fp8_to_int4_kernel(const uint8_t *__restrict__ w8,
                                                                          const float *__restrict__ si,
@@ -104,40 +131,35 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) fp8_to_int4_kernel(const ui
     const int nch = I >> 4, nbi = (I + 127) >> 7;
     const long long stride = (long long)gridDim.x * kWarpsPerCta;
     for (long long o = (long long)blockIdx.x * kWarpsPerCta + warp; o < O; o += stride) {
-        const uint8_t *row = w8 + o * I;
+        const uint4 *row = reinterpret_cast<const uint4 *>(w8 + o * I);
         const float *srow = si + (o >> 7) * nbi;
-        int4 raw[CPL];
+        uint4 raw[CPL];
 #pragma unroll
         for (int j = 0; j < CPL; ++j) {
             const int c = lane + 32 * j;
-            raw[j] = c < nch ? ld_stream16(row + 16 * c) : make_int4(0, 0, 0, 0);
-        }
-        float sc[CPL];
-#pragma unroll
-        for (int j = 0; j < CPL; ++j) {
-            const int c = lane + 32 * j;
-            sc[j] = c < nch ? __ldg(srow + (c >> 3)) : 0.f;
+            raw[j] = c < nch ? __ldg(row + c) : make_uint4(0u, 0u, 0u, 0u);
         }
         float amax = 0.f;
 #pragma unroll
         for (int j = 0; j < CPL; ++j) {
+            const int c = lane + 32 * j;
+            const float sc = c < nch ? __ldg(srow + (c >> 3)) : 0.f;
             const float v = e4m3x2_to_f32x2(max_mag_code(raw[j])).x;
-            amax = fmaxf(amax, fabsf(__fmul_rn(v, sc[j])));
+            amax = fmaxf(amax, fabsf(__fmul_rn(v, sc)));
         }
         amax = warp_max_f(amax);
         const float s = row_scale(amax);
         if (lane == 0) scale[o] = s;
-        uint8_t *qrow = q4 + o * (I >> 1);
         const float inv = __fdiv_rn(1.f, s);
-#pragma unroll
-        for (int j = 0; j < CPL; ++j) {
-            const int c = lane + 32 * j;
-            if (c < nch) {
-                const float g = __fmul_rn(sc[j], inv), scj = sc[j];
-                const uint32_t p0 = pack_word((uint32_t)raw[j].x, scj, g, s), p1 = pack_word((uint32_t)raw[j].y, scj, g, s);
-                const uint32_t p2 = pack_word((uint32_t)raw[j].z, scj, g, s), p3 = pack_word((uint32_t)raw[j].w, scj, g, s);
-                *reinterpret_cast<uint2 *>(qrow + 8 * c) = make_uint2(p0 | (p1 << 16), p2 | (p3 << 16));
-            }
+        uint2 *qrow = reinterpret_cast<uint2 *>(q4 + o * (I >> 1));
+#pragma unroll 1
+        for (int c = lane; c < nch; c += 32) {
+            const uint4 cv = __ldg(row + c);
+            const float sc = __ldg(srow + (c >> 3));
+            bool near = false;
+            uint2 pk = pack_chunk_fast(cv, __fmul_rn(sc, inv), near);
+            if (near) pk = pack_chunk_exact(cv, sc, s);
+            qrow[c] = pk;
         }
     }
 }

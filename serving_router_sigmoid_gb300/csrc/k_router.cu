@@ -75,30 +75,36 @@ __global__ void __launch_bounds__(256) quant_natural_kernel(const float *__restr
 // rows of one expert keep (token, slot) order).  The first selection of each
 // expert also ranks its expert among the distinct ones, which gives the
 // union position (ascending expert id) and the expert's first row.
+// Selections that adaptive top-p dropped (kDroppedSel) take no row; the
+// shared expert's rows follow the kept ones.
 __device__ void build_routing_small(const LayerArgs &a, const int *s_idx, int T) {
     __shared__ int s_first[kSmallT * kMaxK];
     __shared__ int s_nu;
-    const int K = a.K, S = a.S, n = T * K, tid = threadIdx.x;
+    const int K = a.K, S = a.S, tid = threadIdx.x;
     int e = -1, less = 0;
-    bool first = true;
-    if (tid < n) {
+    bool first = false;
+    if (tid < T * K) {
         e = s_idx[tid];
-        for (int j = 0; j < n; ++j) {
-            const int ej = s_idx[j];
-            less += ej < e;
-            if (ej == e && j < tid) {
-                ++less;
-                first = false;
+        if (e != kDroppedSel) {
+            first = true;
+            for (int j = 0; j < T * K; ++j) {
+                const int ej = s_idx[j];
+                if (ej == kDroppedSel) continue;
+                less += ej < e;
+                if (ej == e && j < tid) {
+                    ++less;
+                    first = false;
+                }
             }
+            a.rows[less] = (tid / K) * S + (tid % K);
         }
-        a.rows[less] = (tid / K) * S + (tid % K);
         s_first[tid] = first;
     }
     if (tid == 0) s_nu = 0;
-    __syncthreads();
-    if (tid < n && first) {
+    const int n = __syncthreads_count(tid < T * K && e != kDroppedSel);  // kept selections
+    if (tid < T * K && first) {
         int upos = 0;
-        for (int j = 0; j < n; ++j) upos += s_first[j] && s_idx[j] < e;
+        for (int j = 0; j < T * K; ++j) upos += s_first[j] && s_idx[j] < e;
         a.meta->uexp[upos] = e;
         a.meta->ubeg[upos] = less;
         atomicAdd(&s_nu, 1);
@@ -158,7 +164,8 @@ __global__ void __launch_bounds__(256) router_small_kernel(LayerArgs a) {
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    topk_small_cta<false>(a.logits, a.bias, T, E, a.K, a.routed_scale, s_idx, a.wts, nullptr, a.err, tk, tkp);
+    topk_small_cta<false>(a.logits, a.bias, T, E, a.K, a.routed_scale, s_idx, a.wts, nullptr, a.err, tk, tkp,
+                          a.top_p);
     for (int i = tid; i < T * a.K; i += blockDim.x) a.idx[i] = s_idx[i];
     build_routing_small(a, s_idx, T);
     if (tid == 0) a.meta->counter = 0;
@@ -322,7 +329,7 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const float *__restr
 template <int EPL>
 __global__ void __launch_bounds__(256) router_select_kernel(const float *__restrict__ logits, int nz,
                                                             const float *__restrict__ bias, int T, int E, int K,
-                                                            float scale, int32_t *__restrict__ idx,
+                                                            float scale, float top_p, int32_t *__restrict__ idx,
                                                             float *__restrict__ w, int32_t *err) {
     const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (t >= T) return;
@@ -339,7 +346,7 @@ __global__ void __launch_bounds__(256) router_select_kernel(const float *__restr
             c[j] = -INFINITY;
         }
     }
-    select_topk<EPL>(c, p, E, K, scale, idx + (size_t)t * K, w + (size_t)t * K, nullptr, err);
+    select_topk<EPL>(c, p, E, K, scale, idx + (size_t)t * K, w + (size_t)t * K, nullptr, err, top_p);
 }
 
 // ------------------------------------------------- large-batch permute
@@ -362,9 +369,11 @@ __global__ void __launch_bounds__(1024) permute_large_kernel(LayerArgs a) {
         const int i = g + lane;
         const bool v = i < end;
         int e = v ? a.idx[i] : -1;
-        if (v && (e < 0 || e >= E)) { e = 0; atomicOr(a.err, kErrRouteCount); }
+        const bool kept = v && e != kDroppedSel;  // a selection top-p dropped takes no row
+        if (kept && (e < 0 || e >= E)) { e = 0; atomicOr(a.err, kErrRouteCount); }
+        if (!kept) e = -1;
         const unsigned m = __match_any_sync(0xffffffffu, e);
-        if (v && __popc(m & lt) == 0) hist[warp * E + e] += __popc(m);
+        if (kept && __popc(m & lt) == 0) hist[warp * E + e] += __popc(m);
         __syncwarp();
     }
     __syncthreads();
@@ -379,7 +388,7 @@ __global__ void __launch_bounds__(1024) permute_large_kernel(LayerArgs a) {
         flg[e] = run > 0;
     }
     __syncthreads();
-    block_excl_scan(tot, base, E, wtot);
+    const int n_kept = block_excl_scan(tot, base, E, wtot);
     const int n_routed = block_excl_scan(flg, upos, E, wtot);
     for (int e = tid; e < E; e += blockDim.x)
         if (tot[e] > 0) {
@@ -388,10 +397,10 @@ __global__ void __launch_bounds__(1024) permute_large_kernel(LayerArgs a) {
         }
     if (tid == 0) {
         int nu = n_routed;
-        a.meta->ubeg[n_routed] = n;
+        a.meta->ubeg[n_routed] = n_kept;
         if (a.n_shared) {
             a.meta->uexp[n_routed] = E;
-            a.meta->ubeg[n_routed + 1] = n + T;
+            a.meta->ubeg[n_routed + 1] = n_kept + T;
             nu += 1;
         }
         a.meta->n_union = nu;
@@ -404,16 +413,18 @@ __global__ void __launch_bounds__(1024) permute_large_kernel(LayerArgs a) {
         const int i = g + lane;
         const bool v = i < end;
         int e = v ? a.idx[i] : -1;
-        if (v && (e < 0 || e >= E)) e = 0;
+        const bool kept = v && e != kDroppedSel;
+        if (kept && (e < 0 || e >= E)) e = 0;
+        if (!kept) e = -1;
         const unsigned m = __match_any_sync(0xffffffffu, e);
         const int rank = __popc(m & lt);
-        if (v) a.rows[hist[warp * E + e] + rank] = (i / K) * S + (i % K);
+        if (kept) a.rows[hist[warp * E + e] + rank] = (i / K) * S + (i % K);
         __syncwarp();
-        if (v && rank == 0) hist[warp * E + e] += __popc(m);
+        if (kept && rank == 0) hist[warp * E + e] += __popc(m);
         __syncwarp();
     }
     if (a.n_shared)
-        for (int t = tid; t < T; t += blockDim.x) a.rows[n + t] = t * S + K;
+        for (int t = tid; t < T; t += blockDim.x) a.rows[n_kept + t] = t * S + K;
 }
 
 // ---------------------------------------------------------- launchers
@@ -459,24 +470,25 @@ cudaError_t launch_router_tile(const float *x, const float *Wr, const float *bia
 
 template <int EPL>
 static cudaError_t launch_select_t(const float *logits, int nz, const float *bias, int T, int E, int K, float scale,
-                                   int32_t *idx, float *w, int32_t *err, cudaStream_t s) {
-    router_select_kernel<EPL><<<(T + 7) / 8, 256, 0, s>>>(logits, nz, bias, T, E, K, scale, idx, w, err);
+                                   float top_p, int32_t *idx, float *w, int32_t *err, cudaStream_t s) {
+    router_select_kernel<EPL><<<(T + 7) / 8, 256, 0, s>>>(logits, nz, bias, T, E, K, scale, top_p, idx, w, err);
     return cudaGetLastError();
 }
 
 cudaError_t launch_router_gemm(const float *x, const float *Wr, const float *bias, int T, int D, int E, int K,
-                               float scale, float *logits, int32_t *idx, float *w, int32_t *err, cudaStream_t s) {
+                               float scale, float top_p, float *logits, int32_t *idx, float *w, int32_t *err,
+                               cudaStream_t s) {
     const int nz = D / kRLK < kRouterSplitK ? D / kRLK : kRouterSplitK;
     router_logits_kernel<<<dim3((T + kRLT - 1) / kRLT, (E + kRLE - 1) / kRLE, nz), 256, 0, s>>>(x, Wr, T, D, E,
                                                                                                 logits);
     cudaError_t ce = cudaGetLastError();
     if (ce != cudaSuccess) return ce;
     switch (epl_for(E)) {
-        case 1: return launch_select_t<1>(logits, nz, bias, T, E, K, scale, idx, w, err, s);
-        case 2: return launch_select_t<2>(logits, nz, bias, T, E, K, scale, idx, w, err, s);
-        case 4: return launch_select_t<4>(logits, nz, bias, T, E, K, scale, idx, w, err, s);
-        case 8: return launch_select_t<8>(logits, nz, bias, T, E, K, scale, idx, w, err, s);
-        default: return launch_select_t<16>(logits, nz, bias, T, E, K, scale, idx, w, err, s);
+        case 1: return launch_select_t<1>(logits, nz, bias, T, E, K, scale, top_p, idx, w, err, s);
+        case 2: return launch_select_t<2>(logits, nz, bias, T, E, K, scale, top_p, idx, w, err, s);
+        case 4: return launch_select_t<4>(logits, nz, bias, T, E, K, scale, top_p, idx, w, err, s);
+        case 8: return launch_select_t<8>(logits, nz, bias, T, E, K, scale, top_p, idx, w, err, s);
+        default: return launch_select_t<16>(logits, nz, bias, T, E, K, scale, top_p, idx, w, err, s);
     }
 }
 

@@ -11,6 +11,7 @@ namespace moe {
 struct LayerArgs {
     int D, I, E, K, S, n_shared, T;
     float routed_scale;
+    float top_p;         // adaptive expert top-p in (0, 1); other values: plain top-K
     const float *x;      // [T, D] fp32 layer input (post-norm activations)
     const float *Wr;     // [E, D]
     const float *bias;   // [E]
@@ -58,7 +59,8 @@ cudaError_t launch_permute(const LayerArgs &a, cudaStream_t s);
 // Large-batch router through a logits buffer [T, E]: tiled fp32 GEMM, then
 // one warp per token for the top-K.
 cudaError_t launch_router_gemm(const float *x, const float *Wr, const float *bias, int T, int D, int E, int K,
-                               float scale, float *logits, int32_t *idx, float *w, int32_t *err, cudaStream_t s);
+                               float scale, float top_p, float *logits, int32_t *idx, float *w, int32_t *err,
+                               cudaStream_t s);
 cudaError_t launch_gateup(const LayerArgs &a, int mch, int grid, cudaStream_t s);
 cudaError_t launch_down(const LayerArgs &a, int mch, int grid, bool fused_reduce, cudaStream_t s);
 cudaError_t launch_reduce(const LayerArgs &a, cudaStream_t s);

@@ -153,6 +153,7 @@ int check_desc(const MoeLayerDesc *d) {
     if (d->max_tokens < 1 || d->max_tokens > (1 << 20))
         return fail(MOE_ERR_SHAPE, "max_tokens=%d: need 1 <= max_tokens <= 2^20", d->max_tokens);
     if (!(d->routed_scale == d->routed_scale)) return fail(MOE_ERR_INVALID_ARG, "routed_scale is NaN");
+    if (!(d->top_p == d->top_p)) return fail(MOE_ERR_INVALID_ARG, "top_p is NaN");
     return MOE_OK;
 }
 
@@ -206,6 +207,7 @@ int run_layer(Handle *h, const float *x, int T, float *out, const float *resid, 
     std::memset(&a, 0, sizeof a);
     a.D = h->d.D; a.I = h->d.I; a.E = h->d.E; a.K = h->d.K; a.S = h->S; a.n_shared = h->d.n_shared; a.T = T;
     a.routed_scale = h->d.routed_scale;
+    a.top_p = h->d.top_p;
     a.x = x; a.Wr = h->Wr; a.bias = h->bias; a.experts = h->experts;
     a.xq = h->xq; a.sx = h->sx; a.xsum = h->xsum; a.logits = h->logits; a.idx = h->idx; a.wts = h->wts;
     a.rows = h->rows; a.meta = h->meta; a.h = h->h; a.hamax = h->hamax; a.part = h->part; a.dn_cnt = h->dn_cnt;
@@ -239,8 +241,8 @@ int run_layer(Handle *h, const float *x, int T, float *out, const float *resid, 
         if ((ce = moe::launch_router_small(a, s)) != cudaSuccess) return cuda_fail(ce, "router_small launch");
     } else {
         if ((ce = moe::launch_quant_perm(a, s)) != cudaSuccess) return cuda_fail(ce, "quant launch");
-        if ((ce = moe::launch_router_gemm(x, h->Wr, h->bias, T, a.D, a.E, a.K, a.routed_scale, h->logits, h->idx,
-                                          h->wts, h->err, s)) != cudaSuccess)
+        if ((ce = moe::launch_router_gemm(x, h->Wr, h->bias, T, a.D, a.E, a.K, a.routed_scale, a.top_p, h->logits,
+                                          h->idx, h->wts, h->err, s)) != cudaSuccess)
             return cuda_fail(ce, "router_tile launch");
         if ((ce = moe::launch_permute(a, s)) != cudaSuccess) return cuda_fail(ce, "permute launch");
     }

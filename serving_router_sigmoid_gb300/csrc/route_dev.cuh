@@ -88,14 +88,37 @@ __device__ __forceinline__ uint32_t order_key(float v) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Adaptive expert top-p (aimsg.uk "低配电脑也能跑GLM 5.2" --topp; reader.mx
+// §11 runs the union over the first keff selections of each token): keff is
+// the length of the shortest prefix of the K selections, in selection order,
+// whose routing weights reach top_p times the sum of all K (fp32 sums left to
+// right, the bound one fp32 product), at least 1; top_p outside (0, 1) keeps
+// all K.  w(j) returns the weight of selection j.  Every caller evaluates the
+// same sums in the same order, so the decision is the same everywhere.
+template <typename W>
+__device__ __forceinline__ int topp_keff(W w, int K, float top_p) {
+    if (!(top_p > 0.f && top_p < 1.f)) return K;
+    float total = 0.f;
+    for (int j = 0; j < K; ++j) total = __fadd_rn(total, w(j));
+    const float bound = __fmul_rn(top_p, total);
+    float run = 0.f;
+    for (int j = 0; j < K; ++j) {
+        run = __fadd_rn(run, w(j));
+        if (run >= bound) return j + 1;
+    }
+    return K;
+}
+
 // Greedy top-K of one token by one warp.  Lane l holds experts l + 32 j.
 // Each round takes the largest c among the experts not yet taken; an exact
 // tie goes to the lower expert index (the pages' strict '>' ascending scan).
 // A round is one warp max over the order keys and one warp min over the
-// indices of the lanes that hold that key.  NaN scores never win.
+// indices of the lanes that hold that key.  NaN scores never win.  With
+// top_p in (0, 1) the selections past keff (topp_keff) are dropped: id
+// kDroppedSel, weight 0.
 template <int EPL>
 __device__ __forceinline__ void select_topk(const float (&c)[EPL], const float (&p)[EPL], int E, int K, float scale,
-                            int32_t *idx_out, float *w_out, int *s_idx_out, int32_t *err) {
+                            int32_t *idx_out, float *w_out, int *s_idx_out, int32_t *err, float top_p = 0.f) {
     const int lane = threadIdx.x & 31;
     uint32_t key[EPL];
 #pragma unroll
@@ -136,6 +159,14 @@ __device__ __forceinline__ void select_topk(const float (&c)[EPL], const float (
             idx_out[k] = bi;
             w_out[k] = __fmul_rn(pv, scale);
             if (s_idx_out) s_idx_out[k] = bi;
+        }
+    }
+    if (lane == 0 && top_p > 0.f && top_p < 1.f) {
+        const int keff = topp_keff([&](int j) { return w_out[j]; }, K, top_p);
+        for (int k = keff; k < K; ++k) {
+            idx_out[k] = kDroppedSel;
+            w_out[k] = 0.f;
+            if (s_idx_out) s_idx_out[k] = kDroppedSel;
         }
     }
 }
@@ -182,7 +213,8 @@ __device__ __forceinline__ void warp_sort_desc(unsigned long long (&v)[NPL]) {
 // K (K <= 16) with their sigmoids; then warp g merges the 8 lists of token g.
 // Every logit of the group is loaded before any sort.  Selection order and
 // weights are those of select_topk: weight = sigmoid(logit) * scale, 0 (with
-// kErrNoSelection) for a pick whose score is NaN.  logits: [T][E] (read
+// kErrNoSelection) for a pick whose score is NaN; with top_p in (0, 1) the
+// picks past keff are dropped (id kDroppedSel, weight 0).  logits: [T][E] (read
 // through L2; with POLL the slots are published as data and the CTA reloads
 // them, bounded, until none holds kLogitEmpty).  scratch: shared [4][8][kMaxK]
 // keys, pscr: shared [4][8][kMaxK] sigmoids.  Outputs [T][K]: idx/w (shared or
@@ -192,7 +224,8 @@ template <bool POLL>
 __device__ __forceinline__ void topk_small_cta(const float *logits, const float *__restrict__ bias, int T, int E,
                                                int K, float scale, int32_t *idx, float *w,
                                                unsigned long long *packed, int32_t *err,
-                                               unsigned long long (*scratch)[8][kMaxK], float (*pscr)[8][kMaxK]) {
+                                               unsigned long long (*scratch)[8][kMaxK], float (*pscr)[8][kMaxK],
+                                               float top_p = 0.f) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bool one = E <= 256;  // one expert per lane (else two)
     float bsum[2];
@@ -275,12 +308,19 @@ __device__ __forceinline__ void topk_small_cta(const float *logits, const float 
             } else {
                 warp_sort_desc<4>(v);
             }
+            // the best K are in lanes 0..K-1, in selection order
+            const unsigned long long key = v[0];
+            const int i = (int)(key & 0xFFu);
+            int e = (int)(0xFFFFu - (uint32_t)((key >> 16) & 0xFFFFu));
+            const bool nan_pick = (key >> 32) == 0ull;
+            float wv = (lane < K && !nan_pick) ? __fmul_rn(pscr[warp][i / K][i % K], scale) : 0.f;
+            // adaptive top-p: every lane evaluates keff over the K weights
+            const int keff = topp_keff([&](int j) { return __shfl_sync(0xffffffffu, wv, j); }, K, top_p);
+            if (lane >= keff) {
+                e = kDroppedSel;
+                wv = 0.f;
+            }
             if (lane < K) {
-                const unsigned long long key = v[0];
-                const int i = (int)(key & 0xFFu);
-                const int e = (int)(0xFFFFu - (uint32_t)((key >> 16) & 0xFFFFu));
-                const bool nan_pick = (key >> 32) == 0ull;
-                const float wv = nan_pick ? 0.f : __fmul_rn(pscr[warp][i / K][i % K], scale);
                 if (packed) {
                     st_relaxed_u64(packed + t * K + lane, ((unsigned long long)(uint32_t)e << 32) | __float_as_uint(wv));
                 } else {

@@ -106,28 +106,36 @@ def check_layer(pair, sample=None, x=None):
     ref, od = OL.forward(xs, debug=True)
 
     # routing.  The set of experts of each token is identical (the inputs keep
-    # a margin of >= 1e-5 between the K-th and (K+1)-th score).  The selection
-    # order is identical except inside runs of consecutive picks whose oracle
-    # scores c = sigmoid(logit) + bias lie within 1e-5 of each other: there it
+    # a margin of >= 1e-5 between the K-th and (K+1)-th score, and with
+    # adaptive top-p one around the keff decision).  The selection order is
+    # identical except inside runs of consecutive picks whose oracle scores
+    # c = sigmoid(logit) + bias lie within 1e-5 of each other: there it
     # follows the last bits of the logits, which the GPU sums in another fp32
     # order, and both orders are correct.  Every per-slot array is compared
-    # after mapping each oracle slot to the GPU slot holding the same expert.
+    # after mapping each oracle slot to the GPU slot holding the same expert;
+    # slots that top-p dropped (id -1, weight 0, at the tail on both sides)
+    # have no expert output and are not compared.
     gi, oi = g["idx"][tok], od["idx"]
     np.testing.assert_array_equal(np.sort(gi, 1), np.sort(oi, 1))
+    kept = oi >= 0
+    np.testing.assert_array_equal(gi >= 0, kept)
+    assert (np.diff(kept.astype(np.int8), axis=1) <= 0).all()  # dropped slots form the tail
     _, _, p_or = oracle.router(xs, pair.Wr.numpy(), pair.bias.numpy(), cfg.K, cfg.routed_scale)
     c_or = (p_or + pair.bias.numpy()[None, :]).astype(np.float32)
-    c_pick = np.take_along_axis(c_or, oi.astype(np.int64), 1)
+    c_pick = np.take_along_axis(c_or, np.where(kept, oi, 0).astype(np.int64), 1)
     run = np.concatenate([np.zeros((len(tok), 1), np.int64),
                           np.cumsum(np.abs(np.diff(c_pick, axis=1)) >= 1e-5, axis=1)], axis=1)
     perm = np.empty((len(tok), cfg.S), np.int64)
     for j in range(len(tok)):
-        pos = {int(e): k for k, e in enumerate(gi[j])}
-        perm[j, :cfg.K] = [pos[int(e)] for e in oi[j]]
+        pos = {int(e): k for k, e in enumerate(gi[j]) if e >= 0}
+        perm[j, :cfg.K] = [pos[int(e)] if e >= 0 else k for k, e in enumerate(oi[j])]
         # the GPU slot of every pick lies inside the pick's run of near ties
-        assert all(run[j, perm[j, k]] == run[j, k] for k in range(cfg.K)), (j, gi[j], oi[j])
+        assert all(run[j, perm[j, k]] == run[j, k] for k in range(cfg.K) if kept[j, k]), (j, gi[j], oi[j])
     if cfg.n_shared:
         perm[:, cfg.K] = cfg.K
     n_swapped = int((perm[:, :cfg.K] != np.arange(cfg.K)[None, :]).any(axis=1).sum())
+    valid = np.ones((len(tok), cfg.S), bool)
+    valid[:, :cfg.K] = kept
 
     def by_oracle_slot(a, slots=cfg.S):
         p = perm[:, :slots].reshape(perm.shape[0], slots, *([1] * (a.ndim - 2)))
@@ -142,19 +150,19 @@ def check_layer(pair, sample=None, x=None):
     un = g["union_experts"][:nu]
     routed = un[:-1] if cfg.n_shared else un
     assert len(set(routed.tolist())) == len(routed)
-    assert set(routed.tolist()) == set(g["idx"].reshape(-1).tolist())
+    assert set(routed.tolist()) == set(g["idx"][g["idx"] >= 0].tolist())
     if cfg.n_shared:
         assert un[-1] == cfg.E
     if sample is None:
         assert set(routed.tolist()) == set(od["uniq"].tolist())
-    # exact int32 dot products
-    np.testing.assert_array_equal(by_oracle_slot(g["gate_acc"][tok]), od["gate_acc"])
-    np.testing.assert_array_equal(by_oracle_slot(g["up_acc"][tok]), od["up_acc"])
-    hq_g, hq_o = by_oracle_slot(g["hq"][tok]), od["hq"]
+    # exact int32 dot products (every slot with an expert output)
+    np.testing.assert_array_equal(by_oracle_slot(g["gate_acc"][tok])[valid], od["gate_acc"][valid])
+    np.testing.assert_array_equal(by_oracle_slot(g["up_acc"][tok])[valid], od["up_acc"][valid])
+    hq_g, hq_o = by_oracle_slot(g["hq"][tok])[valid], od["hq"][valid]
     mism = int(np.count_nonzero(hq_g != hq_o))
     assert np.abs(hq_g.astype(np.int32) - hq_o.astype(np.int32)).max() <= 1
     assert mism <= 1e-4 * hq_g.size, f"{mism} of {hq_g.size} hq codes differ"
-    np.testing.assert_allclose(by_oracle_slot(g["sh"][tok]), od["sh"], rtol=1e-6, atol=0)
+    np.testing.assert_allclose(by_oracle_slot(g["sh"][tok])[valid], od["sh"][valid], rtol=1e-6, atol=0)
     if n_swapped:
         print(f"{n_swapped} token(s) with near-tied picks in another order")
     # down dots bit-exact against the plain integer dot of the oracle's
@@ -167,7 +175,7 @@ def check_layer(pair, sample=None, x=None):
     if cfg.n_shared:
         eid[:, cfg.K] = cfg.E
     hq_rows, dn_rows = g["hq"][tok], g["down_acc"][tok]
-    for e in np.unique(eid):
+    for e in np.unique(eid[eid >= 0]):
         sel = eid == e
         dq = unpack_np(pair.oracle_expert(int(e)).dq, cfg.I).astype(np.float64)
         ad = hq_rows[sel].astype(np.float64) @ dq.T
@@ -202,6 +210,45 @@ def test_layer_parity_small(moe, case):
             check_layer(pair, x=pair.x[:1].clone())
         out = torch.empty((0, cfg.D), device="cuda")
         pair.gpu.moe_layer_forward(torch.empty((0, cfg.D), device="cuda"), out)
+    finally:
+        pair.close()
+
+
+TOPP_CASES = [
+    (dict(D=256, I=128, E=16, K=4, n_shared=1, T=1), 0.7),     # single decode kernel, one token
+    (dict(D=256, I=128, E=16, K=4, n_shared=1, T=4), 0.5),
+    (dict(D=256, I=128, E=16, K=4, n_shared=1, T=16), 0.7),
+    (dict(D=256, I=128, E=16, K=4, n_shared=1, T=17), 0.7),    # large-batch router, tcgen05 GEMMs
+    (dict(D=512, I=256, E=8, K=4, n_shared=1, T=300), 0.6),    # several token blocks per expert
+    (dict(D=1056, I=96, E=40, K=5, n_shared=0, T=9), 0.8),     # no shared expert
+    (dict(D=1056, I=96, E=40, K=5, n_shared=0, T=24), 0.8),    # untiled shapes above 16 tokens
+]
+
+
+@pytest.mark.parametrize("case,top_p", TOPP_CASES,
+                         ids=lambda v: f"p{v}" if isinstance(v, float) else
+                         "D{D}-I{I}-E{E}-K{K}-S{n_shared}-T{T}".format(**v))
+def test_layer_parity_adaptive_top_p(moe, case, top_p):
+    """Adaptive expert top-p: the same kept selections, union, integer dots
+    and output as the oracle; fewer union experts than plain top-K; at decode
+    sizes the four-kernel plan equals the single kernel bit for bit."""
+    cfg = synth.LayerCfg("topp", **case, seed=case["T"] * 17 + case["E"])
+    pair = LayerPair(cfg, wdev="cpu", top_p=top_p)
+    try:
+        check_layer(pair)
+        xd = pair.x.cuda()
+        d = pair.gpu.moe_layer_debug(xd, idx=True, union=True)
+        torch.cuda.synchronize()
+        idx = d["idx"].cpu().numpy()
+        assert (idx < 0).any(), "top-p dropped nothing: the case does not exercise it"
+        if cfg.T <= 16:
+            a = pair.gpu.forward(xd)
+            pair.gpu.set_option(moe.MOE_OPT_DECODE_SINGLE_KERNEL, 0)
+            b = pair.gpu.forward(xd)
+            pair.gpu.set_option(moe.MOE_OPT_DECODE_SINGLE_KERNEL, 1)
+            torch.cuda.synchronize()
+            assert torch.equal(a, b)
+        assert pair.gpu.device_status() == 0
     finally:
         pair.close()
 
@@ -257,14 +304,16 @@ def test_layer_rejects_bad_arguments(moe):
 # ------------------------------------------------------- GLM-shaped layer
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name,sample", [("glm_decode_b1", None), ("glm_verify_b8", None),
-                                         ("glm_prefill_2048", None)])
-def test_glm_layer_parity(moe, name, sample):
+@pytest.mark.parametrize("name,top_p", [("glm_decode_b1", 0.0), ("glm_verify_b8", 0.0), ("glm_prefill_2048", 0.0),
+                                        ("glm_decode_b1", 0.7), ("glm_verify_b8", 0.7), ("glm_prefill_2048", 0.7)])
+def test_glm_layer_parity(moe, name, top_p):
     """The GLM-shaped layer at decode batch 1, verify batch 8 and prefill 2048
     tokens (Zipf-skewed routing: the hottest expert gets ~300 tokens, several
-    tcgen05 token blocks), every token compared with the oracle."""
+    tcgen05 token blocks), every token compared with the oracle; plain top-8
+    and adaptive top-p 0.7."""
+    sample = None
     cfg = synth.CONFIGS[name]
-    pair = LayerPair(cfg, wdev="cuda")
+    pair = LayerPair(cfg, wdev="cuda", top_p=top_p)
     try:
         # GPU packing of a few full-size experts is byte-exact with the oracle's
         for e in (0, cfg.E):
@@ -273,7 +322,7 @@ def test_glm_layer_parity(moe, name, sample):
             for a, b in ((gq, px.gq), (gs, px.gs), (uq, px.uq), (us, px.us), (dq, px.dq), (ds, px.ds)):
                 np.testing.assert_array_equal(a, b)
         r, m, mism = check_layer(pair, sample)
-        print(f"{name}: rel_l2={r:.2e} max_abs={m:.2e} hq_mismatch={mism}")
+        print(f"{name} top_p={top_p}: rel_l2={r:.2e} max_abs={m:.2e} hq_mismatch={mism}")
     finally:
         pair.close()
         torch.cuda.empty_cache()
