@@ -580,7 +580,9 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
     const int gpd = D / RPD;
     int rp0, rp1, dp0, dp1;
     if (MCH == 1) {  // one token: every group costs the same, an even split
-        const long long Nr = (long long)n_r * I, Nd = (long long)n_u * gpd;
+        // (the shared expert's gate/up ran in phase 1 unless adaptive top-p
+        // moved it here)
+        const long long Nr = (long long)(sh_early ? n_r : n_u) * I, Nd = (long long)n_u * gpd;
         rp0 = (int)(b * Nr / G);
         rp1 = (int)((b + 1) * Nr / G);
         if (G >= n_u) {
