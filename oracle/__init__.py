@@ -47,7 +47,7 @@ class _Layer(ctypes.Structure):
                 ("K", ctypes.c_int), ("n_shared", ctypes.c_int),
                 ("routed_scale", ctypes.c_float),
                 ("Wr", ctypes.c_void_p), ("bias", ctypes.c_void_p),
-                ("experts", ctypes.POINTER(_Expert)), ("top_p", ctypes.c_float)]
+                ("experts", ctypes.POINTER(_Expert)), ("top_p", ctypes.c_float), ("weight_bits", ctypes.c_int)]
 
 
 class _Debug(ctypes.Structure):
@@ -69,6 +69,9 @@ def lib():
         L.orc_quant_act.argtypes = [vp, vp, vp, i64, i64]
         L.orc_dot_i4_i8.argtypes = [vp, vp, i64]
         L.orc_dot_i4_i8.restype = ctypes.c_int32
+        L.orc_quantize_rows.argtypes = [vp, vp, vp, i64, i64, ci]
+        L.orc_dot_i8_i8.argtypes = [vp, vp, i64]
+        L.orc_dot_i8_i8.restype = ctypes.c_int32
         L.orc_router.argtypes = [vp, vp, vp, ci, ci, ci, ci, cf, vp, vp, vp]
         L.orc_router_gap_f64.argtypes = [vp, vp, vp, ci, ci, ci, ci, vp]
         L.orc_topp_keff.argtypes = [vp, ci, cf]
@@ -179,6 +182,23 @@ def dot_i4_i8(q4row, x):
     return int(lib().orc_dot_i4_i8(_p(q4row), _p(x), x.shape[0]))
 
 
+def quantize_rows(w, bits=8):
+    """w [O, I] fp32 -> (q [O, I] int8, scale [O] fp32), per-row symmetric."""
+    w = _c(w, np.float32)
+    O, I = w.shape
+    q = np.empty((O, I), np.int8)
+    s = np.empty(O, np.float32)
+    lib().orc_quantize_rows(_p(w), _p(q), _p(s), O, I, int(bits))
+    return q, s
+
+
+def dot_i8_i8(w, x):
+    w = _c(w, np.int8).reshape(-1)
+    x = _c(x, np.int8).reshape(-1)
+    assert w.shape == x.shape
+    return int(lib().orc_dot_i8_i8(_p(w), _p(x), x.shape[0]))
+
+
 def router(x, Wr, bias, K, routed_scale=2.5):
     """-> (idx [T,K] int32, w [T,K] fp32, p [T,E] fp32)."""
     x = _c(x, np.float32)
@@ -238,20 +258,23 @@ class PackedExpert:
     ds: np.ndarray
 
 
-def pack_expert(gate, up, down) -> PackedExpert:
-    gq, gs = pack_int4(gate)
-    uq, us = pack_int4(up)
-    dq, ds = pack_int4(down)
+def pack_expert(gate, up, down, bits=4) -> PackedExpert:
+    """bits 4: packed int4 rows (pack_int4); bits 8: int8 rows (quantize_rows)."""
+    pack = pack_int4 if bits == 4 else (lambda w: quantize_rows(w, 8))
+    gq, gs = pack(gate)
+    uq, us = pack(up)
+    dq, ds = pack(down)
     return PackedExpert(gq, gs, uq, us, dq, ds)
 
 
 class Layer:
     """Keeps the numpy buffers alive for the ctypes layer description."""
 
-    def __init__(self, D, I, E, K, n_shared, routed_scale, Wr, bias, experts, top_p=0.0):
+    def __init__(self, D, I, E, K, n_shared, routed_scale, Wr, bias, experts, top_p=0.0, weight_bits=4):
         """experts: dict or list, index -> PackedExpert (shared expert at index E).
         Missing entries are passed as NULL and must not be selected.  top_p in
-        (0, 1) turns on adaptive expert top-p (dropped selections: id -1)."""
+        (0, 1) turns on adaptive expert top-p (dropped selections: id -1).
+        weight_bits 8: the experts hold int8 rows (pack_expert(..., bits=8))."""
         self.D, self.I, self.E, self.K, self.n_shared = D, I, E, K, n_shared
         self.Wr = _c(Wr, np.float32)
         self.bias = _c(bias, np.float32)
@@ -263,7 +286,9 @@ class Layer:
             arr[e] = _Expert(_p(px.gq), _p(px.uq), _p(px.dq), _p(px.gs), _p(px.us), _p(px.ds))
         self._arr = arr
         self.top_p = float(top_p)
-        self._c = _Layer(D, I, E, K, n_shared, float(routed_scale), _p(self.Wr), _p(self.bias), arr, self.top_p)
+        self.weight_bits = int(weight_bits)
+        self._c = _Layer(D, I, E, K, n_shared, float(routed_scale), _p(self.Wr), _p(self.bias), arr, self.top_p,
+                         self.weight_bits)
 
     def forward(self, x, debug: bool = False):
         x = _c(x, np.float32)

@@ -171,6 +171,42 @@ int32_t orc_dot_i4_i8(const uint8_t *q4row, const int8_t *x, int64_t n) {
 }
 
 /* ---------------------------------------------------------------------------
+ * int8 weights.  [A] §05 quantize_rows (the OLMoE prototype's per-row int8
+ * weights, also the engine's fmt 1): qmax = 2^(bits-1) - 1, s = amax/qmax
+ * floored at 1e-8, value = nearest integer of w/s (a true division, ties to
+ * even as lrintf), clamped to [-qmax-1, qmax], one value per int8.  [A] §12
+ * dot_i8i8: the int8 x int8 dot, exact in int32 (its scalar tail is the
+ * plain definition).
+ * ------------------------------------------------------------------------- */
+void orc_quantize_rows(const float *w, int8_t *q, float *scale, int64_t O, int64_t I, int bits) {
+    const int qmax = (1 << (bits - 1)) - 1;
+#pragma omp parallel for schedule(static)
+    for (int64_t o = 0; o < O; o++) {
+        const float *row = w + o * I;
+        float amax = 0.f;
+        for (int64_t i = 0; i < I; i++) {
+            float a = fabsf(row[i]);
+            if (a > amax) amax = a;
+        }
+        float s = amax / (float)qmax;
+        if (s < 1e-8f) s = 1e-8f;
+        scale[o] = s;
+        for (int64_t i = 0; i < I; i++) {
+            int v = (int)lrintf(row[i] / s);
+            if (v > qmax) v = qmax;
+            if (v < -qmax - 1) v = -qmax - 1;
+            q[o * I + i] = (int8_t)v;
+        }
+    }
+}
+
+int32_t orc_dot_i8_i8(const int8_t *w, const int8_t *x, int64_t n) {
+    int32_t acc = 0;
+    for (int64_t i = 0; i < n; i++) acc += (int32_t)w[i] * (int32_t)x[i];
+    return acc;
+}
+
+/* ---------------------------------------------------------------------------
  * Router.  [A] §11 ("sigmoid(logit)+bias picks top-K, weight is plain
  * sigmoid"), [B] §11, model config (scoring_func sigmoid, 256 experts, top-8,
  * routed_scaling_factor 2.5).
@@ -303,20 +339,26 @@ void orc_rmsnorm(const float *x, const float *w, float *out, int D, float eps) {
 /* ---------------------------------------------------------------------------
  * One SwiGLU expert on one activation row, integer path.
  * [A] §11 (gate/up, siluf(g)*u, down), §04 siluf, §12 (int8 activations x
- * int4 weights, integer dot, then scales).
+ * int4 weights, or int8 weights for fmt 1, integer dot, then scales).
  *   ag[o] = dot(gate row o, xq), au[o] likewise            (int32, exact)
  *   g = (ag*sx)*sg[o], u = (au*sx)*su[o], h[o] = g/(1+expf(-g)) * u
  *   (hq, sh) = per-row int8 quantisation of h
  *   ad[o] = dot(down row o, hq); y[o] = (ad*sh)*sd[o]
  * ------------------------------------------------------------------------- */
-static void expert_row(const OrcExpert *ex, int D, int I, const int8_t *xq, float sx,
+/* Dot of output row o of a weight matrix with n columns (int4 packed or
+ * int8 rows) against int8 activations. */
+static int32_t row_dot(const uint8_t *mat, int bits, int64_t o, const int8_t *x, int64_t n) {
+    if (bits == 8) return orc_dot_i8_i8((const int8_t *)mat + o * n, x, n);
+    return orc_dot_i4_i8(mat + o * ((n + 1) / 2), x, n);
+}
+
+static void expert_row(const OrcExpert *ex, int bits, int D, int I, const int8_t *xq, float sx,
                        float *h, int8_t *hq, float *y, int32_t *gacc, int32_t *uacc,
                        float *sh_out, int32_t *dacc) {
-    const int64_t gbytes = (D + 1) / 2, dbytes = (I + 1) / 2;
 #pragma omp parallel for schedule(static)
     for (int o = 0; o < I; o++) {
-        int32_t ag = orc_dot_i4_i8(ex->gq + (int64_t)o * gbytes, xq, D);
-        int32_t au = orc_dot_i4_i8(ex->uq + (int64_t)o * gbytes, xq, D);
+        int32_t ag = row_dot(ex->gq, bits, o, xq, D);
+        int32_t au = row_dot(ex->uq, bits, o, xq, D);
         if (gacc) gacc[o] = ag;
         if (uacc) uacc[o] = au;
         float g = ((float)ag * sx) * ex->gs[o];
@@ -328,7 +370,7 @@ static void expert_row(const OrcExpert *ex, int D, int I, const int8_t *xq, floa
     if (sh_out) *sh_out = sh;
 #pragma omp parallel for schedule(static)
     for (int o = 0; o < D; o++) {
-        int32_t ad = orc_dot_i4_i8(ex->dq + (int64_t)o * dbytes, hq, I);
+        int32_t ad = row_dot(ex->dq, bits, o, hq, I);
         if (dacc) dacc[o] = ad;
         y[o] = ((float)ad * sh) * ex->ds[o];
     }
@@ -348,6 +390,7 @@ static void expert_row(const OrcExpert *ex, int D, int I, const int8_t *xq, floa
 int orc_layer_forward(const OrcLayer *L, const float *x, int T, float *out, OrcDebug *dbg) {
     const int D = L->D, I = L->I, E = L->E, K = L->K, S = L->K + L->n_shared;
     if (K < 1 || K > E || L->n_shared < 0 || L->n_shared > 1) return -1;
+    if (L->weight_bits != 0 && L->weight_bits != 4 && L->weight_bits != 8) return -1;
     int8_t *xq = (int8_t *)malloc((size_t)T * D + 1);
     float *sx = (float *)malloc(sizeof(float) * ((size_t)T + 1));
     int32_t *idx = (int32_t *)malloc(sizeof(int32_t) * ((size_t)T * K + 1));
@@ -386,7 +429,7 @@ int orc_layer_forward(const OrcLayer *L, const float *x, int T, float *out, OrcD
                 const int slot = shared ? K : k;
                 const float wt = shared ? 1.f : w[(int64_t)t * K + k];
                 const int64_t ts = (int64_t)t * S + slot;
-                expert_row(ex, D, I, xq + (int64_t)t * D, sx[t], h, hq, y,
+                expert_row(ex, L->weight_bits == 8 ? 8 : 4, D, I, xq + (int64_t)t * D, sx[t], h, hq, y,
                            dbg && dbg->gate_acc ? dbg->gate_acc + ts * I : NULL,
                            dbg && dbg->up_acc ? dbg->up_acc + ts * I : NULL,
                            dbg && dbg->sh ? dbg->sh + ts : NULL,

@@ -10,6 +10,7 @@
  *   [A] reader.mx, "惊呆了！25GB 内存上运行 GLM 5.2 744B 模型":
  *       §02 model config (FP8 e4m3 checkpoint, 128 x 128 weight blocks),
  *       §04 手写的基础数学 (rmsnorm, siluf, layer order),
+ *       §05 先用 400 行验证流式思路 (per-row int8 weights, quantize_rows),
  *       §06 从 FP8 到 int4 (FP8 block-scale decoding, per-row int4 packer,
  *           nibble layout, worked example),
  *       §11 MoE 路由与专家执行 (sigmoid+bias top-K router, expert union over the
@@ -33,7 +34,9 @@ extern "C" {
 #endif
 
 /* One expert: gate/up are [I, ceil(D/2)] packed int4 + [I] fp32 row scales,
- * down is [D, ceil(I/2)] packed int4 + [D] fp32 row scales. */
+ * down is [D, ceil(I/2)] packed int4 + [D] fp32 row scales; in an int8-weight
+ * layer (weight_bits 8) gate/up are [I, D] int8 and down [D, I] int8 (the
+ * pointers then point at int8 codes). */
 typedef struct {
     const uint8_t *gq, *uq, *dq;
     const float *gs, *us, *ds;
@@ -48,6 +51,7 @@ typedef struct {
     const float *bias; /* [E] fp32 correction bias */
     const OrcExpert *experts;
     float top_p;       /* adaptive expert top-p in (0, 1); 0 or >= 1: plain top-K */
+    int weight_bits;   /* 4 (packed int4, the default; 0 also means 4) or 8 (int8 rows [O, I]) */
 } OrcLayer;
 
 /* Optional per-(token, slot) intermediates; every pointer may be NULL.
@@ -85,6 +89,10 @@ void  orc_fp8_block_to_int4(const uint8_t *w8, const float *scale_inv, uint8_t *
 float orc_qrow_i8(const float *x, int8_t *q, int64_t n);
 void  orc_quant_act(const float *x, int8_t *xq, float *sx, int64_t T, int64_t D);
 int32_t orc_dot_i4_i8(const uint8_t *q4row, const int8_t *x, int64_t n);
+/* Per-row symmetric quantisation to `bits` (2..8) stored one value per int8
+ * ([A] §05 quantize_rows) and the int8 x int8 dot ([A] §12 dot_i8i8). */
+void  orc_quantize_rows(const float *w, int8_t *q, float *scale, int64_t O, int64_t I, int bits);
+int32_t orc_dot_i8_i8(const int8_t *w, const int8_t *x, int64_t n);
 void  orc_router(const float *x, const float *Wr, const float *bias, int T, int D, int E,
                  int K, float routed_scale, int32_t *idx, float *w, float *p_out);
 void  orc_router_gap_f64(const float *x, const float *Wr, const float *bias, int T, int D,

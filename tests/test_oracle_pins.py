@@ -556,3 +556,104 @@ def test_topp_layer_drops_the_tail_selections_only():
         assert len(d["uniq"]) <= prev_nu
         prev_nu = len(d["uniq"])
     assert prev_nu < len(dfull["uniq"])
+
+
+# ------------------------------------------------------------ int8 weights --
+# reader.mx §05 quantize_rows (per-row int8 weights) and §12 dot_i8i8.
+
+def test_quantize_rows_hand_example_and_ties():
+    row = np.array([[127.0, 0.5, 1.5, 2.5, -2.5, -127.0, 63.5, 64.5, -0.5, 0.0]], np.float32)
+    q, s = oracle.quantize_rows(row, 8)
+    assert s[0] == np.float32(1.0)  # amax 127 -> s = 127/127
+    np.testing.assert_array_equal(q[0], [127, 0, 2, 2, -2, -127, 64, 64, 0, 0])
+
+
+def test_quantize_rows_round_trip_every_code_and_zero_row():
+    rng = np.random.default_rng(40)
+    O, I = 32, 300
+    q = rng.integers(-127, 128, size=(O, I))
+    q[:, 7] = np.where(rng.random(O) < 0.5, 127, -127)  # amax = 127 s in every row
+    s = rng.uniform(1e-4, 1.0, size=(O, 1)).astype(np.float32)
+    w = (q * s).astype(np.float32)
+    w[3] = 0.0
+    qq, ss = oracle.quantize_rows(w, 8)
+    keep = np.arange(O) != 3
+    np.testing.assert_array_equal(qq[keep], q[keep])
+    np.testing.assert_allclose(ss[keep], s[keep, 0], rtol=2e-7)
+    assert ss[3] == np.float32(1e-8) and not qq[3].any()
+    assert qq.min() >= -127  # s = amax/127 never yields -128 for real data
+
+
+def test_quantize_rows_four_bits_equals_the_int4_packer():
+    """quantize_rows(bits=4) and the int4 packer state the same rule (s =
+    amax/7, nearest of w/s, clamp [-8, 7]): the codes and scales agree."""
+    rng = np.random.default_rng(41)
+    w = (rng.standard_normal((40, 257)) * 0.02).astype(np.float32)
+    q, s = oracle.quantize_rows(w, 4)
+    q4, s4 = oracle.pack_int4(w)
+    np.testing.assert_array_equal(q, oracle.unpack_int4(q4, 257))
+    np.testing.assert_array_equal(s, s4)
+
+
+def test_dot_i8_i8_numpy_and_extremes():
+    rng = np.random.default_rng(42)
+    for n in (1, 31, 6144):
+        w = rng.integers(-128, 128, n).astype(np.int8)
+        x = rng.integers(-127, 128, n).astype(np.int8)
+        assert oracle.dot_i8_i8(w, x) == int(np.dot(w.astype(np.int64), x.astype(np.int64)))
+    n = 6144
+    assert oracle.dot_i8_i8(np.full(n, 127, np.int8), np.full(n, 127, np.int8)) == 127 * 127 * n
+    assert oracle.dot_i8_i8(np.full(n, -128, np.int8), np.full(n, -127, np.int8)) == 128 * 127 * n
+
+
+def _make_layer8(D, I, E, K, n_shared, seed):
+    rng = np.random.default_rng(seed)
+    Wr = (rng.standard_normal((E, D)) * 0.02).astype(np.float32)
+    b = rng.uniform(-0.1, 0.1, E).astype(np.float32)
+    packed = []
+    for _ in range(E + n_shared):
+        g = (rng.standard_normal((I, D)) * 0.02).astype(np.float32)
+        u = (rng.standard_normal((I, D)) * 0.02).astype(np.float32)
+        d = (rng.standard_normal((D, I)) * 0.02).astype(np.float32)
+        packed.append(oracle.pack_expert(g, u, d, bits=8))
+    return oracle.Layer(D, I, E, K, n_shared, 2.5, Wr, b, packed, weight_bits=8), Wr, b, packed
+
+
+def test_int8_layer_accumulators_exact_and_close_to_dequantised_double():
+    D, I, E, K = 256, 128, 16, 2
+    L, Wr, b, packed = _make_layer8(D, I, E, K, 1, seed=43)
+    x = np.random.default_rng(44).standard_normal((6, D)).astype(np.float32)
+    assert oracle.router_gap_f64(x, Wr, b, K).min() > 1e-5
+    out, dbg = L.forward(x, debug=True)
+    xq = dbg["xq"].astype(np.int64)
+    for t in range(6):
+        for s in range(K + 1):
+            px = packed[E if s == K else dbg["idx"][t, s]]
+            np.testing.assert_array_equal(dbg["gate_acc"][t, s], px.gq.astype(np.int64) @ xq[t])
+            np.testing.assert_array_equal(dbg["up_acc"][t, s], px.uq.astype(np.int64) @ xq[t])
+            np.testing.assert_array_equal(dbg["down_acc"][t, s],
+                                          px.dq.astype(np.int64) @ dbg["hq"][t, s].astype(np.int64))
+    # the dequantised layer in double: int8 weights leave only the two int8
+    # activation quantisations (~0.5-1%); reading the codes as int4 would not
+    x64 = x.astype(np.float64)
+    p = 1 / (1 + np.exp(-(x64 @ Wr.astype(np.float64).T)))
+    c = p + b.astype(np.float64)
+    def mlp(px, xt):
+        g = (px.gq * px.gs[:, None].astype(np.float64)) @ xt
+        u = (px.uq * px.us[:, None].astype(np.float64)) @ xt
+        return (px.dq * px.ds[:, None].astype(np.float64)) @ (g / (1 + np.exp(-g)) * u)
+
+    def ref_with(scale, shared=True):
+        r = np.zeros((6, D))
+        for t in range(6):
+            for e in np.lexsort((np.arange(E), -c[t]))[:K]:
+                r[t] += scale * p[t, e] * mlp(packed[e], x64[t])
+            if shared:
+                r[t] += mlp(packed[E], x64[t])
+        return r
+
+    err = _rel_l2(out, ref_with(2.5))
+    assert 1e-4 < err < 0.03, err
+    # plausible mistakes land far outside that band
+    assert _rel_l2(out, ref_with(1.0)) > 0.1
+    assert _rel_l2(out, ref_with(2.5, shared=False)) > 0.1
