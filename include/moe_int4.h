@@ -73,6 +73,19 @@ int moe_pack_int4(const float *w, uint8_t *q4, float *scale, int64_t O, int64_t 
                   cudaStream_t stream);
 
 /*
+ * Per-row int8 weights (the int8-weight expert format).
+ * reader.mx article §05 (quantize_rows with bits = 8) and §12 (fmt 1:
+ * matmul_q_idot, int8 weights x int8 activations).
+ *   w     [O, I] fp32, row-major (any alignment)
+ *   q8    [O, I] int8 out, natural order
+ *   scale [O] fp32 out: s = max(amax_row / 127, 1e-8)
+ * value = nearest integer of w/s (IEEE division, ties to even), clamped to
+ * [-128, 127].  Byte-exact with the quantiser described on the pages.
+ * Errors: INVALID_ARG for NULL pointers, SHAPE for O < 0, I < 0 or O*I >= 2^62.
+ */
+int moe_pack_int8(const float *w, int8_t *q8, float *scale, int64_t O, int64_t I, cudaStream_t stream);
+
+/*
  * The checkpoint converter's step: an FP8 weight matrix to the packed int4
  * layout.  reader.mx article §02 (checkpoint config: fmt e4m3,
  * weight_block_size [128, 128]) and §06 (FP8 block-scale decoding, then the
@@ -141,11 +154,18 @@ typedef struct {
                          * are dropped (no expert read, no term in the sum; in
                          * moe_layer_debug their idx is -1 and w 0).  0 (or any value
                          * outside (0, 1)): plain top-K.  NaN: INVALID_ARG. */
+    int weight_bits;    /* expert weight width: 4 (packed int4, moe_pack_int4; 0 also
+                         * means 4) or 8 (per-row int8, moe_pack_int8: reader.mx
+                         * article §05 quantize_rows, §12 int8 x int8 dot).  int8
+                         * layers run the row-per-warp expert kernels at every batch
+                         * size (neither the single decode kernel nor the tensor-core
+                         * GEMMs). */
 } MoeLayerDesc;
 
 /* One expert's packed weights (device pointers, as moe_pack_int4 writes them):
  * gate_q/up_q [I, D/2] uint8, gate_s/up_s [I] fp32, down_q [D, I/2] uint8,
- * down_s [D] fp32.  Every pointer 16-byte aligned. */
+ * down_s [D] fp32.  Every pointer 16-byte aligned.  With weight_bits 8 (as
+ * moe_pack_int8 writes them): gate_q/up_q [I, D] int8, down_q [D, I] int8. */
 typedef struct {
     const uint8_t *gate_q, *up_q, *down_q;
     const float *gate_s, *up_s, *down_s;

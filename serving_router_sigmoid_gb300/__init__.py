@@ -35,7 +35,7 @@ if not os.path.exists(LIB_PATH):
 class MoeLayerDesc(ctypes.Structure):
     _fields_ = [("D", ctypes.c_int), ("I", ctypes.c_int), ("E", ctypes.c_int), ("K", ctypes.c_int),
                 ("n_shared", ctypes.c_int), ("routed_scale", ctypes.c_float), ("max_tokens", ctypes.c_int),
-                ("top_p", ctypes.c_float)]
+                ("top_p", ctypes.c_float), ("weight_bits", ctypes.c_int)]
 
 
 class MoeExpertW(ctypes.Structure):
@@ -57,6 +57,7 @@ _SIGS = {
     "moe_pack_int4": ([_vp, _vp, _vp, _i64, _i64, _vp], _ci),
     "moe_quant_act_int8": ([_vp, _vp, _vp, _ci, _ci, _vp], _ci),
     "moe_fp8_block_to_int4": ([_vp, _vp, _vp, _vp, _i64, _i64, _vp], _ci),
+    "moe_pack_int8": ([_vp, _vp, _vp, _i64, _i64, _vp], _ci),
     "moe_router_topk": ([_vp, _vp, _vp, _ci, _ci, _ci, _ci, _cf, _vp, _vp, _vp], _ci),
     "moe_layer_create": ([ctypes.POINTER(MoeLayerDesc), _vp, _vp, ctypes.POINTER(MoeExpertW),
                           ctypes.POINTER(_vp)], _ci),
@@ -151,6 +152,20 @@ def fp8_block_to_int4(w8, scale_inv, stream=None):
     return q4, s
 
 
+def moe_pack_int8(w, q8, scale, stream=None):
+    O, I = w.shape
+    _check(_lib.moe_pack_int8(_ptr(w), _ptr(q8), _ptr(scale), O, I, _stream(stream)))
+
+
+def pack_int8(w, stream=None):
+    """Allocating convenience wrapper: w [O, I] fp32 (cuda) -> (q8 int8 [O, I], scale)."""
+    O, I = w.shape
+    q8 = torch.empty((O, I), dtype=torch.int8, device=w.device)
+    s = torch.empty(O, dtype=torch.float32, device=w.device)
+    moe_pack_int8(w, q8, s, stream)
+    return q8, s
+
+
 def pack_int4(w, stream=None):
     """Allocating convenience wrapper: w [O, I] fp32 (cuda) -> (q4, scale)."""
     O, I = w.shape
@@ -164,16 +179,19 @@ class MoeLayer:
     """Owns a library handle; borrows (and keeps alive) the weight tensors.
 
     experts: list of E + n_shared tuples (gate_q, gate_s, up_q, up_s, down_q, down_s)
-    of CUDA tensors as moe_pack_int4 writes them; entry E is the shared expert.
+    of CUDA tensors as moe_pack_int4 (weight_bits 4) or moe_pack_int8
+    (weight_bits 8) writes them; entry E is the shared expert.
     """
 
-    def __init__(self, D, I, E, K, n_shared, routed_scale, max_tokens, Wr, bias, experts, top_p=0.0):
+    def __init__(self, D, I, E, K, n_shared, routed_scale, max_tokens, Wr, bias, experts, top_p=0.0,
+                 weight_bits=4):
         self.D, self.I, self.E, self.K, self.n_shared = D, I, E, K, n_shared
         self.S = K + n_shared
         self.max_tokens = max_tokens
         self.top_p = float(top_p)
         self._keep = (Wr, bias, list(experts))
-        desc = MoeLayerDesc(D, I, E, K, n_shared, float(routed_scale), max_tokens, self.top_p)
+        self.weight_bits = int(weight_bits)
+        desc = MoeLayerDesc(D, I, E, K, n_shared, float(routed_scale), max_tokens, self.top_p, self.weight_bits)
         arr = (MoeExpertW * (E + n_shared))()
         for e, (gq, gs, uq, us, dq, ds) in enumerate(experts):
             arr[e] = MoeExpertW(_ptr(gq), _ptr(uq), _ptr(dq), _ptr(gs), _ptr(us), _ptr(ds))

@@ -302,6 +302,8 @@ __global__ void __launch_bounds__(256) grouped_gemm_kernel(LayerArgs a) {
 __global__ void __launch_bounds__(256) requant_h_kernel(LayerArgs a) {
     __shared__ int red_i[32];
     const int r = blockIdx.x;
+    // grouped rows of this batch: T*S, fewer when adaptive top-p dropped selections
+    if (r >= a.meta->ubeg[a.meta->n_union]) return;
     const int I = a.I;
     float s, inv;
     act_scale(__uint_as_float(a.hamax[r]), s, inv);

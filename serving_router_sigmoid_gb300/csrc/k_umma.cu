@@ -535,9 +535,11 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
 // The activation operand of the gate/up GEMM: grouped row r = the int8 codes
 // of its token (even/odd order kept) as f16 integers (exact).
 __global__ void __launch_bounds__(256) act_rows_f16_kernel(const int8_t *__restrict__ xq,
-                                                           const int32_t *__restrict__ rows, int S, int D,
-                                                           __half *__restrict__ xf) {
+                                                           const int32_t *__restrict__ rows, const RouteMeta *meta,
+                                                           int S, int D, __half *__restrict__ xf) {
     const int r = blockIdx.x;
+    // grouped rows of this batch: T*S, fewer when adaptive top-p dropped selections
+    if (r >= meta->ubeg[meta->n_union]) return;
     const int tok = rows[r] / S;
     const int8_t *src = xq + (size_t)tok * D;
     __half *dst = xf + (size_t)r * D;
@@ -612,7 +614,7 @@ cudaError_t umma_encode_maps(void *xf, int rows, int D, int I, UmmaMaps *maps) {
 }
 
 cudaError_t launch_act_rows_f16(const LayerArgs &a, cudaStream_t s) {
-    act_rows_f16_kernel<<<a.T * a.S, 256, 0, s>>>(a.xq, a.rows, a.S, a.D, reinterpret_cast<__half *>(a.xf));
+    act_rows_f16_kernel<<<a.T * a.S, 256, 0, s>>>(a.xq, a.rows, a.meta, a.S, a.D, reinterpret_cast<__half *>(a.xf));
     return cudaGetLastError();
 }
 

@@ -12,6 +12,7 @@ struct LayerArgs {
     int D, I, E, K, S, n_shared, T;
     float routed_scale;
     float top_p;         // adaptive expert top-p in (0, 1); other values: plain top-K
+    int wbits;           // expert weight width: 4 (packed int4 rows) or 8 (int8 rows)
     const float *x;      // [T, D] fp32 layer input (post-norm activations)
     const float *Wr;     // [E, D]
     const float *bias;   // [E]
@@ -70,6 +71,11 @@ cudaError_t launch_quant_natural(const float *x, int8_t *xq, float *sx, int T, i
                                  cudaStream_t s);
 cudaError_t launch_pack_int4(const float *w, uint8_t *q4, float *scale, int64_t O, int64_t I,
                              cudaStream_t s);
+cudaError_t launch_pack_int8(const float *w, int8_t *q8, float *scale, int64_t O, int64_t I, cudaStream_t s);
+// int8-weight experts (row-per-warp kernels; the layer's only path for them)
+cudaError_t launch_gateup8(const LayerArgs &a, int mch, int grid, cudaStream_t s);
+cudaError_t launch_down8(const LayerArgs &a, int mch, int grid, bool fused, cudaStream_t s);
+cudaError_t prepare_expert_kernels8(int D, int I, int num_sms, int grid_gu[4], int grid_dn[4]);
 // FP8 E4M3 matrix with 128 x 128 block scales -> packed int4 + row scales.
 cudaError_t launch_fp8_to_int4(const uint8_t *w8, const float *scale_inv, uint8_t *q4, float *scale, int64_t O,
                                int64_t I, cudaStream_t s);

@@ -71,6 +71,7 @@ struct Handle {
     bool single_kernel;  // decode batches run the persistent single-kernel layer
     bool tcgen05_gemm;   // larger batches run the tcgen05 expert GEMMs
     int test_wait_extra;  // MOE_OPT_DECODE_TEST_WAIT_TIMEOUT
+    int wbits;            // expert weight width: 4 or 8
     int dec_grid[moe::kSmallT + 1];  // its grid per token count (0: not available)
     int probe_which;
     cudaEvent_t probe_begin, probe_end;
@@ -154,6 +155,8 @@ int check_desc(const MoeLayerDesc *d) {
         return fail(MOE_ERR_SHAPE, "max_tokens=%d: need 1 <= max_tokens <= 2^20", d->max_tokens);
     if (!(d->routed_scale == d->routed_scale)) return fail(MOE_ERR_INVALID_ARG, "routed_scale is NaN");
     if (!(d->top_p == d->top_p)) return fail(MOE_ERR_INVALID_ARG, "top_p is NaN");
+    if (d->weight_bits != 0 && d->weight_bits != 4 && d->weight_bits != 8)
+        return fail(MOE_ERR_SHAPE, "weight_bits=%d: need 4 (or 0) or 8", d->weight_bits);
     return MOE_OK;
 }
 
@@ -190,7 +193,7 @@ cudaError_t prepare_decode(Handle *h) {
     for (int T = 1; T <= moe::kSmallT; ++T) {
         a.T = T;
         h->dec_grid[T] = 0;
-        if (T > h->d.max_tokens) continue;
+        if (T > h->d.max_tokens || h->wbits != 4) continue;  // the single kernel streams int4 rows only
         cudaError_t ce = moe::decode_grid(a, h->num_sms, &h->dec_grid[T]);
         if (ce != cudaSuccess) return ce;
     }
@@ -208,6 +211,7 @@ int run_layer(Handle *h, const float *x, int T, float *out, const float *resid, 
     a.D = h->d.D; a.I = h->d.I; a.E = h->d.E; a.K = h->d.K; a.S = h->S; a.n_shared = h->d.n_shared; a.T = T;
     a.routed_scale = h->d.routed_scale;
     a.top_p = h->d.top_p;
+    a.wbits = h->wbits;
     a.x = x; a.Wr = h->Wr; a.bias = h->bias; a.experts = h->experts;
     a.xq = h->xq; a.sx = h->sx; a.xsum = h->xsum; a.logits = h->logits; a.idx = h->idx; a.wts = h->wts;
     a.rows = h->rows; a.meta = h->meta; a.h = h->h; a.hamax = h->hamax; a.part = h->part; a.dn_cnt = h->dn_cnt;
@@ -251,8 +255,9 @@ int run_layer(Handle *h, const float *x, int T, float *out, const float *resid, 
 
     // larger batches with tile-aligned shapes: tensor-core grouped GEMMs
     // (tcgen05 with f16-exact operands; the legacy integer MMA on request)
-    const bool umma = h->tcgen05_gemm && h->maps_ok && moe::umma_supported(a.D, a.I);
-    if (!small && (umma || moe::grouped_supported(a.D, a.I))) {
+    // (int8 weights run the row-per-warp kernels at every batch size)
+    const bool umma = h->wbits == 4 && h->tcgen05_gemm && h->maps_ok && moe::umma_supported(a.D, a.I);
+    if (!small && h->wbits == 4 && (umma || moe::grouped_supported(a.D, a.I))) {
         if (umma) {
             a.xf = h->xf;
             if ((ce = moe::launch_act_rows_f16(a, s)) != cudaSuccess) return cuda_fail(ce, "operand rows launch");
@@ -336,6 +341,15 @@ int moe_fp8_block_to_int4(const uint8_t *w8, const float *scale_inv, uint8_t *q4
     return ce == cudaSuccess ? MOE_OK : cuda_fail(ce, "fp8_to_int4 launch");
 }
 
+int moe_pack_int8(const float *w, int8_t *q8, float *scale, int64_t O, int64_t I, cudaStream_t stream) {
+    if (O < 0 || I < 0) return fail(MOE_ERR_SHAPE, "O=%lld I=%lld must be >= 0", (long long)O, (long long)I);
+    if (O == 0) return MOE_OK;
+    if (I > 0 && O > ((int64_t)1 << 62) / I) return fail(MOE_ERR_SHAPE, "O*I too large");
+    if (!w || !q8 || !scale) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+    cudaError_t ce = moe::launch_pack_int8(w, q8, scale, O, I, stream);
+    return ce == cudaSuccess ? MOE_OK : cuda_fail(ce, "pack_int8 launch");
+}
+
 int moe_quant_act_int8(const float *x, int8_t *xq, float *sx, int n_tokens, int D, cudaStream_t stream) {
     if (n_tokens < 0 || D < 1) return fail(MOE_ERR_SHAPE, "n_tokens=%d D=%d", n_tokens, D);
     if (n_tokens == 0) return MOE_OK;
@@ -397,8 +411,11 @@ int moe_layer_create(const MoeLayerDesc *desc, const float *Wr, const float *bia
         return cuda_fail(ce, "device query");
     }
     h->num_sms = nsm;
-    h->stream_ok = moe::stream_supported(desc->D, desc->I);
-    if ((ce = moe::prepare_expert_kernels(desc->D, desc->I, nsm, h->grid_gu, h->grid_dn)) != cudaSuccess ||
+    h->wbits = desc->weight_bits == 8 ? 8 : 4;
+    h->stream_ok = h->wbits == 4 && moe::stream_supported(desc->D, desc->I);
+    if ((ce = h->wbits == 8 ? moe::prepare_expert_kernels8(desc->D, desc->I, nsm, h->grid_gu, h->grid_dn)
+                            : moe::prepare_expert_kernels(desc->D, desc->I, nsm, h->grid_gu, h->grid_dn)) !=
+            cudaSuccess ||
         (ce = prepare_decode(h)) != cudaSuccess) {
         delete h;
         return cuda_fail(ce, "kernel attributes");
@@ -410,7 +427,7 @@ int moe_layer_create(const MoeLayerDesc *desc, const float *Wr, const float *bia
         return fail(MOE_ERR_NOMEM, "workspace of %zu bytes: %s", h->ws_bytes, cudaGetErrorString(ce));
     }
     layout(*desc, h);
-    h->maps_ok = moe::umma_supported(desc->D, desc->I) &&
+    h->maps_ok = h->wbits == 4 && moe::umma_supported(desc->D, desc->I) &&
                  moe::umma_encode_maps(h->xf, desc->max_tokens * h->S, desc->D, desc->I, &h->maps) == cudaSuccess;
     if ((ce = cudaMalloc(&h->experts, sizeof(moe::DevExpert) * ne)) != cudaSuccess) {
         cudaGetLastError();
@@ -619,7 +636,7 @@ constexpr int kStaticPlans = 8;  // launch plans kept per device (distinct layer
 // Grids of one layer shape, as moe_layer_create computes them.
 struct StaticPlan {
     bool used;
-    int D, I, E, K, n_shared;
+    int D, I, E, K, n_shared, wbits;
     int grid_gu[4], grid_dn[4];
     int dec_grid[moe::kSmallT + 1];
 };
@@ -658,7 +675,8 @@ cudaError_t static_ready(StaticDeviceState &st, int dev) {
 cudaError_t static_plan(StaticDeviceState &st, const MoeLayerDesc &d, int dev, const StaticPlan **out) {
     for (int i = 0; i < kStaticPlans; ++i) {
         const StaticPlan &p = st.plans[i];
-        if (p.used && p.D == d.D && p.I == d.I && p.E == d.E && p.K == d.K && p.n_shared == d.n_shared) {
+        if (p.used && p.D == d.D && p.I == d.I && p.E == d.E && p.K == d.K && p.n_shared == d.n_shared &&
+            p.wbits == (d.weight_bits == 8 ? 8 : 4)) {
             *out = &p;
             return cudaSuccess;
         }
@@ -670,13 +688,15 @@ cudaError_t static_plan(StaticDeviceState &st, const MoeLayerDesc &d, int dev, c
     tmp.d.max_tokens = moe::kSmallT;  // decode grids for every decode-sized batch
     tmp.S = d.K + d.n_shared;
     tmp.num_sms = st.num_sms;
-    cudaError_t ce = moe::prepare_expert_kernels(d.D, d.I, st.num_sms, tmp.grid_gu, tmp.grid_dn);
+    tmp.wbits = d.weight_bits == 8 ? 8 : 4;
+    cudaError_t ce = tmp.wbits == 8 ? moe::prepare_expert_kernels8(d.D, d.I, st.num_sms, tmp.grid_gu, tmp.grid_dn)
+                                    : moe::prepare_expert_kernels(d.D, d.I, st.num_sms, tmp.grid_gu, tmp.grid_dn);
     if (ce == cudaSuccess) ce = prepare_decode(&tmp);
     if (ce != cudaSuccess) return ce;
     StaticPlan &p = st.plans[st.next];
     st.next = (st.next + 1) % kStaticPlans;
     p.used = true;
-    p.D = d.D; p.I = d.I; p.E = d.E; p.K = d.K; p.n_shared = d.n_shared;
+    p.D = d.D; p.I = d.I; p.E = d.E; p.K = d.K; p.n_shared = d.n_shared; p.wbits = tmp.wbits;
     std::memcpy(p.grid_gu, tmp.grid_gu, sizeof p.grid_gu);
     std::memcpy(p.grid_dn, tmp.grid_dn, sizeof p.grid_dn);
     std::memcpy(p.dec_grid, tmp.dec_grid, sizeof p.dec_grid);
@@ -737,13 +757,14 @@ extern "C" int moe_layer_forward_static(const MoeLayerDesc *desc, const float *W
     int32_t *err = h.err;
     layout(d, &h);
     h.err = err;  // the fixed error word, not the layout's
-    h.maps_ok = n_tokens > moe::kSmallT && moe::umma_supported(d.D, d.I) &&
+    h.maps_ok = h.wbits == 4 && n_tokens > moe::kSmallT && moe::umma_supported(d.D, d.I) &&
                 moe::umma_encode_maps(h.xf, n_tokens * (d.K + d.n_shared), d.D, d.I, &h.maps) == cudaSuccess;
     h.rpi_gu = kRpiGu;
     h.nb_gu = (d.I + kRpiGu - 1) / kRpiGu;
     h.rpi_dn = kRpiDn;
     h.nb_dn = (d.D + kRpiDn - 1) / kRpiDn;
-    h.stream_ok = moe::stream_supported(d.D, d.I);
+    h.wbits = d.weight_bits == 8 ? 8 : 4;
+    h.stream_ok = h.wbits == 4 && moe::stream_supported(d.D, d.I);
     h.single_kernel = true;
     h.tcgen05_gemm = true;
     // the arrival counters and routing tables must start at zero (their place

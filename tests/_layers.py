@@ -62,9 +62,12 @@ def gap_filtered_x(cfg, T, Wr_cpu, bias_cpu, stream="x", max_attempts=64, top_p=
 class LayerPair:
     """A GPU layer (library handle) and the recipe to build its oracle twin."""
 
-    def __init__(self, cfg, layer=0, max_tokens=None, wdev="cuda", x_stream="x", T=None, top_p=0.0):
+    def __init__(self, cfg, layer=0, max_tokens=None, wdev="cuda", x_stream="x", T=None, top_p=0.0,
+                 weight_bits=4):
         import serving_router_sigmoid_gb300 as moe
         self.cfg, self.layer, self.wdev, self.top_p = cfg, layer, wdev, float(top_p)
+        self.weight_bits = int(weight_bits)
+        pack = moe.pack_int4 if self.weight_bits == 4 else moe.pack_int8
         dev = torch.device("cuda")
         self.Wr = synth.router_weight(cfg, layer)
         self.bias = synth.router_bias(cfg, layer)
@@ -74,21 +77,23 @@ class LayerPair:
         for e in range(cfg.E + cfg.n_shared):
             g, u, d = synth.expert_fp32(cfg, e, layer, wdev)
             g, u, d = g.to(dev), u.to(dev), d.to(dev)
-            gq, gs = moe.pack_int4(g)
-            uq, us = moe.pack_int4(u)
-            dq, ds = moe.pack_int4(d)
+            gq, gs = pack(g)
+            uq, us = pack(u)
+            dq, ds = pack(d)
             self.gpu_experts.append((gq, gs, uq, us, dq, ds))
             del g, u, d
         torch.cuda.synchronize()
         self.Wr_d, self.bias_d = self.Wr.to(dev), self.bias.to(dev)
         self.gpu = moe.MoeLayer(cfg.D, cfg.I, cfg.E, cfg.K, cfg.n_shared, cfg.routed_scale,
-                                max_tokens or max(T, 1), self.Wr_d, self.bias_d, self.gpu_experts, self.top_p)
+                                max_tokens or max(T, 1), self.Wr_d, self.bias_d, self.gpu_experts, self.top_p,
+                                self.weight_bits)
         self._orc_cache = {}
 
     def oracle_expert(self, e):
         if e not in self._orc_cache:
             g, u, d = synth.expert_fp32(self.cfg, e, self.layer, self.wdev)
-            self._orc_cache[e] = oracle.pack_expert(g.cpu().numpy(), u.cpu().numpy(), d.cpu().numpy())
+            self._orc_cache[e] = oracle.pack_expert(g.cpu().numpy(), u.cpu().numpy(), d.cpu().numpy(),
+                                                    bits=self.weight_bits)
         return self._orc_cache[e]
 
     def oracle_layer(self, x_np):
@@ -98,7 +103,13 @@ class LayerPair:
         need = sorted(set(idx.reshape(-1).tolist()) | ({cfg.E} if cfg.n_shared else set()))
         experts = {e: self.oracle_expert(e) for e in need}
         return oracle.Layer(cfg.D, cfg.I, cfg.E, cfg.K, cfg.n_shared, cfg.routed_scale,
-                            self.Wr.numpy(), self.bias.numpy(), experts, top_p=self.top_p)
+                            self.Wr.numpy(), self.bias.numpy(), experts, top_p=self.top_p,
+                            weight_bits=self.weight_bits)
+
+    def down_codes(self, e):
+        """The oracle's down weights of expert e as integers [D, I]."""
+        px = self.oracle_expert(e)
+        return px.dq.astype(np.int64) if self.weight_bits == 8 else unpack_np(px.dq, self.cfg.I)
 
     def close(self):
         self.gpu.close()

@@ -177,7 +177,7 @@ def check_layer(pair, sample=None, x=None):
     hq_rows, dn_rows = g["hq"][tok], g["down_acc"][tok]
     for e in np.unique(eid[eid >= 0]):
         sel = eid == e
-        dq = unpack_np(pair.oracle_expert(int(e)).dq, cfg.I).astype(np.float64)
+        dq = pair.down_codes(int(e)).astype(np.float64)
         ad = hq_rows[sel].astype(np.float64) @ dq.T
         np.testing.assert_array_equal(dn_rows[sel], ad.astype(np.int64))
     r, m = assert_output_close(got[tok], ref)
