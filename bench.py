@@ -56,6 +56,7 @@ DEFAULT_WORKLOAD = "glm_moe_layer_decode_b1"
 # (HBM-bound); larger batches run the grouped GEMM (tensor-pipe bound).
 HOT_KERNEL_DECODE = "stream_kernel<0> (fused int4 gate/up, SiLU*up, max abs h)"
 HOT_KERNEL_SINGLE = "decode_layer_kernel (the whole layer as one persistent kernel)"
+HOT_KERNEL_DECODE8 = "gateup_kernel<12,1,8> (int8 gate/up rows, SiLU*up, max abs h)"
 HOT_KERNEL_PREFILL = "umma_gemm_kernel<0> (tcgen05 f16-exact gate/up GEMM, SiLU*up, max abs h)"
 # DRAM bytes (read + write) per launch of the dominant kernel from one ncu
 # capture of the current kernel source, or None.  Keyed by workload.
@@ -83,6 +84,8 @@ def parse_args():
     p.add_argument("--no-graph", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--weight-bits", type=int, choices=[4, 8], default=4,
+                   help="expert weight width (4: packed int4, the headline; 8: per-row int8)")
     p.add_argument("--top-p", type=float, default=0.0,
                    help="adaptive expert top-p in (0, 1) (0: plain top-K, the headline)")
     p.add_argument("--fp8-experts", type=int, default=64,
@@ -115,13 +118,16 @@ def max_over_ranks(value, world, device="cpu"):
     return float(t.item())
 
 
-def layer_bytes_per_expert(cfg):
+def layer_bytes_per_expert(cfg, wbits=4):
+    """Weight bytes of one expert: int4 packed (two per byte) or int8 rows, plus fp32 row scales."""
+    if wbits == 8:
+        return 2 * (cfg.I * cfg.D + cfg.I * 4) + cfg.D * cfg.I + cfg.D * 4
     import synth
     return synth.expert_bytes(cfg)
 
 
-def gateup_bytes_per_expert(cfg):
-    return 2 * (cfg.I * (cfg.D // 2) + cfg.I * 4)
+def gateup_bytes_per_expert(cfg, wbits=4):
+    return 2 * (cfg.I * (cfg.D if wbits == 8 else cfg.D // 2) + cfg.I * 4)
 
 
 class ClockSampler:
@@ -212,7 +218,7 @@ def measured_peak(kind="hbm_gbs"):
 
 # ------------------------------------------------------------ layer set-up
 
-def build_layers(cfg, n_layers, light, dev, rank_seed=0, top_p=0.0):
+def build_layers(cfg, n_layers, light, dev, rank_seed=0, top_p=0.0, wbits=4):
     """n_layers resident GLM-shaped layers, weights drawn on the GPU from the
     seeded generator and packed by the library's own int4 packer."""
     import torch
@@ -225,16 +231,17 @@ def build_layers(cfg, n_layers, light, dev, rank_seed=0, top_p=0.0):
         bias = synth.router_bias(cfg, lid).to(dev)
         phys = {}
         n_phys = 16 if light else cfg.E
+        pack = moe.pack_int8 if wbits == 8 else moe.pack_int4
         for e in list(range(n_phys)) + [cfg.E]:
             g, u, d = synth.expert_fp32(cfg, e, lid, dev)
-            gq, gs = moe.pack_int4(g)
-            uq, us = moe.pack_int4(u)
-            dq, ds = moe.pack_int4(d)
+            gq, gs = pack(g)
+            uq, us = pack(u)
+            dq, ds = pack(d)
             phys[e] = (gq, gs, uq, us, dq, ds)
             del g, u, d
         table = [phys[e if e < n_phys or e == cfg.E else e % n_phys] for e in range(cfg.E)] + [phys[cfg.E]]
         layers.append(moe.MoeLayer(cfg.D, cfg.I, cfg.E, cfg.K, cfg.n_shared, cfg.routed_scale, max(cfg.T, 1),
-                                   Wr, bias, table, top_p))
+                                   Wr, bias, table, top_p, wbits))
         keep.append((Wr, bias, phys))
     torch.cuda.synchronize()
     return layers, keep
@@ -254,7 +261,7 @@ def union_sizes(layers, xs):
 # ----------------------------------------------------------------- our arm
 
 def run_ours(args, workload, rank, world, local, n_layers=None, steps=None, warmup=None, with_e2e=True,
-             with_cpu=True, top_p=None):
+             with_cpu=True, top_p=None, wbits=None):
     """One workload on this rank's GPU; returns rank 0's JSON object (None on
     the other ranks).  The process group, if any, is already up."""
     import torch
@@ -271,7 +278,8 @@ def run_ours(args, workload, rank, world, local, n_layers=None, steps=None, warm
         n_layers = 8 if stack else max(1, args.layers)
     t_setup = time.time()
     top_p = args.top_p if top_p is None else top_p
-    layers, keep = build_layers(cfg, n_layers, args.light, dev, rank_seed=rank, top_p=top_p)
+    wbits = args.weight_bits if wbits is None else wbits
+    layers, keep = build_layers(cfg, n_layers, args.light, dev, rank_seed=rank, top_p=top_p, wbits=wbits)
     T = cfg.T
     for lyr in layers:
         if args.four_kernel:
@@ -347,7 +355,17 @@ def run_ours(args, workload, rank, world, local, n_layers=None, steps=None, warm
             step_fn(i)
         return 1
 
-    kernels_per_forward = (1 if single else 4 if T <= 16 else 7) + (1 if stack else 0)
+    # single kernel; else router + gate/up + down + reduce (int8 rows: the down
+    # kernel reduces, three); above 16 tokens quantiser, logits, select,
+    # permute, gate/up, requant, down, reduce (+ the f16 operand rows for the
+    # tcgen05 GEMMs; int8 rows: no requant and no operand rows)
+    if single:
+        kernels_per_forward = 1
+    elif T <= 16:
+        kernels_per_forward = 3 if wbits == 8 else 4
+    else:
+        kernels_per_forward = 7 if wbits == 8 else 9
+    kernels_per_forward += 1 if stack else 0
     launches_per_step = kernels_per_forward * (len(layers) if stack else 1)
     setup_s = time.time() - t_setup
 
@@ -400,8 +418,9 @@ def run_ours(args, workload, rank, world, local, n_layers=None, steps=None, warm
     # algorithmic bytes of the dominant kernel and of a whole step
     u1 = union_sizes(layers, xs if not stack else [xs[0]] * len(layers))
     u1_mean = sum(u1) / len(u1)
-    gu_bytes = u1_mean * gateup_bytes_per_expert(cfg) + T * cfg.D + T * cfg.S * cfg.I * 4
-    step_bytes_layer = u1_mean * layer_bytes_per_expert(cfg) + cfg.E * cfg.D * 4 + cfg.E * 4 + 2 * T * cfg.D * 4
+    gu_bytes = u1_mean * gateup_bytes_per_expert(cfg, wbits) + T * cfg.D + T * cfg.S * cfg.I * 4
+    step_bytes_layer = (u1_mean * layer_bytes_per_expert(cfg, wbits) + cfg.E * cfg.D * 4 + cfg.E * 4 +
+                        2 * T * cfg.D * 4)
     step_bytes = step_bytes_layer * (len(layers) if stack else 1)
     if use_probe:
         probe_avg_ms, launches_timed = sum(probe_ms) / len(probe_ms), len(probe_ms)
@@ -422,7 +441,8 @@ def run_ours(args, workload, rank, world, local, n_layers=None, steps=None, warm
     elif not grouped:
         peak, peak_kind = measured_peak("hbm_gbs")
         achieved = gu_bytes / (probe_avg_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "kernel": HOT_KERNEL_DECODE, "achieved": achieved, "peak": peak, "unit": "GB/s",
+        roof = {"bound": "hbm", "kernel": HOT_KERNEL_DECODE if wbits == 4 else HOT_KERNEL_DECODE8,
+                "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_kind": peak_kind + " HBM copy bandwidth",
                 "traffic": TRAFFIC.get(workload), "algorithmic_bytes_per_launch": gu_bytes,
                 "avg_launch_ms": probe_avg_ms, "launches_timed": launches_timed}
@@ -487,11 +507,12 @@ def run_ours(args, workload, rank, world, local, n_layers=None, steps=None, warm
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": warmup,
         "warmup_steps_run": w_done,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "int4 weights x int8 activations -> int32, fp32 scales", "data": "synthetic",
+        "dtype": f"int{wbits} weights x int8 activations -> int32, fp32 scales", "data": "synthetic",
         "config": {"workload": workload, "hidden": cfg.D, "moe_intermediate": cfg.I, "experts": cfg.E,
                    "top_k": cfg.K, "shared_experts": cfg.n_shared, "tokens_per_step": T,
                    "layers_per_step": len(layers) if stack else 1, "layer_sets_cycled": n_layers,
                    "routed_scale": cfg.routed_scale, "zipf_skew": cfg.skew, "top_p": top_p,
+                   "weight_bits": wbits,
                    "experts_streamed_per_layer": u1_mean, "cuda_graph": use_graph,
                    "steps_per_graph": n_layers if run_graph is not None else 1, "light": args.light,
                    "decode_plan": ("single persistent kernel" if single else "four kernels") if T <= 16 else None,
@@ -707,19 +728,23 @@ def secondary_lines(args, rank, world, local):
     """The other two single-layer workloads of the metric (verify batch 8 and
     prefill 2048), timed in the same process after the headline with two
     resident layer weight sets each (9.7 GB, inputs larger than L2); the
-    headline workload again with adaptive expert top-p 0.7; and the FP8 ->
-    int4 converter step."""
+    headline workload again with adaptive expert top-p 0.7 and with int8
+    experts (four resident sets, 2x the weight bytes); and the FP8 -> int4
+    converter step."""
     out = {}
-    runs = [(wl, 0.0, 2) for wl in SECONDARY] + [(DEFAULT_WORKLOAD, 0.7, 8)]
-    for wl, tp, nl in runs:
+    runs = [(wl, 0.0, 4, 2, wl) for wl in SECONDARY] + [
+        (DEFAULT_WORKLOAD, 0.7, 4, 8, DEFAULT_WORKLOAD + "_topp0.7"),
+        (DEFAULT_WORKLOAD, 0.0, 8, 4, DEFAULT_WORKLOAD + "_int8")]
+    for wl, tp, wb, nl, key in runs:
         line = run_ours(args, wl, rank, world, local, n_layers=nl, steps=max(args.steps, 10),
-                        warmup=max(3, min(args.warmup, 20)), with_cpu=False, top_p=tp)
+                        warmup=max(3, min(args.warmup, 20)), with_cpu=False, top_p=tp, wbits=wb)
         if line is None:
             continue
         sub = {k: line[k] for k in SECONDARY_KEYS}
         sub["config"] = {k: line["config"][k] for k in ("tokens_per_step", "zipf_skew", "experts_streamed_per_layer",
-                                                        "layer_sets_cycled", "l2", "cuda_graph", "top_p")}
-        out[wl if tp == 0.0 else f"{wl}_topp{tp}"] = sub
+                                                        "layer_sets_cycled", "l2", "cuda_graph", "top_p",
+                                                        "weight_bits", "decode_plan")}
+        out[key] = sub
     if rank == 0:
         out["glm_fp8_to_int4"] = run_fp8_converter(args, local)
     return out

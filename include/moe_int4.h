@@ -280,7 +280,7 @@ int moe_layer_set_probe(void *handle, int which, cudaEvent_t begin, cudaEvent_t 
  * fp32 accumulation, which is exact for these sizes; the activation tiles
  * arrive by TMA from f16 operand rows the library writes once per batch); 0:
  * on the legacy integer MMA (mma.sync s8 x u8).  Both give bit-identical
- * int32 dot products.  Needs D % 128 == 0 and I % 64 == 0. */
+ * int32 dot products.  Needs D % 256 == 0 and I % 128 == 0. */
 #define MOE_OPT_TCGEN05_GEMM 3
 /* read-only: 1 when the tcgen05 expert GEMMs can run for this handle (tile-
  * aligned sizes, max_tokens > 16, and the TMA tensor maps of their activation

@@ -14,41 +14,46 @@
 // partial sum of a row stays below 6144 * 1016 < 2^24, so fp32 accumulation
 // of these products is exact and the accumulator equals the int32 dot.
 //
-// Design (GB300).  D[weight rows x tokens] = W[rows x K] . X[tokens x K]^T:
-// the weight rows are the MMA's M side (128 per tile) and the tokens of one
-// union entry its N side (up to 128 per tile, padded to 16), so small experts
-// waste at most 15 token columns.  For gate/up the 128 rows are 64 gate rows
-// interleaved with the same 64 up rows, so one lane shuffle pairs g and u in
-// the epilogue.  K runs in stages of 64.
+// Design (GB300).  D[tokens x weight rows] = X[tokens x K] . W[rows x K]^T:
+// the tokens of one union entry are the MMA's M side (128 per tile, rows past
+// the entry's tokens computed and ignored) and 256 weight rows its N side
+// (gate/up: 128 gate rows then the same 128 up rows; down: 256 output rows).
+// On this part one M=128, K=16 tcgen05.mma costs about 125 cycles whatever its
+// N up to 256 (measured back to back from one thread), so only N = 256 runs
+// the tensor cores at their dense rate: the wide weight side goes on N.  K
+// runs in stages of 64.
 //  - The activation operand is not converted here: a small kernel before the
 //    GEMM writes every grouped row of the batch (gate/up: the token's int8
 //    codes; down: the requantised h codes) as f16 integers, once, and one
-//    producer thread moves each stage's token tile into shared memory with
-//    TMA tile loads (boxes of 32 rows x 64 f16 = 128 bytes per row, 128-byte
-//    swizzle: the K-major layout the MMA reads).  Rows past the tile's tokens
-//    belong to the next entry (or lie past the tensor and read as zeros):
-//    their accumulator columns are computed and ignored.
-//  - One CTA per SM, 26 warps: 4 epilogue warps (TMEM lanes 0..127), two
-//    groups of 8 converter warps (even and odd stages), 1 MMA warp, 4 weight
-//    load warps, 1 activation TMA warp.
-//  - The load warps copy the weight rows of 4 stages at a time into a
-//    4-slot raw ring with 16-byte cp.async (32 rows per warp, 8 lanes per
-//    128-byte row, so every warp instruction is fully coalesced); each
-//    lane's copies arrive on the slot's barrier when they land.  Converter
-//    thread c of a group owns one fixed 16-byte chunk of each of its stages,
-//    expands it to f16 (a byte permute into 0x64xx patterns and one f16x2
-//    subtraction per pair) and stores it into TMEM (the MMA's A operand); its
-//    warp then arrives on the stage's barrier.  The packed weight nibbles come
-//    out in the order e0 e2 e4 e6 e1 e3 e5 e7 of each 8-group, which is
-//    exactly the even/odd order in which the activation rows are stored, so
-//    both operands see the same permutation of K.
+//    producer thread moves each stage's 128-token tile into shared memory
+//    with TMA tile loads (boxes of 32 rows x 64 f16 = 128 bytes per row,
+//    128-byte swizzle: the K-major layout the MMA reads).
+//  - One CTA per SM, 26 warps: 4 epilogue warps (TMEM lanes 0..127 = the
+//    tile's tokens), 16 converter warps, 1 MMA warp, 4 weight load warps,
+//    1 activation TMA warp.
+//  - The load warps copy the 256 weight rows of 2 stages at a time into a
+//    3-slot raw ring with 16-byte cp.async (64 rows per warp, 4 lanes per
+//    64-byte row); each lane's copies arrive on the slot's barrier when they
+//    land.  Every stage, converter thread c expands one 16-byte chunk (one
+//    row, half of the stage's K) to f16 (a byte permute into 0x64xx patterns
+//    and one f16x2 subtraction per pair) and stores the four 16-byte results
+//    into the stage's 128-byte-swizzled K-major weight tile in shared memory
+//    (the MMA's B operand); its warp then arrives on the stage's barrier.
+//    The packed weight nibbles come out in the order e0 e2 e4 e6 e1 e3 e5 e7
+//    of each 8-group, which is exactly the even/odd order in which the
+//    activation rows are stored, so both operands see the same permutation
+//    of K.
 //  - The MMA thread waits for a stage's weights (converter barrier) and its
-//    token tile (TMA transaction barrier), issues four K=16 MMAs and commits
-//    them to the stage's "empty" barrier; after a tile's last stage to an
-//    accumulator barrier.  Two 128-column TMEM accumulators let the epilogue
-//    of one tile overlap the MMAs of the next.
-//  - Epilogue: tcgen05.ld 32 columns at a time; gate/up: h = silu(g)*u, max|h|
-//    per token row; down: y = (acc*sh)*sd into the per-slot partial rows.
+//    token tile (TMA transaction barrier), issues four M=128, N=256, K=16 MMAs
+//    (descriptors formed once per stage, +32 bytes per K=16 slice) and
+//    commits them to the stage's "empty" barrier; after a tile's last stage
+//    to an accumulator barrier.  Two 256-column TMEM accumulators (all 512
+//    columns) let the epilogue of one tile overlap the MMAs of the next.
+//  - Epilogue: thread m of the 128 holds token m's whole row of the tile:
+//    gate/up: 16 gate and the matching 16 up columns at a time,
+//    h = silu(g)*u written as contiguous 128-byte runs, max|h| of the token
+//    kept in a register; down: y = (acc*sh)*sd into the token's per-slot
+//    partial row.
 // Every barrier wait is bounded (one second of %globaltimer); a time-out sets
 // kErrSyncTimeout and an abort flag every role polls, the MMA thread drains
 // its outstanding MMAs (bounded), the copy issuers wait (bounded) for their
@@ -64,30 +69,30 @@ namespace {
 
 constexpr int kGU = 0, kDN = 1;
 constexpr int kThreads = 832;             // 26 warps
-constexpr int kConv0 = 128;               // first converter thread: two groups of 8 warps
+constexpr int kConvWarp0 = 4;             // 16 converter warps
 constexpr int kMmaWarp = 20;
 constexpr int kLoadWarp0 = 21;            // four weight load warps
 constexpr int kLoadWarps = 4;
 constexpr int kTmaWarp = 25;              // activation tiles
 constexpr int kBKs = 64;                  // K elements per stage
-constexpr int kTok = 128;                 // token columns per tile at most
+constexpr int kTok = 128;                 // token rows per tile (the MMA's M)
+constexpr int kWN = 256;                  // weight rows per tile (the MMA's N)
 constexpr int kBoxRows = 32;              // token rows per TMA box
-constexpr int kSt = 6;                    // operand stages (weights in TMEM, activations in shared memory)
-constexpr int kRA = 4;                    // weight raw ring: slots of up to 4 stages (128 bytes per row)
-constexpr uint32_t kBF16 = kTok * 128;    // 128 tokens x 64 f16
-constexpr uint32_t kARowPitch = 144;      // raw weight row pitch: 128 bytes + 16 of padding
-// raw weight row r sits at r * pitch (+64 for the second 64-row half), so the
-// 16-byte reads of 8 consecutive tile rows fall in 8 different bank groups
-__device__ __forceinline__ uint32_t raw_row_off(int r) { return (uint32_t)r * kARowPitch + (r >= 64 ? 64u : 0u); }
-constexpr uint32_t kARaw = 128 * kARowPitch + 64;  // 128 rows x up to 4 stages of 64 int4
-constexpr uint32_t kOffB = 0;
-constexpr uint32_t kOffRA = kOffB + kSt * kBF16;
-constexpr uint32_t kDyn = kOffRA + kRA * kARaw;  // 170 KB
+constexpr int kSt = 3;                    // operand stages (f16 tokens and weights, shared memory)
+constexpr int kRA = 3;                    // weight raw ring: slots of up to 2 stages (64 bytes per row)
+constexpr uint32_t kXF16 = kTok * 128;    // 128 tokens x 64 f16
+constexpr uint32_t kWF16 = kWN * 128;     // 256 weight rows x 64 f16
+constexpr uint32_t kARowPitch = 80;       // raw weight row pitch: 64 bytes + 16 of padding
+// raw weight row r sits at r * pitch (+64 for the second 128-row half), so
+// the 16-byte reads of 8 consecutive rows fall in 8 different bank groups
+__device__ __forceinline__ uint32_t raw_row_off(int r) { return (uint32_t)r * kARowPitch + (r >= 128 ? 64u : 0u); }
+constexpr uint32_t kARaw = kWN * kARowPitch + 64;  // 256 rows x 2 stages of 64 int4
+constexpr uint32_t kOffX = 0;
+constexpr uint32_t kOffW = kOffX + kSt * kXF16;
+constexpr uint32_t kOffRA = kOffW + kSt * kWF16;
+constexpr uint32_t kDyn = kOffRA + kRA * kARaw;  // 205 KB
 constexpr size_t kSmemBytes = kDyn + 1024;       // + alignment to 1024 bytes
-constexpr uint32_t kTmemCols = 512;       // accumulators [0, 256), weight stages [256, 256 + 32 kSt)
-constexpr uint32_t kTmemA = 2 * kTok;     // first weight-stage column
-constexpr uint32_t kAcolStage = 32;       // columns per weight stage: 64 f16 as 32 pairs
-static_assert(kTmemA + kSt * kAcolStage <= kTmemCols, "TMEM columns");
+constexpr uint32_t kTmemCols = 2 * kWN;          // two accumulators of 256 columns
 
 struct UmmaSmem {
     uint64_t full[kSt], bfull[kSt], empty[kSt], acc_full[2], acc_empty[2], drain;
@@ -95,10 +100,7 @@ struct UmmaSmem {
     uint32_t tmem;
     int abort;
     int tp[kMaxE + 2];        // tiles before each union entry
-    int tok_r[2][kTok];       // per accumulator: grouped row of each token column
-    int tok_e[2][kTok];       //   its entry id (token * S + slot)
-    float tok_s[2][kTok];     //   its activation scale
-    float red[4][kTok];       // max|h| per token column, per epilogue warp
+    float wsc[2][kWN];        // per accumulator: the row scales of the tile's weight rows
 };
 
 __device__ __forceinline__ uint32_t su32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -176,9 +178,13 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
     return (uint64_t)((saddr & 0x3FFFF) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
-// Instruction descriptor of kind::f16: f16 A and B, K-major, fp32 D, M = 128.
-__device__ __forceinline__ uint32_t idesc_f16(int n) {
-    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+
+// Byte offset of 16-byte chunk c (K positions 8c..8c+7) of row r in a
+// 128-byte-swizzled K-major tile (8-row atoms of 1024 bytes; the chunk index
+// is XORed with the row within the atom), the layout TMA's 128-byte swizzle
+// writes and desc_sw128 describes.
+__device__ __forceinline__ uint32_t sw_off(int r, int c) {
+    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
 __device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
@@ -203,11 +209,34 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// 16 consecutive 32-bit TMEM columns of this warp's 32 lanes (one per lane).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+          "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr));
+}
+
+// 32 consecutive 32-bit TMEM columns of this warp's 32 lanes (one per lane).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+          "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+          "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+          "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr));
+}
+
 struct Tile {
-    int u, wb, r0, nvalid, npad;
+    int u, wb, r0, nvalid;
 };
 
-__device__ __forceinline__ Tile tile_of(const LayerArgs &a, const UmmaSmem &sm, int nu, int nwb, int t) {
+// Tile t: union entry u, weight block wb (256 rows), token block (128 rows);
+// the token blocks of one weight block are consecutive.
+__device__ __forceinline__ Tile tile_of(const LayerArgs &a, const UmmaSmem &sm, int nu, int t) {
     int lo = 0, hi = nu - 1;
     while (lo < hi) {  // last entry with tp[u] <= t
         const int mid = (lo + hi + 1) >> 1;
@@ -221,7 +250,6 @@ __device__ __forceinline__ Tile tile_of(const LayerArgs &a, const UmmaSmem &sm, 
     const int tb = local - x.wb * ntb;
     x.r0 = beg + tb * kTok;
     x.nvalid = min(kTok, M - tb * kTok);
-    x.npad = (x.nvalid + 15) & ~15;
     return x;
 }
 
@@ -235,9 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
     const int b = blockIdx.x, G = gridDim.x, S = a.S;
     const int kdim = KIND == kGU ? a.D : a.I;
     const int rowb = kdim >> 1;
-    const int nwb = KIND == kGU ? a.I / 64 : a.D / 128;  // weight blocks per expert
-    const int kst = kdim / kBKs;                          // stages per tile
-    const int ch = kst % 4 == 0 ? 4 : kst % 2 == 0 ? 2 : 1;  // stages per weight copy (slot of the raw ring)
+    const int nwb = KIND == kGU ? a.I / (kWN / 2) : a.D / kWN;  // weight blocks per expert
+    const int kst = kdim / kBKs;                                // stages per tile
+    const int ch = kst % 2 == 0 ? 2 : 1;                        // stages per raw slot
     const int nu = a.meta->n_union;
     volatile int *abort = &sm.abort;
 
@@ -250,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
         sm.tp[nu] = run;
         sm.abort = 0;
         for (int s = 0; s < kSt; ++s) {
-            mb_init(&sm.full[s], 8);   // the 8 converter warps of the stage's group
+            mb_init(&sm.full[s], 16);  // the 16 converter warps
             mb_init(&sm.bfull[s], 1);  // the TMA issuer's arrival, plus the tile's bytes
             mb_init(&sm.empty[s], 1);
         }
@@ -261,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
         mb_init(&sm.drain, 1);
         for (int s = 0; s < kRA; ++s) {
             mb_init(&sm.raw_full[s], 32 * kLoadWarps);
-            mb_init(&sm.raw_empty[s], ch == 1 ? 8 : 16);  // the warps of every group that converts from the slot
+            mb_init(&sm.raw_empty[s], 16);  // the converter warps, after the slot's last stage
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -278,76 +306,67 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
     const int n_my = b < n_tiles ? (n_tiles - b + G - 1) / G : 0;
     const int n_stages = n_my * kst;
 
-    if (tid >= kConv0 && tid < kConv0 + 512) {
+    if (warp >= kConvWarp0 && warp < kConvWarp0 + 16) {
         // ------------------------------------------------------ converters
-        const int grp = (tid - kConv0) >> 8;      // this group converts stages i = grp (mod 2)
-        const int ct = (tid - kConv0) & 255;
-        // the warp writes its TMEM lane quarter (warp % 4); tile row
-        // m = 32 * quarter + lane, 16-byte half ah = converter warp / 4; raw
-        // row ra holds tile row m (gate/up rows interleave: m = 2i gate, 2i+1 up)
-        const int cw = ct >> 5, m = 32 * (warp & 3) + lane, ah = cw >> 2;
-        const int ra = KIND == kGU ? ((m & 1) * 64 + (m >> 1)) : m;
-        const int lch = ch == 4 ? 2 : ch == 2 ? 1 : 0;
-        int fs = grp, use3 = 0;  // TMEM stage slot (i % kSt) and its use (i / kSt)
-        for (int i = grp; i < n_stages; i += 2) {
-            const int q = i >> lch, within = i & (ch - 1), rs = q & (kRA - 1);
-            bool ok = true;
-            if (within < 2) ok = mb_wait(&sm.raw_full[rs], (uint32_t)((q / kRA) & 1), abort, a.err);
-            if (ok && i >= kSt) ok = mb_wait(&sm.empty[fs], (uint32_t)((use3 - 1) & 1), abort, a.err);
+        // row n = 32 * (cw % 8) + lane of the weight tile, 16-byte half
+        // hf = cw / 8 of the stage's 32 raw bytes; raw row = tile row
+        const int cw = warp - kConvWarp0, n = 32 * (cw & 7) + lane, hf = cw >> 3;
+        int fs = 0, fph = 0;  // stage slot i % kSt and its use parity
+        for (int i = 0; i < n_stages; ++i) {
+            const int q = i / ch, within = i - q * ch, rs = q % kRA;
+            bool ok = within != 0 || mb_wait(&sm.raw_full[rs], (uint32_t)((q / kRA) & 1), abort, a.err);
+            if (ok && i >= kSt) ok = mb_wait(&sm.empty[fs], (uint32_t)(fph ^ 1), abort, a.err);
             if (__any_sync(0xffffffffu, !ok)) break;  // the whole warp leaves together
-            // 4 packed words -> 16 f16 pairs of tile row m, to TMEM
-            const uint4 w = *reinterpret_cast<const uint4 *>(dyn + kOffRA + (uint32_t)rs * kARaw + raw_row_off(ra) +
-                                                             within * 32 + ah * 16);
-            if (within + 2 >= ch) {  // this group's last stage of the slot: one arrival per warp
+            const uint4 w = *reinterpret_cast<const uint4 *>(dyn + kOffRA + (uint32_t)rs * kARaw + raw_row_off(n) +
+                                                             within * 32 + hf * 16);
+            if (within == ch - 1) {  // the slot's last stage has been read
                 __syncwarp();
                 if (lane == 0) mb_arrive(&sm.raw_empty[rs]);
             }
-            const uint4 p0 = w4_to_f16(w.x), p1 = w4_to_f16(w.y), p2 = w4_to_f16(w.z), p3 = w4_to_f16(w.w);
-            const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kTmemA + (uint32_t)fs * kAcolStage +
-                                (uint32_t)ah * 16;
-            asm volatile(
-                "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(ta),
-                "r"(p0.x), "r"(p0.y), "r"(p0.z), "r"(p0.w), "r"(p1.x), "r"(p1.y), "r"(p1.z), "r"(p1.w), "r"(p2.x),
-                "r"(p2.y), "r"(p2.z), "r"(p2.w), "r"(p3.x), "r"(p3.y), "r"(p3.z), "r"(p3.w)
-                : "memory");
-            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            uint8_t *wt = dyn + kOffW + (uint32_t)fs * kWF16;
+            *reinterpret_cast<uint4 *>(wt + sw_off(n, 4 * hf + 0)) = w4_to_f16(w.x);
+            *reinterpret_cast<uint4 *>(wt + sw_off(n, 4 * hf + 1)) = w4_to_f16(w.y);
+            *reinterpret_cast<uint4 *>(wt + sw_off(n, 4 * hf + 2)) = w4_to_f16(w.z);
+            *reinterpret_cast<uint4 *>(wt + sw_off(n, 4 * hf + 3)) = w4_to_f16(w.w);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // to the MMA's proxy
             __syncwarp();
             if (lane == 0) mb_arrive(&sm.full[fs]);
-            fs += 2;
-            if (fs >= kSt) { fs -= kSt; ++use3; }
+            if (++fs == kSt) { fs = 0; fph ^= 1; }
         }
     } else if (warp == kMmaWarp) {
         // ----------------------------------------------------------- MMA
         if (lane == 0) {
+            const uint32_t idesc = (1u << 4) | ((uint32_t)(kWN >> 3) << 17) | ((uint32_t)(kTok >> 4) << 24);
+            int fs = 0, fph = 0;
             for (int ti = 0; ti < n_my && !*abort; ++ti) {
-                const Tile x = tile_of(a, sm, nu, nwb, b + ti * G);
-                const uint32_t idesc = idesc_f16(x.npad);
                 const int buf = ti & 1;
                 if (ti >= 2 && !mb_wait(&sm.acc_empty[buf], (uint32_t)(((ti >> 1) - 1) & 1), abort, a.err)) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t dt = tmem + (uint32_t)(buf * kTok);
+                const uint32_t dt = tmem + (uint32_t)(buf * kWN);
                 bool ok = true;
                 for (int ks = 0; ks < kst; ++ks) {
-                    const int i = ti * kst + ks, fs = i % kSt;
-                    const uint32_t ph = (uint32_t)((i / kSt) & 1);
-                    if (!mb_wait(&sm.full[fs], ph, abort, a.err) || !mb_wait(&sm.bfull[fs], ph, abort, a.err)) {
+                    if (!mb_wait(&sm.full[fs], (uint32_t)fph, abort, a.err) ||
+                        !mb_wait(&sm.bfull[fs], (uint32_t)fph, abort, a.err)) {
                         ok = false;
                         break;
                     }
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                    const uint32_t at = tmem + kTmemA + (uint32_t)fs * kAcolStage, b0 = sbase + kOffB + (uint32_t)fs * kBF16;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint32_t acc = (ks | kk) != 0 ? 1u : 0u;
-                        asm volatile(
-                            "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-                            " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(dt),
-                            "r"(at + kk * 8), "l"(desc_sw128(b0 + kk * 32)), "r"(idesc), "r"(acc));
-                    }
+                    const uint64_t dx = desc_sw128(sbase + kOffX + (uint32_t)fs * kXF16);
+                    const uint64_t dw = desc_sw128(sbase + kOffW + (uint32_t)fs * kWF16);
+                    const uint32_t acc = ks != 0 ? 1u : 0u;
+                    // four K=16 slices: the descriptors' start address steps 32 bytes (2 units)
+                    asm volatile(
+                        "{\n .reg .pred p, q;\n setp.ne.b32 p, %4, 0;\n setp.ne.b32 q, 1, 0;\n"
+                        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+                        " tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %6, %3, q;\n"
+                        " tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %3, q;\n"
+                        " tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %10, %3, q;\n}" ::"r"(dt),
+                        "l"(dx), "l"(dw), "r"(idesc), "r"(acc), "l"(dx + 2), "l"(dw + 2), "l"(dx + 4), "l"(dw + 4),
+                        "l"(dx + 6), "l"(dw + 6));
                     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                                      su32(&sm.empty[fs]))
                                  : "memory");
+                    if (++fs == kSt) { fs = 0; fph ^= 1; }
                 }
                 if (!ok) break;
                 asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -369,22 +388,22 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
     } else if (warp == kTmaWarp) {
         // -------------------------------------------- activation tiles (TMA)
         if (lane == 0) {
-            int issued = 0, t_ti = -1, nbox = 0, r0 = 0;
+            int issued = 0, t_ti = -1, r0 = 0, fs = 0, fph = 0;
             for (int i = 0; i < n_stages && !*abort; ++i) {
-                const int ti = i / kst, ks = i - ti * kst, fs = i % kSt;
+                const int ti = i / kst, ks = i - ti * kst;
                 if (ti != t_ti) {
                     t_ti = ti;
-                    const Tile x = tile_of(a, sm, nu, nwb, b + ti * G);
-                    nbox = (x.npad + kBoxRows - 1) / kBoxRows;
-                    r0 = x.r0;
+                    r0 = tile_of(a, sm, nu, b + ti * G).r0;
                 }
                 // the slot is free once the MMAs that read it have completed
-                if (i >= kSt && !mb_wait(&sm.empty[fs], (uint32_t)(((i / kSt) - 1) & 1), abort, a.err)) break;
-                mb_expect_tx(&sm.bfull[fs], (uint32_t)nbox * kBoxRows * 128u);
-                const uint32_t dst = sbase + kOffB + (uint32_t)fs * kBF16;
-                for (int bx = 0; bx < nbox; ++bx)
+                if (i >= kSt && !mb_wait(&sm.empty[fs], (uint32_t)(fph ^ 1), abort, a.err)) break;
+                mb_expect_tx(&sm.bfull[fs], kXF16);
+                const uint32_t dst = sbase + kOffX + (uint32_t)fs * kXF16;
+#pragma unroll
+                for (int bx = 0; bx < kTok / kBoxRows; ++bx)
                     tma_load_2d(dst + (uint32_t)bx * kBoxRows * 128u, &xmap, ks * kBKs, r0 + kBoxRows * bx, &sm.bfull[fs]);
                 issued = i + 1;
+                if (++fs == kSt) { fs = 0; fph ^= 1; }
             }
             // tiles still in flight land before the CTA may leave (bounded)
             const unsigned long long t0 = global_ns();
@@ -398,37 +417,36 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
         __syncwarp();
     } else if (warp >= kLoadWarp0 && warp < kLoadWarp0 + kLoadWarps) {
         // ------------------------------------------------------ weight loads
-        // slot q of the raw ring: 128 weight rows x ch stages (ch * 32 bytes
+        // slot q of the raw ring: 256 weight rows x ch stages (ch * 32 bytes
         // per row), kRA slots ahead of the converters; load warp w copies rows
-        // 32w .. 32w+31, lane l the 16-byte pieces l, l + 32, ... of them
-        // (row = piece / 8, column piece % 8)
+        // 64w .. 64w+63, lane l the 16-byte pieces l, l + 32, ... of them
+        // (row = piece / 4, column piece % 4)
         const int lw = warp - kLoadWarp0;
-        const int n_q = n_stages / ch;
+        const int n_q = (n_stages + ch - 1) / ch;
         int l_ti = -1, issued = 0;
-        const uint8_t *r0p = nullptr, *r1p = nullptr;  // first rows of the two 64-row halves
+        const uint8_t *r0p = nullptr, *r1p = nullptr;  // first rows of the two 128-row halves
         for (int q = 0; q < n_q; ++q) {
             const int rs = q % kRA;
             if (q >= kRA && !mb_wait(&sm.raw_empty[rs], (uint32_t)(((q / kRA) - 1) & 1), abort, a.err)) break;
             const int i0 = q * ch, ti = i0 / kst, ks0 = i0 - ti * kst;
             if (ti != l_ti) {
                 l_ti = ti;
-                const Tile x = tile_of(a, sm, nu, nwb, b + ti * G);
+                const Tile x = tile_of(a, sm, nu, b + ti * G);
                 const DevExpert ex = a.experts[a.meta->uexp[x.u]];
                 if (KIND == kGU) {
-                    r0p = ex.gq + (size_t)(x.wb * 64) * rowb;
-                    r1p = ex.uq + (size_t)(x.wb * 64) * rowb;
+                    r0p = ex.gq + (size_t)(x.wb * 128) * rowb;
+                    r1p = ex.uq + (size_t)(x.wb * 128) * rowb;
                 } else {
-                    r0p = ex.dq + (size_t)(x.wb * 128) * rowb;
-                    r1p = r0p + (size_t)64 * rowb;
+                    r0p = ex.dq + (size_t)(x.wb * 256) * rowb;
+                    r1p = r0p + (size_t)128 * rowb;
                 }
             }
             const uint32_t dst = sbase + kOffRA + (uint32_t)rs * kARaw;
-            const int pcs = 2 * ch;  // 16-byte pieces per row in this slot
 #pragma unroll
-            for (int p = lane; p < 32 * 8; p += 32) {
-                const int row = 32 * lw + (p >> 3), col = p & 7;
-                if (col < pcs) {
-                    const uint8_t *src = (row < 64 ? r0p + (size_t)row * rowb : r1p + (size_t)(row - 64) * rowb) +
+            for (int p = lane; p < 64 * 4; p += 32) {
+                const int row = 64 * lw + (p >> 2), col = p & 3;
+                if (col < 2 * ch) {
+                    const uint8_t *src = (row < 128 ? r0p + (size_t)row * rowb : r1p + (size_t)(row - 128) * rowb) +
                                          ks0 * 32 + col * 16;
                     cp_async16(dst + raw_row_off(row) + col * 16, src, 16u);
                 }
@@ -446,82 +464,73 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
                 }
     } else if (warp < 4) {
         // ------------------------------------------------------ epilogue
+        // thread m = token row m of the tile (TMEM lane m)
+        const int m = tid;
         for (int ti = 0; ti < n_my; ++ti) {
-            const Tile x = tile_of(a, sm, nu, nwb, b + ti * G);
+            const Tile x = tile_of(a, sm, nu, b + ti * G);
             const int buf = ti & 1;
             const DevExpert ex = a.experts[a.meta->uexp[x.u]];
-            if (tid < x.nvalid) {
-                const int r = x.r0 + tid, e = a.rows[r];
-                sm.tok_r[buf][tid] = r;
-                sm.tok_e[buf][tid] = e;
-                sm.tok_s[buf][tid] = KIND == kGU ? a.sx[e / S] : a.shq[r];
-            }
-            if (epi_bar_or(*abort != 0)) break;
+            // the tile's 256 weight-row scales (gate/up: gate then up)
+            for (int j = tid; j < kWN; j += 128)
+                sm.wsc[buf][j] = KIND == kGU ? __ldg((j < 128 ? ex.gs : ex.us) + x.wb * 128 + (j & 127))
+                                             : __ldg(ex.ds + x.wb * 256 + j);
+            const bool valid = m < x.nvalid;
+            const int r = x.r0 + m;
+            const int e = valid ? a.rows[r] : 0;
+            const float ts = valid ? (KIND == kGU ? a.sx[e / S] : a.shq[r]) : 0.f;
+            if (epi_bar_or(*abort != 0)) break;  // also orders the scale stores before their reads
             const bool got = mb_wait(&sm.acc_full[buf], (uint32_t)((ti >> 1) & 1), abort, a.err);
             if (epi_bar_or(!got)) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * kTok);
-            int o;
-            float s_a = 0.f, s_b = 0.f;
+            const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * kWN);
+            float hmax = 0.f;
             if (KIND == kGU) {
-                o = x.wb * 64 + warp * 16 + (lane >> 1);
-                s_a = __ldg(ex.gs + o);
-                s_b = __ldg(ex.us + o);
-            } else {
-                o = x.wb * 128 + warp * 32 + lane;
-                s_a = __ldg(ex.ds + o);
-            }
-            for (int c0 = 0; c0 < x.npad; c0 += 32) {
-                uint32_t v[32];
-                asm volatile(
-                    "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-                    "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-                    : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-                      "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
-                      "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
-                      "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
-                      "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-                    : "r"(ta + (uint32_t)c0));
-                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                // 16 gate columns and the matching 16 up columns at a time
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t v[16], u[16];
+                    tmem_ld16(ta + (uint32_t)(16 * c), v);
+                    tmem_ld16(ta + (uint32_t)(128 + 16 * c), u);
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                    if (!valid) continue;
+                    const int o0 = x.wb * 128 + 16 * c;
+                    float hv[16];
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int j = c0 + jj;
-                    const float acc = __uint_as_float(v[jj]);
-                    if (KIND == kGU) {
-                        const float up = __shfl_xor_sync(0xffffffffu, acc, 1);
-                        float hv = 0.f;
-                        if (j < x.nvalid && (lane & 1) == 0) {
-                            const int gi = __float2int_rn(acc), ui = __float2int_rn(up);
-                            const float sx = sm.tok_s[buf][j];
-                            const float gf = __fmul_rn(__fmul_rn((float)gi, sx), s_a);
-                            const float uf = __fmul_rn(__fmul_rn((float)ui, sx), s_b);
-                            hv = __fmul_rn(silu_f(gf), uf);
-                            a.h[(size_t)sm.tok_r[buf][j] * a.I + o] = hv;
-                            if (a.dbg.gate_acc) a.dbg.gate_acc[(size_t)sm.tok_e[buf][j] * a.I + o] = gi;
-                            if (a.dbg.up_acc) a.dbg.up_acc[(size_t)sm.tok_e[buf][j] * a.I + o] = ui;
-                        }
-                        float mx = fabsf(hv);
-#pragma unroll
-                        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                        if (lane == 0 && j < kTok) sm.red[warp][j] = mx;
-                    } else if (j < x.nvalid) {
-                        const int di = __float2int_rn(acc);
-                        const float y = __fmul_rn(__fmul_rn((float)di, sm.tok_s[buf][j]), s_a);
-                        a.part[(size_t)sm.tok_e[buf][j] * a.D + o] = y;
-                        if (a.dbg.down_acc) a.dbg.down_acc[(size_t)sm.tok_e[buf][j] * a.D + o] = di;
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int gi = __float2int_rn(__uint_as_float(v[jj])), ui = __float2int_rn(__uint_as_float(u[jj]));
+                        const float gf = __fmul_rn(__fmul_rn((float)gi, ts), sm.wsc[buf][16 * c + jj]);
+                        const float uf = __fmul_rn(__fmul_rn((float)ui, ts), sm.wsc[buf][128 + 16 * c + jj]);
+                        hv[jj] = __fmul_rn(silu_f(gf), uf);
+                        hmax = fmaxf(hmax, fabsf(hv[jj]));
+                        if (a.dbg.gate_acc) a.dbg.gate_acc[(size_t)e * a.I + o0 + jj] = gi;
+                        if (a.dbg.up_acc) a.dbg.up_acc[(size_t)e * a.I + o0 + jj] = ui;
                     }
+                    float4 *hp = reinterpret_cast<float4 *>(a.h + (size_t)r * a.I + o0);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) hp[q] = make_float4(hv[4 * q], hv[4 * q + 1], hv[4 * q + 2], hv[4 * q + 3]);
+                }
+            } else {
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(ta + (uint32_t)(32 * c), v);
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                    if (!valid) continue;
+                    const int o0 = x.wb * 256 + 32 * c;
+                    float yv[32];
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) {
+                        const int di = __float2int_rn(__uint_as_float(v[jj]));
+                        yv[jj] = __fmul_rn(__fmul_rn((float)di, ts), sm.wsc[buf][32 * c + jj]);
+                        if (a.dbg.down_acc) a.dbg.down_acc[(size_t)e * a.D + o0 + jj] = di;
+                    }
+                    float4 *yp = reinterpret_cast<float4 *>(a.part + (size_t)e * a.D + o0);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) yp[q] = make_float4(yv[4 * q], yv[4 * q + 1], yv[4 * q + 2], yv[4 * q + 3]);
                 }
             }
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
             if (lane == 0) mb_arrive(&sm.acc_empty[buf]);
-            if (KIND == kGU) {
-                asm volatile("bar.sync 1, 128;" ::: "memory");
-                if (tid < x.nvalid) {
-                    const float m = fmaxf(fmaxf(sm.red[0][tid], sm.red[1][tid]), fmaxf(sm.red[2][tid], sm.red[3][tid]));
-                    atomicMax(a.hamax + x.r0 + tid, __float_as_uint(m));
-                }
-            }
+            if (KIND == kGU && valid) atomicMax(a.hamax + r, __float_as_uint(hmax));
         }
     }
 
@@ -604,7 +613,8 @@ cudaError_t encode_rows_f16(void *base, int rows, int cols, CUtensorMap *map) {
 
 }  // namespace
 
-bool umma_supported(int D, int I) { return D % 128 == 0 && I % 64 == 0 && D <= kMaxDim && I <= kMaxDim; }
+// gate/up tiles take 128 gate and 128 up rows, down tiles 256 output rows
+bool umma_supported(int D, int I) { return D % 256 == 0 && I % 128 == 0 && D <= kMaxDim && I <= kMaxDim; }
 
 cudaError_t umma_encode_maps(void *xf, int rows, int D, int I, UmmaMaps *maps) {
     if ((reinterpret_cast<uintptr_t>(xf) & 15u) || rows < 1) return cudaErrorInvalidValue;

@@ -24,7 +24,7 @@ CASES = [
     dict(D=256, I=128, E=16, K=2, n_shared=1, T=17),
     dict(D=256, I=128, E=16, K=2, n_shared=1, T=64),
     dict(D=512, I=256, E=8, K=2, n_shared=1, T=300),   # 2-3 token blocks per expert
-    dict(D=768, I=192, E=32, K=6, n_shared=0, T=129),  # ragged token blocks, no shared expert
+    dict(D=768, I=384, E=32, K=6, n_shared=0, T=129),  # ragged token blocks, no shared expert
 ]
 
 
