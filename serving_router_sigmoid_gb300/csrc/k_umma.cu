@@ -28,15 +28,14 @@
 //    producer thread moves each stage's 128-token tile into shared memory
 //    with TMA tile loads (boxes of 32 rows x 64 f16 = 128 bytes per row,
 //    128-byte swizzle: the K-major layout the MMA reads).
-//  - One CTA per SM, 26 warps: 4 epilogue warps (TMEM lanes 0..127 = the
-//    tile's tokens), 16 converter warps, 1 MMA warp, 4 weight load warps,
-//    1 activation TMA warp.
-//  - The load warps copy the 256 weight rows of 2 stages at a time into a
-//    3-slot raw ring with 16-byte cp.async (64 rows per warp, 4 lanes per
-//    64-byte row); each lane's copies arrive on the slot's barrier when they
-//    land.  Every stage, converter thread c expands one 16-byte chunk (one
-//    row, half of the stage's K) to f16 (a byte permute into 0x64xx patterns
-//    and one f16x2 subtraction per pair) and stores the four 16-byte results
+//  - One CTA per SM, 22 warps: 4 epilogue warps (TMEM lanes 0..127 = the
+//    tile's tokens), 16 converter warps, 1 MMA warp, 1 activation TMA warp.
+//  - Converter thread c owns one 16-byte half of one weight row of every
+//    stage (a warp: 16 rows x 32 bytes, whole 32-byte sectors).  It loads
+//    its packed bytes straight from global memory into registers, kPD
+//    stages ahead and across tile boundaries, then, once the stage's slot
+//    is free, expands them to f16 (a byte permute into 0x64xx patterns and
+//    one f16x2 subtraction per pair) and stores the four 16-byte results
 //    into the stage's 128-byte-swizzled K-major weight tile in shared memory
 //    (the MMA's B operand); its warp then arrives on the stage's barrier.
 //    The packed weight nibbles come out in the order e0 e2 e4 e6 e1 e3 e5 e7
@@ -46,9 +45,15 @@
 //  - The MMA thread waits for a stage's weights (converter barrier) and its
 //    token tile (TMA transaction barrier), issues four M=128, N=256, K=16 MMAs
 //    (descriptors formed once per stage, +32 bytes per K=16 slice) and
-//    commits them to the stage's "empty" barrier; after a tile's last stage
-//    to an accumulator barrier.  Two 256-column TMEM accumulators (all 512
-//    columns) let the epilogue of one tile overlap the MMAs of the next.
+//    commits them to the "empty" barriers of the stage's weight slot (3
+//    slots) and token slot (5 slots: the TMA loads are the slower ones);
+//    after a tile's last stage to an accumulator barrier.  Two 256-column
+//    TMEM accumulators (all 512 columns) let the epilogue of one tile
+//    overlap the MMAs of the next.
+//  - Shared memory stays at 176 KB (+ 4 KB of barriers and scales): at most
+//    196 KB per CTA leaves the L1 a 60 KB share of the SM's 256 KB, and the
+//    weight loads in flight need it (the same kernel with 32 KB more shared
+//    memory, unused, ran 1.2x slower).
 //  - Epilogue: thread m of the 128 holds token m's whole row of the tile:
 //    gate/up: 16 gate and the matching 16 up columns at a time,
 //    h = silu(g)*u written as contiguous 128-byte runs, max|h| of the token
@@ -68,40 +73,34 @@ namespace moe {
 namespace {
 
 constexpr int kGU = 0, kDN = 1;
-constexpr int kThreads = 832;             // 26 warps
+constexpr int kThreads = 704;             // 22 warps
 constexpr int kConvWarp0 = 4;             // 16 converter warps
 constexpr int kMmaWarp = 20;
-constexpr int kLoadWarp0 = 21;            // four weight load warps
-constexpr int kLoadWarps = 4;
-constexpr int kTmaWarp = 25;              // activation tiles
+constexpr int kTmaWarp = 21;              // activation tiles
 constexpr int kBKs = 64;                  // K elements per stage
 constexpr int kTok = 128;                 // token rows per tile (the MMA's M)
 constexpr int kWN = 256;                  // weight rows per tile (the MMA's N)
 constexpr int kBoxRows = 32;              // token rows per TMA box
-constexpr int kSt = 3;                    // operand stages (f16 tokens and weights, shared memory)
-constexpr int kRA = 3;                    // weight raw ring: slots of up to 2 stages (64 bytes per row)
+constexpr int kStW = 3;                   // f16 weight tile stages (converted, shared memory)
+constexpr int kStX = 5;                   // f16 token tile stages (TMA, shared memory)
+constexpr int kPD = 4;                    // weight stages each converter thread has in flight (registers)
 constexpr uint32_t kXF16 = kTok * 128;    // 128 tokens x 64 f16
 constexpr uint32_t kWF16 = kWN * 128;     // 256 weight rows x 64 f16
-constexpr uint32_t kARowPitch = 80;       // raw weight row pitch: 64 bytes + 16 of padding
-// raw weight row r sits at r * pitch (+64 for the second 128-row half), so
-// the 16-byte reads of 8 consecutive rows fall in 8 different bank groups
-__device__ __forceinline__ uint32_t raw_row_off(int r) { return (uint32_t)r * kARowPitch + (r >= 128 ? 64u : 0u); }
-constexpr uint32_t kARaw = kWN * kARowPitch + 64;  // 256 rows x 2 stages of 64 int4
 constexpr uint32_t kOffX = 0;
-constexpr uint32_t kOffW = kOffX + kSt * kXF16;
-constexpr uint32_t kOffRA = kOffW + kSt * kWF16;
-constexpr uint32_t kDyn = kOffRA + kRA * kARaw;  // 205 KB
+constexpr uint32_t kOffW = kOffX + kStX * kXF16;
+constexpr uint32_t kDyn = kOffW + kStW * kWF16;
 constexpr size_t kSmemBytes = kDyn + 1024;       // + alignment to 1024 bytes
 constexpr uint32_t kTmemCols = 2 * kWN;          // two accumulators of 256 columns
 
 struct UmmaSmem {
-    uint64_t full[kSt], bfull[kSt], empty[kSt], acc_full[2], acc_empty[2], drain;
-    uint64_t raw_full[kRA], raw_empty[kRA];
+    uint64_t full[kStW], empty_w[kStW], bfull[kStX], empty_x[kStX], acc_full[2], acc_empty[2], drain;
     uint32_t tmem;
     int abort;
     int tp[kMaxE + 2];        // tiles before each union entry
     float wsc[2][kWN];        // per accumulator: the row scales of the tile's weight rows
 };
+
+static_assert(kSmemBytes + sizeof(UmmaSmem) <= 196 * 1024, "keep the L1 share the weight loads need");
 
 __device__ __forceinline__ uint32_t su32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -161,14 +160,14 @@ __device__ __forceinline__ bool epi_bar_or(bool p) {
 __device__ __forceinline__ void mb_expect_tx(uint64_t *b, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
 }
-// The barrier receives one arrival once every cp.async this thread issued
-// before has landed (noinc: the arrival counts toward the initial count).
-__device__ __forceinline__ void cp_async_arrive(uint64_t *b) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(su32(b)) : "memory");
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+// 16 bytes of packed weights straight into registers (read once per CTA:
+// no L1 allocation).
+__device__ __forceinline__ uint4 ld_weights16(const uint8_t *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
 }
 
 // tcgen05 shared-memory descriptor: K-major, 128-byte swizzle, 8-row atoms
@@ -265,7 +264,6 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
     const int rowb = kdim >> 1;
     const int nwb = KIND == kGU ? a.I / (kWN / 2) : a.D / kWN;  // weight blocks per expert
     const int kst = kdim / kBKs;                                // stages per tile
-    const int ch = kst % 2 == 0 ? 2 : 1;                        // stages per raw slot
     const int nu = a.meta->n_union;
     volatile int *abort = &sm.abort;
 
@@ -277,20 +275,19 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
         }
         sm.tp[nu] = run;
         sm.abort = 0;
-        for (int s = 0; s < kSt; ++s) {
+        for (int s = 0; s < kStW; ++s) {
             mb_init(&sm.full[s], 16);  // the 16 converter warps
+            mb_init(&sm.empty_w[s], 1);
+        }
+        for (int s = 0; s < kStX; ++s) {
             mb_init(&sm.bfull[s], 1);  // the TMA issuer's arrival, plus the tile's bytes
-            mb_init(&sm.empty[s], 1);
+            mb_init(&sm.empty_x[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
             mb_init(&sm.acc_full[s], 1);
             mb_init(&sm.acc_empty[s], 4);
         }
         mb_init(&sm.drain, 1);
-        for (int s = 0; s < kRA; ++s) {
-            mb_init(&sm.raw_full[s], 32 * kLoadWarps);
-            mb_init(&sm.raw_empty[s], 16);  // the converter warps, after the slot's last stage
-        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == kMmaWarp) {
@@ -308,36 +305,61 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
 
     if (warp >= kConvWarp0 && warp < kConvWarp0 + 16) {
         // ------------------------------------------------------ converters
-        // row n = 32 * (cw % 8) + lane of the weight tile, 16-byte half
-        // hf = cw / 8 of the stage's 32 raw bytes; raw row = tile row
-        const int cw = warp - kConvWarp0, n = 32 * (cw & 7) + lane, hf = cw >> 3;
-        int fs = 0, fph = 0;  // stage slot i % kSt and its use parity
-        for (int i = 0; i < n_stages; ++i) {
-            const int q = i / ch, within = i - q * ch, rs = q % kRA;
-            bool ok = within != 0 || mb_wait(&sm.raw_full[rs], (uint32_t)((q / kRA) & 1), abort, a.err);
-            if (ok && i >= kSt) ok = mb_wait(&sm.empty[fs], (uint32_t)(fph ^ 1), abort, a.err);
-            if (__any_sync(0xffffffffu, !ok)) break;  // the whole warp leaves together
-            const uint4 w = *reinterpret_cast<const uint4 *>(dyn + kOffRA + (uint32_t)rs * kARaw + raw_row_off(n) +
-                                                             within * 32 + hf * 16);
-            if (within == ch - 1) {  // the slot's last stage has been read
-                __syncwarp();
-                if (lane == 0) mb_arrive(&sm.raw_empty[rs]);
+        // thread: weight row n = 16 * cw + lane / 2 of the tile (a warp reads
+        // 16 whole 32-byte row pieces per stage), 16-byte half hf = lane % 2
+        // of the stage's 32 packed bytes; the loads run kPD stages ahead in
+        // registers, across tile boundaries
+        const int cw = warp - kConvWarp0, n = 16 * cw + (lane >> 1), hf = lane & 1;
+        int l_i = 0, l_ti = 0, l_ks = 0;  // the next stage to load and its tile / K stage
+        const uint8_t *src = nullptr;     // this thread's row piece in the tile l_ti
+        auto load_next = [&](uint4 &dst) {
+            if (l_i >= n_stages) return;
+            if (l_ks == 0) {
+                const Tile x = tile_of(a, sm, nu, b + l_ti * G);
+                const DevExpert ex = a.experts[a.meta->uexp[x.u]];
+                if (KIND == kGU)
+                    src = n < 128 ? ex.gq + (size_t)(x.wb * 128 + n) * rowb : ex.uq + (size_t)(x.wb * 128 + n - 128) * rowb;
+                else
+                    src = ex.dq + (size_t)(x.wb * 256 + n) * rowb;
+                src += hf * 16;
             }
-            uint8_t *wt = dyn + kOffW + (uint32_t)fs * kWF16;
-            *reinterpret_cast<uint4 *>(wt + sw_off(n, 4 * hf + 0)) = w4_to_f16(w.x);
-            *reinterpret_cast<uint4 *>(wt + sw_off(n, 4 * hf + 1)) = w4_to_f16(w.y);
-            *reinterpret_cast<uint4 *>(wt + sw_off(n, 4 * hf + 2)) = w4_to_f16(w.z);
-            *reinterpret_cast<uint4 *>(wt + sw_off(n, 4 * hf + 3)) = w4_to_f16(w.w);
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // to the MMA's proxy
-            __syncwarp();
-            if (lane == 0) mb_arrive(&sm.full[fs]);
-            if (++fs == kSt) { fs = 0; fph ^= 1; }
+            dst = ld_weights16(src + l_ks * 32);
+            ++l_i;
+            if (++l_ks == kst) { l_ks = 0; ++l_ti; }
+        };
+        uint4 pre[kPD];
+#pragma unroll
+        for (int k = 0; k < kPD; ++k) load_next(pre[k]);
+        int fs = 0, fph = 0;  // stage slot i % kStW and its use parity
+        bool run = true;
+        for (int i0 = 0; i0 < n_stages && run; i0 += kPD) {
+#pragma unroll
+            for (int k = 0; k < kPD; ++k) {
+                const int i = i0 + k;
+                if (i >= n_stages) break;
+                const uint4 w = pre[k];
+                load_next(pre[k]);
+                const bool ok = i < kStW || mb_wait(&sm.empty_w[fs], (uint32_t)(fph ^ 1), abort, a.err);
+                if (__any_sync(0xffffffffu, !ok)) {  // the whole warp leaves together
+                    run = false;
+                    break;
+                }
+                uint8_t *wt = dyn + kOffW + (uint32_t)fs * kWF16;
+                *reinterpret_cast<uint4 *>(wt + sw_off(n, 4 * hf + 0)) = w4_to_f16(w.x);
+                *reinterpret_cast<uint4 *>(wt + sw_off(n, 4 * hf + 1)) = w4_to_f16(w.y);
+                *reinterpret_cast<uint4 *>(wt + sw_off(n, 4 * hf + 2)) = w4_to_f16(w.z);
+                *reinterpret_cast<uint4 *>(wt + sw_off(n, 4 * hf + 3)) = w4_to_f16(w.w);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // to the MMA's proxy
+                __syncwarp();
+                if (lane == 0) mb_arrive(&sm.full[fs]);
+                if (++fs == kStW) { fs = 0; fph ^= 1; }
+            }
         }
     } else if (warp == kMmaWarp) {
         // ----------------------------------------------------------- MMA
         if (lane == 0) {
             const uint32_t idesc = (1u << 4) | ((uint32_t)(kWN >> 3) << 17) | ((uint32_t)(kTok >> 4) << 24);
-            int fs = 0, fph = 0;
+            int fs = 0, fph = 0, xs = 0, xph = 0;  // weight and token stage slots, use parities
             for (int ti = 0; ti < n_my && !*abort; ++ti) {
                 const int buf = ti & 1;
                 if (ti >= 2 && !mb_wait(&sm.acc_empty[buf], (uint32_t)(((ti >> 1) - 1) & 1), abort, a.err)) break;
@@ -346,12 +368,12 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
                 bool ok = true;
                 for (int ks = 0; ks < kst; ++ks) {
                     if (!mb_wait(&sm.full[fs], (uint32_t)fph, abort, a.err) ||
-                        !mb_wait(&sm.bfull[fs], (uint32_t)fph, abort, a.err)) {
+                        !mb_wait(&sm.bfull[xs], (uint32_t)xph, abort, a.err)) {
                         ok = false;
                         break;
                     }
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                    const uint64_t dx = desc_sw128(sbase + kOffX + (uint32_t)fs * kXF16);
+                    const uint64_t dx = desc_sw128(sbase + kOffX + (uint32_t)xs * kXF16);
                     const uint64_t dw = desc_sw128(sbase + kOffW + (uint32_t)fs * kWF16);
                     const uint32_t acc = ks != 0 ? 1u : 0u;
                     // four K=16 slices: the descriptors' start address steps 32 bytes (2 units)
@@ -364,9 +386,13 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
                         "l"(dx), "l"(dw), "r"(idesc), "r"(acc), "l"(dx + 2), "l"(dw + 2), "l"(dx + 4), "l"(dw + 4),
                         "l"(dx + 6), "l"(dw + 6));
                     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                                     su32(&sm.empty[fs]))
+                                     su32(&sm.empty_w[fs]))
                                  : "memory");
-                    if (++fs == kSt) { fs = 0; fph ^= 1; }
+                    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                                     su32(&sm.empty_x[xs]))
+                                 : "memory");
+                    if (++fs == kStW) { fs = 0; fph ^= 1; }
+                    if (++xs == kStX) { xs = 0; xph ^= 1; }
                 }
                 if (!ok) break;
                 asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -396,72 +422,25 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
                     r0 = tile_of(a, sm, nu, b + ti * G).r0;
                 }
                 // the slot is free once the MMAs that read it have completed
-                if (i >= kSt && !mb_wait(&sm.empty[fs], (uint32_t)(fph ^ 1), abort, a.err)) break;
+                if (i >= kStX && !mb_wait(&sm.empty_x[fs], (uint32_t)(fph ^ 1), abort, a.err)) break;
                 mb_expect_tx(&sm.bfull[fs], kXF16);
                 const uint32_t dst = sbase + kOffX + (uint32_t)fs * kXF16;
 #pragma unroll
                 for (int bx = 0; bx < kTok / kBoxRows; ++bx)
                     tma_load_2d(dst + (uint32_t)bx * kBoxRows * 128u, &xmap, ks * kBKs, r0 + kBoxRows * bx, &sm.bfull[fs]);
                 issued = i + 1;
-                if (++fs == kSt) { fs = 0; fph ^= 1; }
+                if (++fs == kStX) { fs = 0; fph ^= 1; }
             }
             // tiles still in flight land before the CTA may leave (bounded)
             const unsigned long long t0 = global_ns();
-            for (int i = issued - kSt < 0 ? 0 : issued - kSt; i < issued; ++i)
-                while (!mb_try(&sm.bfull[i % kSt], (uint32_t)((i / kSt) & 1)))
+            for (int i = issued - kStX < 0 ? 0 : issued - kStX; i < issued; ++i)
+                while (!mb_try(&sm.bfull[i % kStX], (uint32_t)((i / kStX) & 1)))
                     if (global_ns() - t0 > kWaitNs) {
                         atomicOr(a.err, kErrSyncTimeout);
                         break;
                     }
         }
         __syncwarp();
-    } else if (warp >= kLoadWarp0 && warp < kLoadWarp0 + kLoadWarps) {
-        // ------------------------------------------------------ weight loads
-        // slot q of the raw ring: 256 weight rows x ch stages (ch * 32 bytes
-        // per row), kRA slots ahead of the converters; load warp w copies rows
-        // 64w .. 64w+63, lane l the 16-byte pieces l, l + 32, ... of them
-        // (row = piece / 4, column piece % 4)
-        const int lw = warp - kLoadWarp0;
-        const int n_q = (n_stages + ch - 1) / ch;
-        int l_ti = -1, issued = 0;
-        const uint8_t *r0p = nullptr, *r1p = nullptr;  // first rows of the two 128-row halves
-        for (int q = 0; q < n_q; ++q) {
-            const int rs = q % kRA;
-            if (q >= kRA && !mb_wait(&sm.raw_empty[rs], (uint32_t)(((q / kRA) - 1) & 1), abort, a.err)) break;
-            const int i0 = q * ch, ti = i0 / kst, ks0 = i0 - ti * kst;
-            if (ti != l_ti) {
-                l_ti = ti;
-                const Tile x = tile_of(a, sm, nu, b + ti * G);
-                const DevExpert ex = a.experts[a.meta->uexp[x.u]];
-                if (KIND == kGU) {
-                    r0p = ex.gq + (size_t)(x.wb * 128) * rowb;
-                    r1p = ex.uq + (size_t)(x.wb * 128) * rowb;
-                } else {
-                    r0p = ex.dq + (size_t)(x.wb * 256) * rowb;
-                    r1p = r0p + (size_t)128 * rowb;
-                }
-            }
-            const uint32_t dst = sbase + kOffRA + (uint32_t)rs * kARaw;
-#pragma unroll
-            for (int p = lane; p < 64 * 4; p += 32) {
-                const int row = 64 * lw + (p >> 2), col = p & 3;
-                if (col < 2 * ch) {
-                    const uint8_t *src = (row < 128 ? r0p + (size_t)row * rowb : r1p + (size_t)(row - 128) * rowb) +
-                                         ks0 * 32 + col * 16;
-                    cp_async16(dst + raw_row_off(row) + col * 16, src, 16u);
-                }
-            }
-            cp_async_arrive(&sm.raw_full[rs]);
-            issued = q + 1;
-        }
-        // copies still in flight land before the CTA may leave (bounded)
-        const unsigned long long t0 = global_ns();
-        for (int q = issued - kRA < 0 ? 0 : issued - kRA; q < issued; ++q)
-            while (!mb_try(&sm.raw_full[q % kRA], (uint32_t)((q / kRA) & 1)))
-                if (global_ns() - t0 > kWaitNs) {
-                    atomicOr(a.err, kErrSyncTimeout);
-                    break;
-                }
     } else if (warp < 4) {
         // ------------------------------------------------------ epilogue
         // thread m = token row m of the tile (TMEM lane m)
