@@ -438,11 +438,38 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
     // one-entry view of the shared expert: grouped rows [n_sel, n_sel + T)
     if (tid < T) sm.rows[n_sel + tid] = tid * S + K;
     if (tid == 0) {
-        sm.epoch = ld_relaxed_u32(&a.dstate->epoch);
         sm.sh_uexp[0] = E;
         sm.sh_ubeg[0] = n_sel;
         sm.sh_ubeg[1] = n_sel + T;
     }
+    __syncthreads();
+
+    // Weights first: the router rows, then the first rows of the shared
+    // expert, which need no routing.  They depend on nothing the previous
+    // kernel in the stream writes, so they are requested before waiting for
+    // it (launched with programmatic stream serialisation, this grid may
+    // start while that one drains).
+    WrRegs<CPLG, MCH == 1> wr;  // D <= 1024 * CPLG; at one token also token 0's activations
+    if (b < E) logits_request_w(wr, a.Wr + (size_t)b * D, D);
+    int ex_u = -1;
+    DevExpert ex{};
+    UnitRegs<kGateUp, CPLG> A, B;
+    // (one token: the shared expert's gate/up streams here, within the
+    // routing's latency; more tokens: it is compute bound in the wide dot
+    // loops and would hold up the union, so it joins the routed entries'
+    // cost-weighted slices instead)
+    // (with adaptive top-p the shared rows follow the kept selections, whose
+    // count the routing decides: the shared expert then joins the slices)
+    const bool sh_early = MCH == 1 && a.n_shared && !(a.top_p > 0.f && a.top_p < 1.f);
+    const int sp0 = sh_early ? (int)((long long)b * I / G) : 0;
+    const int sp1 = sh_early ? (int)((long long)(b + 1) * I / G) : 0;
+    // (a router CTA requests them once its logits are out, so that the router
+    // rows have HBM to themselves at the start)
+    if (b >= E) prime<kGateUp, CPLG>(A, B, a, sm.sh_uexp, I, sp0, sp1, ex_u, ex);
+    // everything the previous kernel wrote (the activations, the decode
+    // state) is read from here on
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (tid == 0) sm.epoch = ld_relaxed_u32(&a.dstate->epoch);
     __syncthreads();
     stamp(a, 0);
     // this launch's set of counters and hand-over buffers; the other set
@@ -465,30 +492,9 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
         }
     }
 
-    // ---- phase 1.  The router rows go first (everything downstream waits on
-    // the logits), then the first rows of the shared expert, which need no
-    // routing.
-    WrRegs<CPLG, MCH == 1> wr;  // D <= 1024 * CPLG; at one token also token 0's activations
-    if (b < E) {
-        logits_request(wr, a.Wr + (size_t)b * D, a.x, D);
-    } else {
-        if constexpr (MCH == 1) x0_request(wr, a.x, D);
-    }
-    int ex_u = -1;
-    DevExpert ex{};
-    UnitRegs<kGateUp, CPLG> A, B;
-    // (one token: the shared expert's gate/up streams here, within the
-    // routing's latency; more tokens: it is compute bound in the wide dot
-    // loops and would hold up the union, so it joins the routed entries'
-    // cost-weighted slices instead)
-    // (with adaptive top-p the shared rows follow the kept selections, whose
-    // count the routing decides: the shared expert then joins the slices)
-    const bool sh_early = MCH == 1 && a.n_shared && !(a.top_p > 0.f && a.top_p < 1.f);
-    const int sp0 = sh_early ? (int)((long long)b * I / G) : 0;
-    const int sp1 = sh_early ? (int)((long long)(b + 1) * I / G) : 0;
-    // (a router CTA requests them once its logits are out, so that the router
-    // rows have HBM to themselves at the start)
-    if (b >= E) prime<kGateUp, CPLG>(A, B, a, sm.sh_uexp, I, sp0, sp1, ex_u, ex);
+    // ---- phase 1.  The router logits (everything downstream waits on
+    // them); at one token every CTA also holds token 0's activations.
+    if constexpr (MCH == 1) x0_request(wr, a.x, D);
 
     // router logits of experts b, b + G, ... (the arithmetic of the
     // four-kernel router), published as data: the slot itself is the flag
@@ -625,6 +631,9 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
     stamp(a, 7);
     stream_phase<kDown, CPLD, MCH>(a, sm, xs, sm.uexp, sm.ubeg, dp0, dp1, A2, B2, ex_u, ex);
     stamp(a, 8);
+    // the next kernel in the stream may launch once every CTA is here: its
+    // prologue (weight requests) overlaps this grid's reduce and exit
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // rows written per reduce block; the CTA whose rows complete a block
     // (n_u entries x its rows) reduces it.  Thread 0 lists the (block, rows)

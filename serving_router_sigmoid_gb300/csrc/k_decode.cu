@@ -59,11 +59,15 @@ cudaError_t launch_decode_layer(const LayerArgs &a, int grid, cudaStream_t s) {
     cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = smem_of(a);
     cfg.stream = s;
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeCooperative;
     at[0].val.cooperative = 1;
+    // the kernel waits (griddepcontrol.wait) before it reads anything the
+    // previous kernel in the stream writes, so it may start early
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, fn, a);
 }
 

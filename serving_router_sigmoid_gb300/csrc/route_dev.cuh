@@ -400,6 +400,21 @@ __device__ __forceinline__ float logits_finish(const WrRegs<NW, X0> &r, const fl
     return l;
 }
 
+// Loads only the router row into r.w (logits_request without the
+// activations: weights may be requested before the previous kernel in the
+// stream, which writes the activations, has finished).
+template <int NW, bool X0>
+__device__ __forceinline__ void logits_request_w(WrRegs<NW, X0> &r, const float *__restrict__ wrow, int D) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int L8 = D >> 5;
+    const float4 *wr = reinterpret_cast<const float4 *>(wrow) + warp * L8;
+#pragma unroll
+    for (int j = 0; j < NW; ++j) {
+        const int c = j * 32 + lane;
+        r.w[j] = c < L8 ? __ldg(wr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
 // Loads only token 0's activations into r.x0, in logits_request's layout (for
 // a CTA that computes no logit but quantises token 0 from registers).
 template <int NW>
