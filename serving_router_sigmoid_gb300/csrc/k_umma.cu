@@ -73,10 +73,10 @@ namespace moe {
 namespace {
 
 constexpr int kGU = 0, kDN = 1;
-constexpr int kThreads = 704;             // 22 warps
 constexpr int kConvWarp0 = 4;             // 16 converter warps
 constexpr int kMmaWarp = 20;
 constexpr int kTmaWarp = 21;              // activation tiles
+constexpr int kWTmaWarp = 22;             // packed weight tiles (TMA variant)
 constexpr int kBKs = 64;                  // K elements per stage
 constexpr int kTok = 128;                 // token rows per tile (the MMA's M)
 constexpr int kWN = 256;                  // weight rows per tile (the MMA's N)
@@ -84,23 +84,37 @@ constexpr int kBoxRows = 32;              // token rows per TMA box
 constexpr int kStW = 3;                   // f16 weight tile stages (converted, shared memory)
 constexpr int kStX = 5;                   // f16 token tile stages (TMA, shared memory)
 constexpr int kPD = 4;                    // weight stages each converter thread has in flight (registers)
+constexpr int kRW = 5;                    // packed weight tile stages (TMA variant)
 constexpr uint32_t kXF16 = kTok * 128;    // 128 tokens x 64 f16
 constexpr uint32_t kWF16 = kWN * 128;     // 256 weight rows x 64 f16
+constexpr uint32_t kRawB = kWN * 32;      // 256 weight rows x 64 packed int4
 constexpr uint32_t kOffX = 0;
 constexpr uint32_t kOffW = kOffX + kStX * kXF16;
-constexpr uint32_t kDyn = kOffW + kStW * kWF16;
-constexpr size_t kSmemBytes = kDyn + 1024;       // + alignment to 1024 bytes
-constexpr uint32_t kTmemCols = 2 * kWN;          // two accumulators of 256 columns
+constexpr uint32_t kOffR = kOffW + kStW * kWF16;
+constexpr uint32_t kTmemCols = 2 * kWN;   // two accumulators of 256 columns
+// WTMA: the packed weights arrive by TMA into a ring of kRW stages (one more
+// warp issues them); else the converter threads load them into registers.
+template <bool WTMA>
+struct Cfg {
+    static constexpr int kThreads = WTMA ? 736 : 704;  // 23 or 22 warps
+    static constexpr uint32_t kDyn = kOffR + (WTMA ? kRW * kRawB : 0);
+    static constexpr size_t kSmemBytes = kDyn + 1024;  // + alignment to 1024 bytes
+};
 
 struct UmmaSmem {
     uint64_t full[kStW], empty_w[kStW], bfull[kStX], empty_x[kStX], acc_full[2], acc_empty[2], drain;
+    uint64_t raw_full[kRW], raw_empty[kRW];
     uint32_t tmem;
     int abort;
     int tp[kMaxE + 2];        // tiles before each union entry
     float wsc[2][kWN];        // per accumulator: the row scales of the tile's weight rows
 };
 
-static_assert(kSmemBytes + sizeof(UmmaSmem) <= 196 * 1024, "keep the L1 share the weight loads need");
+// Loads into registers need the L1 (its share of the SM's 256 KB is what
+// shared memory leaves): 176 KB leaves 60 KB, and the same kernel with 32 KB
+// more shared memory, unused, ran 1.2x slower.  TMA loads do not.
+static_assert(Cfg<false>::kSmemBytes + sizeof(UmmaSmem) <= 196 * 1024, "keep the L1 share the weight loads need");
+static_assert(Cfg<true>::kSmemBytes + sizeof(UmmaSmem) <= 227 * 1024, "shared memory of one CTA");
 
 __device__ __forceinline__ uint32_t su32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -252,8 +266,9 @@ __device__ __forceinline__ Tile tile_of(const LayerArgs &a, const UmmaSmem &sm, 
     return x;
 }
 
-template <int KIND>
-__global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, LayerArgs a) {
+template <int KIND, bool WTMA>
+__global__ void __launch_bounds__(Cfg<WTMA>::kThreads, 1)
+    umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, LayerArgs a) {
     extern __shared__ uint8_t dyn_raw[];
     __shared__ UmmaSmem sm;
     uint8_t *dyn = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dyn_raw) + 1023) & ~uintptr_t(1023));
@@ -288,6 +303,10 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
             mb_init(&sm.acc_empty[s], 4);
         }
         mb_init(&sm.drain, 1);
+        for (int s = 0; s < kRW; ++s) {
+            mb_init(&sm.raw_full[s], 1);    // the weight TMA issuer's arrival, plus the tile's bytes
+            mb_init(&sm.raw_empty[s], 16);  // the converter warps
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == kMmaWarp) {
@@ -303,7 +322,39 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
     const int n_my = b < n_tiles ? (n_tiles - b + G - 1) / G : 0;
     const int n_stages = n_my * kst;
 
-    if (warp >= kConvWarp0 && warp < kConvWarp0 + 16) {
+    if (WTMA && warp >= kConvWarp0 && warp < kConvWarp0 + 16) {
+        // ------------------------------------ converters (weights by TMA)
+        // thread: weight row n = 16 * cw + lane / 2 of the tile, 16-byte half
+        // hf = lane % 2 of its 32 packed bytes (a warp reads 512 contiguous
+        // bytes of the ring slot).  The ring slot is written by the async
+        // proxy (TMA) and read here by the generic one, so it is released
+        // only after the proxy fence that also publishes the f16 tile.
+        const int cw = warp - kConvWarp0, n = 16 * cw + (lane >> 1), hf = lane & 1;
+        int fs = 0, fph = 0, rs = 0, rph = 0;  // weight tile and ring slots, use parities
+        for (int i = 0; i < n_stages; ++i) {
+            bool ok = mb_wait(&sm.raw_full[rs], (uint32_t)rph, abort, a.err);
+            if (__any_sync(0xffffffffu, !ok)) break;  // the whole warp leaves together
+            const uint4 w = *reinterpret_cast<const uint4 *>(dyn + kOffR + (uint32_t)rs * kRawB + (uint32_t)n * 32u +
+                                                             (uint32_t)hf * 16u);
+            ok = i < kStW || mb_wait(&sm.empty_w[fs], (uint32_t)(fph ^ 1), abort, a.err);
+            if (__any_sync(0xffffffffu, !ok)) break;
+            uint8_t *wt = dyn + kOffW + (uint32_t)fs * kWF16;
+            *reinterpret_cast<uint4 *>(wt + sw_off(n, 4 * hf + 0)) = w4_to_f16(w.x);
+            *reinterpret_cast<uint4 *>(wt + sw_off(n, 4 * hf + 1)) = w4_to_f16(w.y);
+            *reinterpret_cast<uint4 *>(wt + sw_off(n, 4 * hf + 2)) = w4_to_f16(w.z);
+            *reinterpret_cast<uint4 *>(wt + sw_off(n, 4 * hf + 3)) = w4_to_f16(w.w);
+            // the slot read and the tile written, both ordered before the
+            // async proxy's next accesses (the TMA refill, the MMA)
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+                mb_arrive(&sm.raw_empty[rs]);
+                mb_arrive(&sm.full[fs]);
+            }
+            if (++rs == kRW) { rs = 0; rph ^= 1; }
+            if (++fs == kStW) { fs = 0; fph ^= 1; }
+        }
+    } else if (!WTMA && warp >= kConvWarp0 && warp < kConvWarp0 + 16) {
         // ------------------------------------------------------ converters
         // thread: weight row n = 16 * cw + lane / 2 of the tile (a warp reads
         // 16 whole 32-byte row pieces per stage), 16-byte half hf = lane % 2
@@ -441,6 +492,48 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
                     }
         }
         __syncwarp();
+    } else if (WTMA && warp == kWTmaWarp) {
+        // ------------------------------------------ packed weight tiles (TMA)
+        // each stage: the tile's 256 rows x 32 bytes, two boxes of 128 rows
+        // (gate/up: the gate rows, then the same rows of up; down: 256 rows)
+        if (lane == 0) {
+            int issued = 0, t_ti = -1, y0 = 0, y1 = 0, rs = 0, rph = 0;
+            const CUtensorMap *m0 = nullptr, *m1 = nullptr;
+            for (int i = 0; i < n_stages && !*abort; ++i) {
+                const int ti = i / kst, ks = i - ti * kst;
+                if (ti != t_ti) {
+                    t_ti = ti;
+                    const Tile x = tile_of(a, sm, nu, b + ti * G);
+                    const int e = a.meta->uexp[x.u];
+                    if (KIND == kGU) {
+                        m0 = a.wmaps + 3 * e;
+                        m1 = m0 + 1;
+                        y0 = y1 = x.wb * 128;
+                    } else {
+                        m0 = m1 = a.wmaps + 3 * e + 2;
+                        y0 = x.wb * 256;
+                        y1 = y0 + 128;
+                    }
+                }
+                // the slot is free once every converter warp has read it
+                if (i >= kRW && !mb_wait(&sm.raw_empty[rs], (uint32_t)(rph ^ 1), abort, a.err)) break;
+                mb_expect_tx(&sm.raw_full[rs], kRawB);
+                const uint32_t dst = sbase + kOffR + (uint32_t)rs * kRawB;
+                tma_load_2d(dst, m0, ks * 32, y0, &sm.raw_full[rs]);
+                tma_load_2d(dst + kRawB / 2, m1, ks * 32, y1, &sm.raw_full[rs]);
+                issued = i + 1;
+                if (++rs == kRW) { rs = 0; rph ^= 1; }
+            }
+            // tiles still in flight land before the CTA may leave (bounded)
+            const unsigned long long t0 = global_ns();
+            for (int i = issued - kRW < 0 ? 0 : issued - kRW; i < issued; ++i)
+                while (!mb_try(&sm.raw_full[i % kRW], (uint32_t)((i / kRW) & 1)))
+                    if (global_ns() - t0 > kWaitNs) {
+                        atomicOr(a.err, kErrSyncTimeout);
+                        break;
+                    }
+        }
+        __syncwarp();
     } else if (warp < 4) {
         // ------------------------------------------------------ epilogue
         // thread m = token row m of the tile (TMEM lane m)
@@ -544,12 +637,13 @@ __global__ void __launch_bounds__(256) act_rows_f16_kernel(const int8_t *__restr
     }
 }
 
-template <int KIND>
+template <int KIND, bool WTMA>
 cudaError_t launch_u(const LayerArgs &a, const CUtensorMap &map, int num_sms, cudaStream_t s) {
-    auto fn = umma_gemm_kernel<KIND>;
-    cudaError_t ce = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    auto fn = umma_gemm_kernel<KIND, WTMA>;
+    constexpr size_t smem = Cfg<WTMA>::kSmemBytes;
+    cudaError_t ce = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (ce != cudaSuccess) return ce;
-    fn<<<num_sms, kThreads, kSmemBytes, s>>>(map, a);
+    fn<<<num_sms, Cfg<WTMA>::kThreads, smem, s>>>(map, a);
     return cudaGetLastError();
 }
 
@@ -608,11 +702,35 @@ cudaError_t launch_act_rows_f16(const LayerArgs &a, cudaStream_t s) {
 }
 
 cudaError_t launch_umma_gateup(const LayerArgs &a, const UmmaMaps &maps, int num_sms, cudaStream_t s) {
-    return launch_u<kGU>(a, maps.gu, num_sms, s);
+    return a.wmaps ? launch_u<kGU, true>(a, maps.gu, num_sms, s) : launch_u<kGU, false>(a, maps.gu, num_sms, s);
 }
 
 cudaError_t launch_umma_down(const LayerArgs &a, const UmmaMaps &maps, int num_sms, cudaStream_t s) {
-    return launch_u<kDN>(a, maps.dn, num_sms, s);
+    return a.wmaps ? launch_u<kDN, true>(a, maps.dn, num_sms, s) : launch_u<kDN, false>(a, maps.dn, num_sms, s);
+}
+
+// The packed weight tiles of every expert of the table: per expert three
+// maps (gate, up, down) of uint8 rows, boxes of 32 bytes x 128 rows, no
+// swizzle (the converters read 32-byte row pieces), 256-byte L2 promotion.
+cudaError_t umma_encode_weight_maps(const DevExpert *tab, int ne, int D, int I, CUtensorMap *maps) {
+    EncodeTiledFn fn = nullptr;
+    cudaError_t ce = encode_fn(&fn);
+    if (ce != cudaSuccess) return ce;
+    auto enc = [&](const uint8_t *base, int rows, int rowb, CUtensorMap *m) {
+        if (!base || (reinterpret_cast<uintptr_t>(base) & 15u)) return false;
+        const cuuint64_t dims[2] = {(cuuint64_t)rowb, (cuuint64_t)rows};
+        const cuuint64_t strides[1] = {(cuuint64_t)rowb};
+        const cuuint32_t box[2] = {32u, 128u};
+        const cuuint32_t estr[2] = {1, 1};
+        return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    for (int e = 0; e < ne; ++e)
+        if (!enc(tab[e].gq, I, D / 2, &maps[3 * e]) || !enc(tab[e].uq, I, D / 2, &maps[3 * e + 1]) ||
+            !enc(tab[e].dq, D, I / 2, &maps[3 * e + 2]))
+            return cudaErrorInvalidValue;
+    return cudaSuccess;
 }
 
 }  // namespace moe

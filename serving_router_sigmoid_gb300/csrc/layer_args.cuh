@@ -47,6 +47,7 @@ struct LayerArgs {
     int nb_gu, rpi_gu;   // gate/up: row blocks per expert, rows per block
     int nb_dn, rpi_dn;   // down: row blocks per expert, rows per block
     int wait_extra;      // test hook: arrivals the decode kernel's grid barrier waits for beyond G
+    const CUtensorMap *wmaps;  // [3 (E + n_shared)] TMA maps of the packed gate, up, down rows, or null
     DebugPtrs dbg;
 };
 
@@ -99,6 +100,8 @@ struct UmmaMaps {
 };
 bool umma_supported(int D, int I);
 cudaError_t umma_encode_maps(void *xf, int rows, int D, int I, UmmaMaps *maps);
+// Host: the weight maps of an expert table (host copy of the device table).
+cudaError_t umma_encode_weight_maps(const DevExpert *tab, int ne, int D, int I, CUtensorMap *maps);
 cudaError_t launch_act_rows_f16(const LayerArgs &a, cudaStream_t s);
 cudaError_t launch_umma_gateup(const LayerArgs &a, const UmmaMaps &maps, int num_sms, cudaStream_t s);
 cudaError_t launch_umma_down(const LayerArgs &a, const UmmaMaps &maps, int num_sms, cudaStream_t s);

@@ -56,6 +56,7 @@ struct Handle {
     uint16_t *xf;  // f16 operand rows of the tcgen05 GEMMs
     moe::UmmaMaps maps;  // their TMA tensor maps
     bool maps_ok;
+    CUtensorMap *wmaps;  // device [3 (E + n_shared)]: TMA maps of the packed expert rows, or null
     int32_t *hsum;
     float *shq;
     int32_t *dn_cnt;
@@ -221,6 +222,7 @@ int run_layer(Handle *h, const float *x, int T, float *out, const float *resid, 
     a.out = out; a.resid = resid; a.err = h->err;
     a.nb_gu = h->nb_gu; a.rpi_gu = h->rpi_gu; a.nb_dn = h->nb_dn; a.rpi_dn = h->rpi_dn;
     a.wait_extra = h->test_wait_extra;
+    a.wmaps = h->wmaps;
     a.dbg = dbg;
     const int mch = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8;
     const int mi = moe::mch_index(mch);
@@ -446,6 +448,20 @@ int moe_layer_create(const MoeLayerDesc *desc, const float *Wr, const float *bia
         tab[e] = moe::DevExpert{experts[e].gate_q, experts[e].up_q, experts[e].down_q,
                                 experts[e].gate_s, experts[e].up_s, experts[e].down_s};
     ce = cudaMemcpy(h->experts, tab, sizeof(moe::DevExpert) * ne, cudaMemcpyHostToDevice);
+    // TMA maps of the packed rows for the tcgen05 GEMMs (without them, or if
+    // a row start is not 16-byte aligned, those GEMMs load the rows into
+    // registers instead)
+    if (ce == cudaSuccess && h->maps_ok) {
+        CUtensorMap *hm = new (std::nothrow) CUtensorMap[3 * (size_t)ne];
+        if (hm && moe::umma_encode_weight_maps(tab, ne, desc->D, desc->I, hm) == cudaSuccess &&
+            cudaMalloc(&h->wmaps, sizeof(CUtensorMap) * 3 * (size_t)ne) == cudaSuccess) {
+            ce = cudaMemcpy(h->wmaps, hm, sizeof(CUtensorMap) * 3 * (size_t)ne, cudaMemcpyHostToDevice);
+        } else {
+            cudaGetLastError();
+            h->wmaps = nullptr;
+        }
+        delete[] hm;
+    }
     delete[] tab;
     if (ce == cudaSuccess) ce = cudaMemset(h->ws, 0, h->ws_bytes);
     if (ce == cudaSuccess) ce = reset_decode_state(h, 0);
@@ -453,6 +469,7 @@ int moe_layer_create(const MoeLayerDesc *desc, const float *Wr, const float *bia
     if (ce != cudaSuccess) {
         cudaFree(h->ws);
         cudaFree(h->experts);
+        cudaFree(h->wmaps);
         delete h;
         return cuda_fail(ce, "handle initialisation");
     }
@@ -468,6 +485,7 @@ int moe_layer_destroy(void *handle) {
     cudaError_t ce = cudaDeviceSynchronize();
     cudaFree(h->ws);
     cudaFree(h->experts);
+    cudaFree(h->wmaps);
     h->magic = 0;
     delete h;
     return ce == cudaSuccess ? MOE_OK : cuda_fail(ce, "destroy");
