@@ -28,20 +28,30 @@
 //    producer thread moves each stage's 128-token tile into shared memory
 //    with TMA tile loads (boxes of 32 rows x 64 f16 = 128 bytes per row,
 //    128-byte swizzle: the K-major layout the MMA reads).
-//  - One CTA per SM, 22 warps: 4 epilogue warps (TMEM lanes 0..127 = the
-//    tile's tokens), 16 converter warps, 1 MMA warp, 1 activation TMA warp.
+//  - Packed weights, two ways.  With per-expert tensor maps (built with the
+//    layer handle) one producer thread moves each stage's 256 rows x 32
+//    packed bytes into a 5-stage ring by TMA (boxes of 128 rows).  Without
+//    them (the allocation-free entry point) the converter threads load
+//    their packed bytes straight from global memory into registers, kPD
+//    stages ahead and across tile boundaries (a warp: 16 rows x 32 bytes,
+//    whole sectors).
 //  - Converter thread c owns one 16-byte half of one weight row of every
-//    stage (a warp: 16 rows x 32 bytes, whole 32-byte sectors).  It loads
-//    its packed bytes straight from global memory into registers, kPD
-//    stages ahead and across tile boundaries, then, once the stage's slot
-//    is free, expands them to f16 (a byte permute into 0x64xx patterns and
-//    one f16x2 subtraction per pair) and stores the four 16-byte results
-//    into the stage's 128-byte-swizzled K-major weight tile in shared memory
-//    (the MMA's B operand); its warp then arrives on the stage's barrier.
-//    The packed weight nibbles come out in the order e0 e2 e4 e6 e1 e3 e5 e7
-//    of each 8-group, which is exactly the even/odd order in which the
-//    activation rows are stored, so both operands see the same permutation
-//    of K.
+//    stage.  Once the stage's f16 slot is free it expands its bytes to f16
+//    (a byte permute into 0x64xx patterns and one f16x2 subtraction per
+//    pair) and stores the four 16-byte results into the stage's
+//    128-byte-swizzled K-major weight tile in shared memory (the MMA's B
+//    operand); after a proxy fence its warp arrives on the stage's barrier
+//    (and releases the TMA ring slot it read: generic reads of memory the
+//    async proxy rewrites).  The packed weight nibbles come out in the order
+//    e0 e2 e4 e6 e1 e3 e5 e7 of each 8-group, which is exactly the even/odd
+//    order in which the activation rows are stored, so both operands see
+//    the same permutation of K.
+//  - One CTA per SM.  Warps 0..3 are the epilogue (TMEM lanes 0..127 = the
+//    tile's tokens); with the TMA weight path the MMA issuer, both TMA
+//    issuers and one converter share the first scheduler (warp % 4 == 0)
+//    and the other 15 converters the other three, because the MMA issuer
+//    runs a stage only when it gets issue slots (moving 3 converters off its
+//    scheduler took gate/up at prefill 2048 from 1.53 to 1.46 ms).
 //  - The MMA thread waits for a stage's weights (converter barrier) and its
 //    token tile (TMA transaction barrier), issues four M=128, N=256, K=16 MMAs
 //    (descriptors formed once per stage, +32 bytes per K=16 slice) and
@@ -50,10 +60,16 @@
 //    after a tile's last stage to an accumulator barrier.  Two 256-column
 //    TMEM accumulators (all 512 columns) let the epilogue of one tile
 //    overlap the MMAs of the next.
-//  - Shared memory stays at 176 KB (+ 4 KB of barriers and scales): at most
-//    196 KB per CTA leaves the L1 a 60 KB share of the SM's 256 KB, and the
-//    weight loads in flight need it (the same kernel with 32 KB more shared
+//  - Shared memory: 5 token stages (80 KB), 3 f16 weight stages (96 KB) and,
+//    with TMA weights, 5 packed stages (40 KB).  The register-load path keeps
+//    the CTA at most 196 KB, which leaves the L1 a 60 KB share of the SM's
+//    256 KB for its loads in flight (the same kernel with 32 KB more shared
 //    memory, unused, ran 1.2x slower).
+//  - What bounds it (ncu, gate/up at prefill 2048): the tensor pipe is
+//    active ~50% of the time, the LSU data pipe ~50% (the f16 weight stores
+//    and their bank conflicts with the tensor core's operand reads), issue
+//    ~50%; deeper rings (4 f16 weight stages, 6-8 packed stages) changed
+//    nothing, the scheduler that runs the MMA issuer did.
 //  - Epilogue: thread m of the 128 holds token m's whole row of the tile:
 //    gate/up: 16 gate and the matching 16 up columns at a time,
 //    h = silu(g)*u written as contiguous 128-byte runs, max|h| of the token
@@ -73,37 +89,51 @@ namespace moe {
 namespace {
 
 constexpr int kGU = 0, kDN = 1;
-constexpr int kConvWarp0 = 4;             // 16 converter warps
-constexpr int kMmaWarp = 20;
-constexpr int kTmaWarp = 21;              // activation tiles
-constexpr int kWTmaWarp = 22;             // packed weight tiles (TMA variant)
 constexpr int kBKs = 64;                  // K elements per stage
 constexpr int kTok = 128;                 // token rows per tile (the MMA's M)
 constexpr int kWN = 256;                  // weight rows per tile (the MMA's N)
 constexpr int kBoxRows = 32;              // token rows per TMA box
-constexpr int kStW = 3;                   // f16 weight tile stages (converted, shared memory)
-constexpr int kStX = 5;                   // f16 token tile stages (TMA, shared memory)
-constexpr int kPD = 4;                    // weight stages each converter thread has in flight (registers)
-constexpr int kRW = 5;                    // packed weight tile stages (TMA variant)
 constexpr uint32_t kXF16 = kTok * 128;    // 128 tokens x 64 f16
 constexpr uint32_t kWF16 = kWN * 128;     // 256 weight rows x 64 f16
 constexpr uint32_t kRawB = kWN * 32;      // 256 weight rows x 64 packed int4
-constexpr uint32_t kOffX = 0;
-constexpr uint32_t kOffW = kOffX + kStX * kXF16;
-constexpr uint32_t kOffR = kOffW + kStW * kWF16;
+constexpr int kPD = 4;                    // weight stages each converter thread has in flight (registers)
 constexpr uint32_t kTmemCols = 2 * kWN;   // two accumulators of 256 columns
-// WTMA: the packed weights arrive by TMA into a ring of kRW stages (one more
-// warp issues them); else the converter threads load them into registers.
+// Stage rings in shared memory: f16 token tiles (TMA), f16 weight tiles
+// (converted) and, when the packed weights arrive by TMA (WTMA, one more
+// warp issues them), their packed tiles; else the converter threads load the
+// packed weights into registers.
 template <bool WTMA>
 struct Cfg {
-    static constexpr int kThreads = WTMA ? 736 : 704;  // 23 or 22 warps
-    static constexpr uint32_t kDyn = kOffR + (WTMA ? kRW * kRawB : 0);
+    // warps: 0..3 epilogue (TMEM lane quadrants), then the MMA issuer, the
+    // token tile TMA issuer, (WTMA) the weight tile TMA issuer, all on the
+    // first sub-partition (warp % 4 == 0) with one converter; the other
+    // converters fill sub-partitions 1..3, so that the MMA issuer shares its
+    // scheduler with little converter work
+    static constexpr int kThreads = WTMA ? 768 : 704;  // 24 or 22 warps
+    static constexpr int kMmaWarp = WTMA ? 4 : 20;
+    static constexpr int kTmaWarp = WTMA ? 8 : 21;     // token tiles
+    static constexpr int kWTmaWarp = WTMA ? 12 : -1;   // packed weight tiles
+    // converter index of a warp (0..15), or -1
+    __device__ static int conv_of(int w) {
+        if (!WTMA) return w >= 4 && w < 20 ? w - 4 : -1;
+        if (w == 16) return 15;
+        if (w < 5 || w > 23 || (w & 3) == 0) return -1;
+        return ((w >> 2) - 1) * 3 + (w & 3) - 1;
+    }
+    static constexpr int kStX = 5;
+    static constexpr int kStW = 3;
+    static constexpr int kRW = WTMA ? 5 : 0;
+    static constexpr uint32_t kOffX = 0;
+    static constexpr uint32_t kOffW = kOffX + kStX * kXF16;
+    static constexpr uint32_t kOffR = kOffW + kStW * kWF16;
+    static constexpr uint32_t kDyn = kOffR + kRW * kRawB;
     static constexpr size_t kSmemBytes = kDyn + 1024;  // + alignment to 1024 bytes
 };
+constexpr int kStMax = 8;                 // barrier slots of the largest ring
 
 struct UmmaSmem {
-    uint64_t full[kStW], empty_w[kStW], bfull[kStX], empty_x[kStX], acc_full[2], acc_empty[2], drain;
-    uint64_t raw_full[kRW], raw_empty[kRW];
+    uint64_t full[kStMax], empty_w[kStMax], bfull[kStMax], empty_x[kStMax], acc_full[2], acc_empty[2], drain;
+    uint64_t raw_full[kStMax], raw_empty[kStMax];
     uint32_t tmem;
     int abort;
     int tp[kMaxE + 2];        // tiles before each union entry
@@ -269,6 +299,10 @@ __device__ __forceinline__ Tile tile_of(const LayerArgs &a, const UmmaSmem &sm, 
 template <int KIND, bool WTMA>
 __global__ void __launch_bounds__(Cfg<WTMA>::kThreads, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap xmap, LayerArgs a) {
+    constexpr int kStX = Cfg<WTMA>::kStX, kStW = Cfg<WTMA>::kStW, kRW = Cfg<WTMA>::kRW;
+    constexpr int kMmaWarp = Cfg<WTMA>::kMmaWarp, kTmaWarp = Cfg<WTMA>::kTmaWarp, kWTmaWarp = Cfg<WTMA>::kWTmaWarp;
+    constexpr uint32_t kOffX = Cfg<WTMA>::kOffX, kOffW = Cfg<WTMA>::kOffW, kOffR = Cfg<WTMA>::kOffR;
+    static_assert(kStX <= kStMax && kStW <= kStMax && kRW <= kStMax, "barrier slots");
     extern __shared__ uint8_t dyn_raw[];
     __shared__ UmmaSmem sm;
     uint8_t *dyn = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dyn_raw) + 1023) & ~uintptr_t(1023));
@@ -322,14 +356,15 @@ __global__ void __launch_bounds__(Cfg<WTMA>::kThreads, 1)
     const int n_my = b < n_tiles ? (n_tiles - b + G - 1) / G : 0;
     const int n_stages = n_my * kst;
 
-    if (WTMA && warp >= kConvWarp0 && warp < kConvWarp0 + 16) {
+    const int cw = Cfg<WTMA>::conv_of(warp);
+    if (WTMA && cw >= 0) {
         // ------------------------------------ converters (weights by TMA)
         // thread: weight row n = 16 * cw + lane / 2 of the tile, 16-byte half
         // hf = lane % 2 of its 32 packed bytes (a warp reads 512 contiguous
         // bytes of the ring slot).  The ring slot is written by the async
         // proxy (TMA) and read here by the generic one, so it is released
         // only after the proxy fence that also publishes the f16 tile.
-        const int cw = warp - kConvWarp0, n = 16 * cw + (lane >> 1), hf = lane & 1;
+        const int n = 16 * cw + (lane >> 1), hf = lane & 1;
         int fs = 0, fph = 0, rs = 0, rph = 0;  // weight tile and ring slots, use parities
         for (int i = 0; i < n_stages; ++i) {
             bool ok = mb_wait(&sm.raw_full[rs], (uint32_t)rph, abort, a.err);
@@ -354,13 +389,13 @@ __global__ void __launch_bounds__(Cfg<WTMA>::kThreads, 1)
             if (++rs == kRW) { rs = 0; rph ^= 1; }
             if (++fs == kStW) { fs = 0; fph ^= 1; }
         }
-    } else if (!WTMA && warp >= kConvWarp0 && warp < kConvWarp0 + 16) {
+    } else if (!WTMA && cw >= 0) {
         // ------------------------------------------------------ converters
         // thread: weight row n = 16 * cw + lane / 2 of the tile (a warp reads
         // 16 whole 32-byte row pieces per stage), 16-byte half hf = lane % 2
         // of the stage's 32 packed bytes; the loads run kPD stages ahead in
         // registers, across tile boundaries
-        const int cw = warp - kConvWarp0, n = 16 * cw + (lane >> 1), hf = lane & 1;
+        const int n = 16 * cw + (lane >> 1), hf = lane & 1;
         int l_i = 0, l_ti = 0, l_ks = 0;  // the next stage to load and its tile / K stage
         const uint8_t *src = nullptr;     // this thread's row piece in the tile l_ti
         auto load_next = [&](uint4 &dst) {
