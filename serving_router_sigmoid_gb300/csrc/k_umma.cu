@@ -35,10 +35,11 @@
 //    their packed bytes straight from global memory into registers, kPD
 //    stages ahead and across tile boundaries (a warp: 16 rows x 32 bytes,
 //    whole sectors).
-//  - Converter thread c owns one 16-byte half of one weight row of every
-//    stage.  Once the stage's f16 slot is free it expands its bytes to f16
+//  - A converter thread owns one weight row of every stage (TMA path: all
+//    32 packed bytes, 8 warps; register path: one 16-byte half, 16 warps).
+//    Once the stage's f16 slot is free it expands its bytes to f16
 //    (a byte permute into 0x64xx patterns and one f16x2 subtraction per
-//    pair) and stores the four 16-byte results into the stage's
+//    pair) and stores the 16-byte results into the stage's
 //    128-byte-swizzled K-major weight tile in shared memory (the MMA's B
 //    operand); after a proxy fence its warp arrives on the stage's barrier
 //    (and releases the TMA ring slot it read: generic reads of memory the
@@ -47,11 +48,11 @@
 //    order in which the activation rows are stored, so both operands see
 //    the same permutation of K.
 //  - One CTA per SM.  Warps 0..3 are the epilogue (TMEM lanes 0..127 = the
-//    tile's tokens); with the TMA weight path the MMA issuer, both TMA
-//    issuers and one converter share the first scheduler (warp % 4 == 0)
-//    and the other 15 converters the other three, because the MMA issuer
-//    runs a stage only when it gets issue slots (moving 3 converters off its
-//    scheduler took gate/up at prefill 2048 from 1.53 to 1.46 ms).
+//    tile's tokens); with the TMA weight path the MMA issuer and both TMA
+//    issuers share the first scheduler (warp % 4 == 0) with epilogue warp 0
+//    only, and the 8 converters the other three, because the MMA issuer
+//    runs a stage only when it gets issue slots (moving the converters off
+//    its scheduler took gate/up at prefill 2048 from 1.53 to 1.45 ms).
 //  - The MMA thread waits for a stage's weights (converter barrier) and its
 //    token tile (TMA transaction barrier), issues four M=128, N=256, K=16 MMAs
 //    (descriptors formed once per stage, +32 bytes per K=16 slice) and
@@ -104,20 +105,19 @@ constexpr uint32_t kTmemCols = 2 * kWN;   // two accumulators of 256 columns
 // packed weights into registers.
 template <bool WTMA>
 struct Cfg {
-    // warps: 0..3 epilogue (TMEM lane quadrants), then the MMA issuer, the
-    // token tile TMA issuer, (WTMA) the weight tile TMA issuer, all on the
-    // first sub-partition (warp % 4 == 0) with one converter; the other
-    // converters fill sub-partitions 1..3, so that the MMA issuer shares its
-    // scheduler with little converter work
-    static constexpr int kThreads = WTMA ? 768 : 704;  // 24 or 22 warps
+    // warps: 0..3 epilogue (TMEM lane quadrants); WTMA: the MMA issuer, the
+    // token tile and weight tile TMA issuers on the first sub-partition
+    // (warp % 4 == 0), the 8 converters on sub-partitions 1..3, so that the
+    // MMA issuer shares its scheduler with no converter work
+    static constexpr int kThreads = WTMA ? 480 : 704;  // 15 or 22 warps
+    static constexpr int kConv = WTMA ? 8 : 16;        // converter warps
     static constexpr int kMmaWarp = WTMA ? 4 : 20;
     static constexpr int kTmaWarp = WTMA ? 8 : 21;     // token tiles
     static constexpr int kWTmaWarp = WTMA ? 12 : -1;   // packed weight tiles
     // converter index of a warp (0..15), or -1
     __device__ static int conv_of(int w) {
         if (!WTMA) return w >= 4 && w < 20 ? w - 4 : -1;
-        if (w == 16) return 15;
-        if (w < 5 || w > 23 || (w & 3) == 0) return -1;
+        if (w < 5 || w > 14 || (w & 3) == 0) return -1;
         return ((w >> 2) - 1) * 3 + (w & 3) - 1;
     }
     static constexpr int kStX = 5;
@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(Cfg<WTMA>::kThreads, 1)
         sm.tp[nu] = run;
         sm.abort = 0;
         for (int s = 0; s < kStW; ++s) {
-            mb_init(&sm.full[s], 16);  // the 16 converter warps
+            mb_init(&sm.full[s], Cfg<WTMA>::kConv);  // the converter warps
             mb_init(&sm.empty_w[s], 1);
         }
         for (int s = 0; s < kStX; ++s) {
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(Cfg<WTMA>::kThreads, 1)
         mb_init(&sm.drain, 1);
         for (int s = 0; s < kRW; ++s) {
             mb_init(&sm.raw_full[s], 1);    // the weight TMA issuer's arrival, plus the tile's bytes
-            mb_init(&sm.raw_empty[s], 16);  // the converter warps
+            mb_init(&sm.raw_empty[s], Cfg<WTMA>::kConv);  // the converter warps
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -359,25 +359,30 @@ __global__ void __launch_bounds__(Cfg<WTMA>::kThreads, 1)
     const int cw = Cfg<WTMA>::conv_of(warp);
     if (WTMA && cw >= 0) {
         // ------------------------------------ converters (weights by TMA)
-        // thread: weight row n = 16 * cw + lane / 2 of the tile, 16-byte half
-        // hf = lane % 2 of its 32 packed bytes (a warp reads 512 contiguous
-        // bytes of the ring slot).  The ring slot is written by the async
+        // thread: weight row n = 32 * cw + lane of the tile, its 32 packed
+        // bytes (a warp reads 1 KB of the ring slot, contiguous; its 16-byte
+        // stores of 8 consecutive rows hit 8 different bank groups).  The
+        // ring slot is written by the async
         // proxy (TMA) and read here by the generic one, so it is released
         // only after the proxy fence that also publishes the f16 tile.
-        const int n = 16 * cw + (lane >> 1), hf = lane & 1;
+        const int n = 32 * cw + lane;
         int fs = 0, fph = 0, rs = 0, rph = 0;  // weight tile and ring slots, use parities
         for (int i = 0; i < n_stages; ++i) {
             bool ok = mb_wait(&sm.raw_full[rs], (uint32_t)rph, abort, a.err);
             if (__any_sync(0xffffffffu, !ok)) break;  // the whole warp leaves together
-            const uint4 w = *reinterpret_cast<const uint4 *>(dyn + kOffR + (uint32_t)rs * kRawB + (uint32_t)n * 32u +
-                                                             (uint32_t)hf * 16u);
+            const uint8_t *rp = dyn + kOffR + (uint32_t)rs * kRawB + (uint32_t)n * 32u;
+            const uint4 w = *reinterpret_cast<const uint4 *>(rp), v = *reinterpret_cast<const uint4 *>(rp + 16);
             ok = i < kStW || mb_wait(&sm.empty_w[fs], (uint32_t)(fph ^ 1), abort, a.err);
             if (__any_sync(0xffffffffu, !ok)) break;
             uint8_t *wt = dyn + kOffW + (uint32_t)fs * kWF16;
-            *reinterpret_cast<uint4 *>(wt + sw_off(n, 4 * hf + 0)) = w4_to_f16(w.x);
-            *reinterpret_cast<uint4 *>(wt + sw_off(n, 4 * hf + 1)) = w4_to_f16(w.y);
-            *reinterpret_cast<uint4 *>(wt + sw_off(n, 4 * hf + 2)) = w4_to_f16(w.z);
-            *reinterpret_cast<uint4 *>(wt + sw_off(n, 4 * hf + 3)) = w4_to_f16(w.w);
+            *reinterpret_cast<uint4 *>(wt + sw_off(n, 0)) = w4_to_f16(w.x);
+            *reinterpret_cast<uint4 *>(wt + sw_off(n, 1)) = w4_to_f16(w.y);
+            *reinterpret_cast<uint4 *>(wt + sw_off(n, 2)) = w4_to_f16(w.z);
+            *reinterpret_cast<uint4 *>(wt + sw_off(n, 3)) = w4_to_f16(w.w);
+            *reinterpret_cast<uint4 *>(wt + sw_off(n, 4)) = w4_to_f16(v.x);
+            *reinterpret_cast<uint4 *>(wt + sw_off(n, 5)) = w4_to_f16(v.y);
+            *reinterpret_cast<uint4 *>(wt + sw_off(n, 6)) = w4_to_f16(v.z);
+            *reinterpret_cast<uint4 *>(wt + sw_off(n, 7)) = w4_to_f16(v.w);
             // the slot read and the tile written, both ordered before the
             // async proxy's next accesses (the TMA refill, the MMA)
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
