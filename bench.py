@@ -57,15 +57,20 @@ DEFAULT_WORKLOAD = "glm_moe_layer_decode_b1"
 HOT_KERNEL_DECODE = "stream_kernel<0> (fused int4 gate/up, SiLU*up, max abs h)"
 HOT_KERNEL_SINGLE = "decode_layer_kernel (the whole layer as one persistent kernel)"
 HOT_KERNEL_DECODE8 = "gateup_kernel<12,1,8> (int8 gate/up rows, SiLU*up, max abs h)"
-HOT_KERNEL_PREFILL = ("umma_gemm_kernel<0> (tcgen05 f16-exact gate/up GEMM, tokens x 256 weight rows per MMA, "
-                      "SiLU*up, max abs h)")
+HOT_KERNEL_PREFILL = ("umma_gemm_kernel<0, 1> (tcgen05 f16-exact gate/up GEMM, tokens x 256 weight rows per MMA, "
+                      "packed weights by TMA, SiLU*up, max abs h)")
 # DRAM bytes (read + write) per launch of the dominant kernel from one ncu
 # capture of the current kernel source, or None.  Keyed by workload.
 TRAFFIC = {
     # decode_layer_kernel on the full decode batch-1 workload (launch-list
-    # capture with the DRAM byte counters): 176.7 MB read + 0.57 MB written
-    # per launch
-    "glm_moe_layer_decode_b1": 177.3e6,
+    # capture with the DRAM byte counters, 14 launches): 176.72 MB read +
+    # 0.30 MB written per launch
+    "glm_moe_layer_decode_b1": 177.02e6,
+    # umma_gemm_kernel<0, 1> (gate/up, packed weights by TMA) at prefill 2048,
+    # full capture of the profiling layout (16 physical experts aliased over
+    # the 257 table entries; the routing, tiles and bytes per tile are the
+    # full layer's): 2.507 GB read + 0.133 GB written per launch
+    "glm_moe_layer_prefill_2048": 2.640e9,
 }
 
 
