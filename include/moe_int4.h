@@ -287,6 +287,13 @@ int moe_layer_set_probe(void *handle, int which, cudaEvent_t begin, cudaEvent_t 
  * operand encoded at create); otherwise batches above 16 tokens run on the
  * legacy integer MMA whatever MOE_OPT_TCGEN05_GEMM says. */
 #define MOE_OPT_TCGEN05_GEMM_AVAILABLE 5
+/* 1 (default): the tcgen05 GEMMs bring the packed weight rows in by TMA,
+ * through tensor maps of every expert's gate, up and down rows that the
+ * handle encodes at create (3 x 128 bytes per expert, device memory owned by
+ * the handle); 0: the converter threads load them into registers.  Both give
+ * bit-identical results.  Reading it returns 0 when the maps could not be
+ * made (e.g. a weight row not 16-byte aligned): the register loads then run. */
+#define MOE_OPT_TCGEN05_TMA_WEIGHTS 6
 /* Test hook of the failure path, 0 (default) or 1: with 1 the persistent
  * decode kernel's grid barrier (after gate/up) waits for one arrival more
  * than there are CTAs, so that bounded wait runs out (one second) and the

@@ -26,6 +26,7 @@ MOE_PROBE_NONE, MOE_PROBE_GATE_UP, MOE_PROBE_DOWN, MOE_PROBE_ROUTER = 0, 1, 2, 3
 MOE_OPT_DECODE_SINGLE_KERNEL, MOE_OPT_DECODE_SINGLE_KERNEL_AVAILABLE, MOE_OPT_TCGEN05_GEMM = 1, 2, 3
 MOE_OPT_DECODE_TEST_WAIT_TIMEOUT = 4
 MOE_OPT_TCGEN05_GEMM_AVAILABLE = 5
+MOE_OPT_TCGEN05_TMA_WEIGHTS = 6
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it with "

@@ -57,6 +57,7 @@ struct Handle {
     moe::UmmaMaps maps;  // their TMA tensor maps
     bool maps_ok;
     CUtensorMap *wmaps;  // device [3 (E + n_shared)]: TMA maps of the packed expert rows, or null
+    bool tma_weights;    // MOE_OPT_TCGEN05_TMA_WEIGHTS
     int32_t *hsum;
     float *shq;
     int32_t *dn_cnt;
@@ -222,7 +223,7 @@ int run_layer(Handle *h, const float *x, int T, float *out, const float *resid, 
     a.out = out; a.resid = resid; a.err = h->err;
     a.nb_gu = h->nb_gu; a.rpi_gu = h->rpi_gu; a.nb_dn = h->nb_dn; a.rpi_dn = h->rpi_dn;
     a.wait_extra = h->test_wait_extra;
-    a.wmaps = h->wmaps;
+    a.wmaps = h->tma_weights ? h->wmaps : nullptr;
     a.dbg = dbg;
     const int mch = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8;
     const int mi = moe::mch_index(mch);
@@ -473,6 +474,7 @@ int moe_layer_create(const MoeLayerDesc *desc, const float *Wr, const float *bia
         delete h;
         return cuda_fail(ce, "handle initialisation");
     }
+    h->tma_weights = true;
     h->magic = kMagic;
     *handle_out = h;
     return MOE_OK;
@@ -567,6 +569,10 @@ int moe_layer_set_option(void *handle, int option, int value) {
             if (value != 0 && value != 1) return fail(MOE_ERR_INVALID_ARG, "value %d: need 0 or 1", value);
             h->test_wait_extra = value;
             return MOE_OK;
+        case MOE_OPT_TCGEN05_TMA_WEIGHTS:
+            if (value != 0 && value != 1) return fail(MOE_ERR_INVALID_ARG, "value %d: need 0 or 1", value);
+            h->tma_weights = value != 0;
+            return MOE_OK;
         default:
             return fail(MOE_ERR_INVALID_ARG, "unknown option %d", option);
     }
@@ -587,6 +593,9 @@ int moe_layer_get_option(void *handle, int option, int *value_out) {
             return MOE_OK;
         case MOE_OPT_TCGEN05_GEMM_AVAILABLE:
             *value_out = h->maps_ok && moe::umma_supported(h->d.D, h->d.I) ? 1 : 0;
+            return MOE_OK;
+        case MOE_OPT_TCGEN05_TMA_WEIGHTS:
+            *value_out = h->tma_weights && h->wmaps ? 1 : 0;
             return MOE_OK;
         case MOE_OPT_DECODE_SINGLE_KERNEL_AVAILABLE: {
             int any = 0;

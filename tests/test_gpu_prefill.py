@@ -62,6 +62,38 @@ def test_tcgen05_and_legacy_mma_bit_identical(moe, case):
         pair.close()
 
 
+TMA_WEIGHTS = 6  # MOE_OPT_TCGEN05_TMA_WEIGHTS
+
+
+@pytest.mark.parametrize("case", CASES + [dict(D=512, I=512, E=64, K=8, n_shared=1, T=2000)], ids=_ids)
+def test_tma_and_register_weight_paths_bit_identical(moe, case):
+    """The packed weights by TMA (per-expert tensor maps, the default) and by
+    the converter threads' register loads (the allocation-free entry point's
+    path) give the same int32 dots and outputs; a tile count several times
+    the SM count exercises both rings across many tiles per CTA."""
+    cfg = synth.LayerCfg("pfw", **case, seed=case["T"] + 5 * case["E"])
+    pair = LayerPair(cfg, wdev="cpu")
+    try:
+        xd = pair.x.cuda()
+        assert pair.gpu.get_option(TCGEN05_AVAILABLE) == 1
+        assert pair.gpu.get_option(TMA_WEIGHTS) == 1
+        want = dict(gate_acc=True, up_acc=True, hq=True, down_acc=True)
+        outs, dbgs = [], []
+        for opt in (1, 0):
+            pair.gpu.set_option(TMA_WEIGHTS, opt)
+            assert pair.gpu.get_option(TMA_WEIGHTS) == opt
+            out = torch.empty_like(xd)
+            dbgs.append(pair.gpu.moe_layer_debug(xd, out, **want))
+            outs.append(out)
+        torch.cuda.synchronize()
+        assert pair.gpu.device_status() == 0
+        for k in want:
+            assert torch.equal(dbgs[0][k], dbgs[1][k]), k
+        assert torch.equal(outs[0], outs[1])
+    finally:
+        pair.close()
+
+
 def test_saturated_dots_exact(moe):
     """All weights +c (int4 code 7) and all activations 1.0 (int8 code 127):
     every gate/up dot is 6144 * 7 * 127 = 5,462,016, near the 2^24 limit of
