@@ -82,6 +82,7 @@ struct DebugPtrs {
 // arithmetic never produces (it yields the canonical 0x7FFFFFFF).
 constexpr uint32_t kLogitEmpty = 0xFFFFFFFFu;
 constexpr unsigned long long kSelEmpty = 0xFFFFFFFFFFFFFFFFull;
+constexpr uint32_t kHEmpty = 0xFFFFFFFFu;  // an h value not yet written (one-token decode launches)
 constexpr unsigned long long kWaitNs = 1000000000ull;  // bound of every wait: 1 s
 
 __device__ __forceinline__ unsigned long long global_ns() {
@@ -105,6 +106,14 @@ __device__ __forceinline__ uint32_t ld_relaxed_u32(const void *p) {
 __device__ __forceinline__ unsigned long long ld_relaxed_u64(const void *p) {
     unsigned long long v;
     asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint4 ld_relaxed_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.relaxed.gpu.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p)
+                 : "memory");
     return v;
 }
 __device__ __forceinline__ void st_relaxed_u32(void *p, uint32_t v) {

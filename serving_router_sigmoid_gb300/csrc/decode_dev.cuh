@@ -169,7 +169,7 @@ __device__ __forceinline__ void prime(UnitRegs<KIND, CPL> &A, UnitRegs<KIND, CPL
 template <int KIND, int CPL, int MCH>
 __device__ __forceinline__ void stream_phase(const LayerArgs &a, DecodeSmem &sm, int8_t *xs, const int *uexp,
                                              const int *ubeg, int p0, int p1, UnitRegs<KIND, CPL> &A,
-                                             UnitRegs<KIND, CPL> &B, int &ex_u, DevExpert &ex) {
+                                             UnitRegs<KIND, CPL> &B, int &ex_u, DevExpert &ex, float *hset) {
     constexpr int UPG = KIND == kGateUp ? 2 : 1, RPG = UnitShape<KIND, CPL>::kRows;
     // at one token every gate/up entry multiplies the same row (token 0),
     // staged once in xs / sm.sx[0] / sm.xsum[0] by the caller
@@ -224,9 +224,33 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, DecodeSmem &sm,
             for (int m = 0; m < M; ++m) {
                 float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
                 if (gi < n8) {
-                    const float *hp = a.h + (size_t)(r0 + m) * kdim + 8 * gi;
-                    v0 = ld_cg_f4(hp);
-                    v1 = ld_cg_f4(hp + 4);
+                    if (MCH == 1 && hset) {
+                        // one token: the h values are their own flags (the
+                        // gate/up CTAs write them with no fence or counter);
+                        // this thread's 8 are read until none is still empty
+                        const float *hp = hset + (size_t)(r0 + m) * kdim + 8 * gi;
+                        const unsigned long long t0 = global_ns();
+                        for (;;) {
+                            const uint4 w0 = ld_relaxed_v4(hp), w1 = ld_relaxed_v4(hp + 4);
+                            v0 = make_float4(__uint_as_float(w0.x), __uint_as_float(w0.y), __uint_as_float(w0.z),
+                                             __uint_as_float(w0.w));
+                            v1 = make_float4(__uint_as_float(w1.x), __uint_as_float(w1.y), __uint_as_float(w1.z),
+                                             __uint_as_float(w1.w));
+                            const bool empty = w0.x == kHEmpty || w0.y == kHEmpty || w0.z == kHEmpty ||
+                                               w0.w == kHEmpty || w1.x == kHEmpty || w1.y == kHEmpty ||
+                                               w1.z == kHEmpty || w1.w == kHEmpty;
+                            if (!empty) break;
+                            if (global_ns() - t0 > kWaitNs) {
+                                atomicOr(a.err, kErrSyncTimeout);
+                                break;
+                            }
+                            __nanosleep(32);
+                        }
+                    } else {
+                        const float *hp = a.h + (size_t)(r0 + m) * kdim + 8 * gi;
+                        v0 = ld_cg_f4(hp);
+                        v1 = ld_cg_f4(hp + 4);
+                    }
                 }
                 float amax = fmaxf(fmaxf(fmaxf(fabsf(v0.x), fabsf(v0.y)), fmaxf(fabsf(v0.z), fabsf(v0.w))),
                                    fmaxf(fmaxf(fabsf(v1.x), fabsf(v1.y)), fmaxf(fabsf(v1.z), fabsf(v1.w))));
@@ -285,7 +309,12 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, DecodeSmem &sm,
                     const float gf = __fmul_rn(__fmul_rn((float)gi, sm.sx[lane]), held_gs);
                     const float uf = __fmul_rn(__fmul_rn((float)ui, sm.sx[lane]), R.s[0]);
                     const float hv = __fmul_rn(silu_f(gf), uf);
-                    a.h[(size_t)(r0 + lane) * a.I + o0] = hv;
+                    if (MCH == 1 && hset) {  // published as data: the down CTAs poll it
+                        const uint32_t bits = __float_as_uint(hv);
+                        st_relaxed_u32(hset + (size_t)(r0 + lane) * a.I + o0, bits == kHEmpty ? 0x7FFFFFFFu : bits);
+                    } else {
+                        a.h[(size_t)(r0 + lane) * a.I + o0] = hv;
+                    }
                     if (a.dbg.gate_acc) a.dbg.gate_acc[(size_t)sm.ent[lane] * a.I + o0] = gi;
                     if (a.dbg.up_acc) a.dbg.up_acc[(size_t)sm.ent[lane] * a.I + o0] = ui;
                 }
@@ -478,6 +507,12 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
     FusedSync *sy = &a.dstate->set[par];
     float *const dlog = a.dlog + (size_t)par * kSmallT * E;
     unsigned long long *const dsel = a.dsel + (size_t)par * kSmallT * K;
+    // one token with the hand-over buffer: the h rows, each value its own
+    // flag, instead of a grid barrier after gate/up (null: the barrier)
+    float *const hset = MCH == 1 && a.dh ? a.dh + (size_t)par * S * I : nullptr;
+    // (then the CTA counts itself as having read the epoch; CTA 0 advances
+    // it once all have)
+    if (hset && tid == 0) atomicAdd(&sy->gu_cnt, 1);
     {
         FusedSync *so = &a.dstate->set[par ^ 1];
         float *const olog = a.dlog + (size_t)(par ^ 1) * kSmallT * E;
@@ -486,6 +521,12 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
         for (int i = b * blockDim.x + tid; i < kSmallT * E; i += stride) st_relaxed_u32(olog + i, kLogitEmpty);
         for (int i = b * blockDim.x + tid; i < kSmallT * K; i += stride) st_relaxed_u64(osel + i, kSelEmpty);
         for (int i = b * blockDim.x + tid; i < kMaxRedBlk; i += stride) so->blk[i] = 0;
+        // (every launch, whatever its batch: the next launch may be a
+        // one-token one, which polls that set's h values)
+        if (a.dh) {
+            float *const oh = a.dh + (size_t)(par ^ 1) * S * I;
+            for (int i = b * blockDim.x + tid; i < S * I; i += stride) st_relaxed_u32(oh + i, kHEmpty);
+        }
         if (b == 0 && tid == 0) {
             so->quant_cnt = 0;
             so->gu_cnt = 0;
@@ -535,7 +576,7 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
     // shared expert gate/up, once the quantised tokens are in
     if (MCH > 1) cta_wait(&sy->quant_cnt, T, a.err);
     stamp(a, 2);
-    stream_phase<kGateUp, CPLG, MCH>(a, sm, xs, sm.sh_uexp, sm.sh_ubeg, sp0, sp1, A, B, ex_u, ex);
+    stream_phase<kGateUp, CPLG, MCH>(a, sm, xs, sm.sh_uexp, sm.sh_ubeg, sp0, sp1, A, B, ex_u, ex, hset);
     stamp(a, 3);
 
     // ---- phase 2: every CTA reads the published selections (bounded wait;
@@ -616,20 +657,26 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
         dp1 = sm.slice[3];
     }
     prime<kGateUp, CPLG>(A, B, a, sm.uexp, I, rp0, rp1, ex_u, ex);
-    stream_phase<kGateUp, CPLG, MCH>(a, sm, xs, sm.uexp, sm.ubeg, rp0, rp1, A, B, ex_u, ex);
+    stream_phase<kGateUp, CPLG, MCH>(a, sm, xs, sm.uexp, sm.ubeg, rp0, rp1, A, B, ex_u, ex, hset);
     stamp(a, 6);
 
-    // ---- phase 3: the CTA arrives, requests its first down rows, then
-    // waits for every h row and max|h| (arrival first: its fence would
-    // otherwise wait for these loads too)
-    cta_arrive(&sy->gu_cnt);
+    // ---- phase 3.  More tokens: the CTA arrives, requests its first down
+    // rows, then waits for every h row (arrival first: its fence would
+    // otherwise wait for these loads too).  One token: no barrier; the CTA
+    // requests its first down rows and its staging reads the entry's h rows
+    // until every value is there.
     UnitRegs<kDown, CPLD> A2, B2;
-    prime<kDown, CPLD>(A2, B2, a, sm.uexp, gpd, dp0, dp1, ex_u, ex);
-    cta_wait(&sy->gu_cnt, G + a.wait_extra, a.err);
-    // every CTA has read the epoch (before it arrived): advance it
-    if (b == 0 && tid == 0) st_relaxed_u32(&a.dstate->epoch, sm.epoch + 1u);
+    if (hset) {
+        prime<kDown, CPLD>(A2, B2, a, sm.uexp, gpd, dp0, dp1, ex_u, ex);
+    } else {
+        cta_arrive(&sy->gu_cnt);
+        prime<kDown, CPLD>(A2, B2, a, sm.uexp, gpd, dp0, dp1, ex_u, ex);
+        cta_wait(&sy->gu_cnt, G + a.wait_extra, a.err);
+        // every CTA has read the epoch (before it arrived): advance it
+        if (b == 0 && tid == 0) st_relaxed_u32(&a.dstate->epoch, sm.epoch + 1u);
+    }
     stamp(a, 7);
-    stream_phase<kDown, CPLD, MCH>(a, sm, xs, sm.uexp, sm.ubeg, dp0, dp1, A2, B2, ex_u, ex);
+    stream_phase<kDown, CPLD, MCH>(a, sm, xs, sm.uexp, sm.ubeg, dp0, dp1, A2, B2, ex_u, ex, hset);
     stamp(a, 8);
     // the next kernel in the stream may launch once every CTA is here: its
     // prologue (weight requests) overlaps this grid's reduce and exit
@@ -715,6 +762,24 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
             }
             *reinterpret_cast<float4 *>(a.out + (size_t)t * D + o) = acc;
         }
+    }
+
+    // one token: every CTA has read the epoch (each counted itself after
+    // reading it) before CTA 0 advances it (bounded; the test hook's extra
+    // arrival makes this wait run out)
+    if (hset && b == 0 && tid == 0) {
+        const int target = G + a.wait_extra;
+        if (ld_acquire(&sy->gu_cnt) < target) {
+            const unsigned long long t0 = global_ns();
+            while (ld_acquire(&sy->gu_cnt) < target) {
+                if (global_ns() - t0 > kWaitNs) {
+                    atomicOr(a.err, kErrSyncTimeout);
+                    break;
+                }
+                __nanosleep(64);
+            }
+        }
+        st_relaxed_u32(&a.dstate->epoch, sm.epoch + 1u);
     }
 
     stamp(a, 9);

@@ -39,6 +39,7 @@ struct LayerArgs {
     // counters; a set is empty (logits / selections) when its launch starts
     float *dlog;                 // [2][kSmallT, E] logits, kLogitEmpty until written
     unsigned long long *dsel;    // [2][kSmallT, K] packed selections, kSelEmpty until written
+    float *dh;                   // [2][S, I] h rows of a one-token launch, kHEmpty until written
     unsigned long long *trace;  // [trace_n] phase stamps of that kernel, or null
     int trace_n;
     float *out;          // [T, D]

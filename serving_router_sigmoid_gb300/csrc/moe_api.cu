@@ -64,6 +64,7 @@ struct Handle {
     moe::DecodeState *dstate;
     float *dlog;
     unsigned long long *dsel;
+    float *dh;  // [2][S, I] one-token h hand-over of the decode kernel (own allocation; null: grid barrier)
     int32_t *err;
     float *xnorm;  // [Tmax, D] RMSNorm output of moe_block_forward
     int nb_gu, rpi_gu, nb_dn, rpi_dn;
@@ -182,6 +183,7 @@ cudaError_t reset_decode_state(const Handle *h, cudaStream_t s) {
     cudaError_t ce = cudaMemsetAsync(h->dstate, 0, sizeof(moe::DecodeState), s);
     if (ce == cudaSuccess) ce = cudaMemsetAsync(h->dlog, 0xFF, 2 * 4 * moe::kSmallT * (size_t)h->d.E, s);
     if (ce == cudaSuccess) ce = cudaMemsetAsync(h->dsel, 0xFF, 2 * 8 * moe::kSmallT * (size_t)h->d.K, s);
+    if (ce == cudaSuccess && h->dh) ce = cudaMemsetAsync(h->dh, 0xFF, 2 * 4 * (size_t)h->S * h->d.I, s);
     return ce;
 }
 
@@ -218,7 +220,7 @@ int run_layer(Handle *h, const float *x, int T, float *out, const float *resid, 
     a.xq = h->xq; a.sx = h->sx; a.xsum = h->xsum; a.logits = h->logits; a.idx = h->idx; a.wts = h->wts;
     a.rows = h->rows; a.meta = h->meta; a.h = h->h; a.hamax = h->hamax; a.part = h->part; a.dn_cnt = h->dn_cnt;
     a.hq = h->hq; a.hsum = h->hsum; a.shq = h->shq; a.dstate = h->dstate;
-    a.dlog = h->dlog; a.dsel = h->dsel;
+    a.dlog = h->dlog; a.dsel = h->dsel; a.dh = h->dh;
     a.trace = h->trace; a.trace_n = h->trace_n;
     a.out = out; a.resid = resid; a.err = h->err;
     a.nb_gu = h->nb_gu; a.rpi_gu = h->rpi_gu; a.nb_dn = h->nb_dn; a.rpi_dn = h->rpi_dn;
@@ -465,12 +467,16 @@ int moe_layer_create(const MoeLayerDesc *desc, const float *Wr, const float *bia
     }
     delete[] tab;
     if (ce == cudaSuccess) ce = cudaMemset(h->ws, 0, h->ws_bytes);
+    // the one-token h hand-over (its own allocation, so that the workspace
+    // size, which the allocation-free entry point shares, does not change)
+    if (ce == cudaSuccess) ce = cudaMalloc(&h->dh, 2 * 4 * (size_t)h->S * desc->I);
     if (ce == cudaSuccess) ce = reset_decode_state(h, 0);
     if (ce == cudaSuccess) ce = cudaDeviceSynchronize();
     if (ce != cudaSuccess) {
         cudaFree(h->ws);
         cudaFree(h->experts);
         cudaFree(h->wmaps);
+        cudaFree(h->dh);
         delete h;
         return cuda_fail(ce, "handle initialisation");
     }
@@ -488,6 +494,7 @@ int moe_layer_destroy(void *handle) {
     cudaFree(h->ws);
     cudaFree(h->experts);
     cudaFree(h->wmaps);
+    cudaFree(h->dh);
     h->magic = 0;
     delete h;
     return ce == cudaSuccess ? MOE_OK : cuda_fail(ce, "destroy");
