@@ -477,14 +477,14 @@ def run_ours(args, workload, rank, world, local, n_layers=None, steps=None, warm
             lyr.set_probe(moe.MOE_PROBE_NONE)
 
         def e2e_step(i):
-            xd.copy_(xh[i % n_layers], non_blocking=True)
             if stack:
+                xd.copy_(xh[i % n_layers], non_blocking=True)
                 for lyr in layers:
                     lyr.moe_block_forward(xd, norm_w, cfg.eps)
                 oh.copy_(xd, non_blocking=True)
             else:
-                layers[i % n_layers].moe_layer_forward(xd, od)
-                oh.copy_(od, non_blocking=True)
+                # one C-ABI call: the copy in, the forward and the copy out
+                layers[i % n_layers].forward_host(xh[i % n_layers], oh, s)
 
         with torch.cuda.stream(s):
             for i in range(min(64, Ke)):
@@ -502,7 +502,7 @@ def run_ours(args, workload, rank, world, local, n_layers=None, steps=None, warm
         e_ms = max_over_ranks(e_ms, world, dev)
         e2e = {"value": T * Ke * world / (e_ms / 1e3), "unit": UNIT, "steps": Ke,
                "h2d_bytes_per_step": T * cfg.D * 4, "d2h_bytes_per_step": T * cfg.D * 4,
-               "api": "moe_block_forward" if stack else "moe_layer_forward", "graph": False}
+               "api": "moe_block_forward" if stack else "moe_layer_forward_host", "graph": False}
 
     cpu = None
     if rank == 0 and with_cpu and not args.no_cpu_baseline:

@@ -207,6 +207,23 @@ int moe_layer_forward(void *handle, const float *x, int n_tokens, float *out,
                       cudaStream_t stream);
 
 /*
+ * The same layer forward on host buffers (the pages' engine takes its
+ * activations from host memory; the pages have no separate entry point for
+ * it): enqueues on `stream`, in this order, the copy of x to the handle's
+ * device staging rows, moe_layer_forward, and the copy of the result back to
+ * out; returns before they finish (synchronise the stream before reading
+ * out).
+ *   x_host   host [n_tokens, D] fp32;  out_host host [n_tokens, D] fp32 out
+ *   Page-locked host memory lets the copies run asynchronously; with
+ *   pageable memory CUDA performs them synchronously.  The staging rows are
+ *   part of the handle (one forward at a time per handle, as for
+ *   moe_layer_forward); 0 <= n_tokens <= max_tokens.
+ * Errors: INVALID_ARG, SHAPE, CUDA.
+ */
+int moe_layer_forward_host(void *handle, const float *x_host, int n_tokens, float *out_host,
+                           cudaStream_t stream);
+
+/*
  * Residual MoE block of a layer stack: x <- x + MoE(RMSNorm(x)).
  * reader.mx article §04 (rmsnorm: mean of squares in double, r = 1/sqrtf(ms/D
  * + eps), x*r*w; layer order norm -> MoE -> residual add).

@@ -68,6 +68,7 @@ _SIGS = {
     "moe_layer_debug": ([_vp, _vp, _ci, _vp, ctypes.POINTER(MoeDebugOut), _vp], _ci),
     "moe_layer_device_status": ([_vp, _vp, ctypes.POINTER(_ci)], _ci),
     "moe_layer_set_probe": ([_vp, _ci, _vp, _vp], _ci),
+    "moe_layer_forward_host": ([_vp, _vp, _ci, _vp, _vp], _ci),
     "moe_layer_set_option": ([_vp, _ci, _ci], _ci),
     "moe_layer_set_trace": ([_vp, _vp, _ci], _ci),
     "moe_layer_get_option": ([_vp, _ci, ctypes.POINTER(_ci)], _ci),
@@ -218,6 +219,19 @@ class MoeLayer:
         out = torch.empty_like(x)
         self.moe_layer_forward(x, out, stream)
         return out
+
+    def forward_host(self, x_host, out_host, stream=None):
+        """moe_layer_forward_host: x_host / out_host are CPU float32 tensors
+        [n_tokens, D] (pinned memory keeps the copies asynchronous); the
+        result is in out_host once the stream has been synchronised."""
+        for name, t in (("x_host", x_host), ("out_host", out_host)):
+            if t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous() or t.dim() != 2 or \
+                    t.shape[1] != self.D:
+                raise ValueError(f"{name} must be a contiguous CPU float32 tensor [n_tokens, {self.D}]")
+        if out_host.shape[0] != x_host.shape[0]:
+            raise ValueError("x_host and out_host must have the same number of rows")
+        _check(_lib.moe_layer_forward_host(self.handle, ctypes.c_void_p(x_host.data_ptr()), x_host.shape[0],
+                                           ctypes.c_void_p(out_host.data_ptr()), _stream(stream)))
 
     def moe_block_forward(self, x_inout, norm_w, eps, stream=None):
         _check(_lib.moe_block_forward(self.handle, _ptr(x_inout), _ptr(norm_w), float(eps), x_inout.shape[0],

@@ -66,7 +66,8 @@ struct Handle {
     unsigned long long *dsel;
     float *dh;  // [2][S, I] one-token h hand-over of the decode kernel (own allocation; null: grid barrier)
     int32_t *err;
-    float *xnorm;  // [Tmax, D] RMSNorm output of moe_block_forward
+    float *xnorm;  // [Tmax, D] RMSNorm output of moe_block_forward; input staging of moe_layer_forward_host
+    float *xout;   // [Tmax, D] output staging of moe_layer_forward_host (own allocation)
     int nb_gu, rpi_gu, nb_dn, rpi_dn;
     int grid_gu[4], grid_dn[4];
     int num_sms;
@@ -470,6 +471,7 @@ int moe_layer_create(const MoeLayerDesc *desc, const float *Wr, const float *bia
     // the one-token h hand-over (its own allocation, so that the workspace
     // size, which the allocation-free entry point shares, does not change)
     if (ce == cudaSuccess) ce = cudaMalloc(&h->dh, 2 * 4 * (size_t)h->S * desc->I);
+    if (ce == cudaSuccess) ce = cudaMalloc(&h->xout, 4 * (size_t)desc->max_tokens * desc->D);
     if (ce == cudaSuccess) ce = reset_decode_state(h, 0);
     if (ce == cudaSuccess) ce = cudaDeviceSynchronize();
     if (ce != cudaSuccess) {
@@ -477,6 +479,7 @@ int moe_layer_create(const MoeLayerDesc *desc, const float *Wr, const float *bia
         cudaFree(h->experts);
         cudaFree(h->wmaps);
         cudaFree(h->dh);
+        cudaFree(h->xout);
         delete h;
         return cuda_fail(ce, "handle initialisation");
     }
@@ -495,6 +498,7 @@ int moe_layer_destroy(void *handle) {
     cudaFree(h->experts);
     cudaFree(h->wmaps);
     cudaFree(h->dh);
+    cudaFree(h->xout);
     h->magic = 0;
     delete h;
     return ce == cudaSuccess ? MOE_OK : cuda_fail(ce, "destroy");
@@ -506,6 +510,27 @@ int moe_layer_forward(void *handle, const float *x, int n_tokens, float *out, cu
     if (rc || n_tokens == 0) return rc;
     if (x == out) return fail(MOE_ERR_INVALID_ARG, "out may not alias x");
     return run_layer(h, x, n_tokens, out, nullptr, moe::DebugPtrs{}, stream);
+}
+
+int moe_layer_forward_host(void *handle, const float *x_host, int n_tokens, float *out_host,
+                           cudaStream_t stream) {
+    Handle *h = as_handle(handle);
+    if (!h) return fail(MOE_ERR_INVALID_ARG, "invalid handle");
+    if (n_tokens < 0 || n_tokens > h->d.max_tokens)
+        return fail(MOE_ERR_SHAPE, "n_tokens=%d outside [0, max_tokens=%d]", n_tokens, h->d.max_tokens);
+    if (n_tokens == 0) return MOE_OK;
+    if (!x_host || !out_host) return fail(MOE_ERR_INVALID_ARG, "x_host or out_host is NULL");
+    if (!h->xout) return fail(MOE_ERR_INVALID_ARG, "handle has no staging rows");
+    int rc = check_forward(h, h->xnorm, n_tokens, h->xout);
+    if (rc) return rc;
+    const size_t bytes = sizeof(float) * (size_t)n_tokens * h->d.D;
+    cudaError_t ce = cudaMemcpyAsync(h->xnorm, x_host, bytes, cudaMemcpyHostToDevice, stream);
+    if (ce != cudaSuccess) return cuda_fail(ce, "copy of x to the device");
+    rc = run_layer(h, h->xnorm, n_tokens, h->xout, nullptr, moe::DebugPtrs{}, stream);
+    if (rc) return rc;
+    ce = cudaMemcpyAsync(out_host, h->xout, bytes, cudaMemcpyDeviceToHost, stream);
+    if (ce != cudaSuccess) return cuda_fail(ce, "copy of out to the host");
+    return MOE_OK;
 }
 
 int moe_block_forward(void *handle, float *x_inout, const float *norm_w, float eps, int n_tokens,

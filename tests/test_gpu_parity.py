@@ -253,6 +253,38 @@ def test_layer_parity_adaptive_top_p(moe, case, top_p):
         pair.close()
 
 
+@pytest.mark.parametrize("T", [1, 5, 40])
+def test_forward_host_equals_forward(moe, T):
+    """moe_layer_forward_host (host buffers, copies in and out on the stream)
+    gives the device forward's output bit for bit, with pinned and with
+    pageable host memory; an empty batch does nothing; a batch beyond
+    max_tokens is a SHAPE error."""
+    cfg = synth.LayerCfg("host", D=256, I=128, E=16, K=2, n_shared=1, T=T, seed=T + 11)
+    pair = LayerPair(cfg, wdev="cpu")
+    try:
+        xd = pair.x.cuda()
+        ref = pair.gpu.forward(xd)
+        torch.cuda.synchronize()
+        for pinned in (True, False):
+            xh = pair.x.clone().contiguous()
+            oh = torch.full_like(xh, float("nan"))
+            if pinned:
+                xh, oh = xh.pin_memory(), oh.pin_memory()
+            s = torch.cuda.current_stream()
+            pair.gpu.forward_host(xh, oh, s)
+            s.synchronize()
+            assert torch.equal(oh, ref.cpu()), pinned
+        assert pair.gpu.device_status() == 0
+        empty = torch.empty((0, cfg.D), dtype=torch.float32)
+        pair.gpu.forward_host(empty, empty)
+        big = torch.zeros((cfg.T + 1, cfg.D), dtype=torch.float32)
+        with pytest.raises(moe.MoeError) as e:
+            pair.gpu.forward_host(big, big.clone())
+        assert e.value.code == moe.MOE_ERR_SHAPE
+    finally:
+        pair.close()
+
+
 def test_layer_forward_is_deterministic(moe):
     cfg = synth.LayerCfg("det", D=256, I=128, E=16, K=2, n_shared=1, T=40, seed=5)
     pair = LayerPair(cfg, wdev="cpu")
