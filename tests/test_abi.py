@@ -22,11 +22,12 @@ def lib():
     return moe.library()
 
 
-def test_header_declares_the_north_star_calls():
+def test_header_declares_the_layer_path_calls():
     names = declared_functions()
-    for n in ("moe_pack_int4", "moe_quant_act_int8", "moe_router_topk", "moe_layer_forward",
-              "moe_layer_create", "moe_layer_destroy", "moe_block_forward", "moe_layer_debug",
-              "moe_last_error"):
+    for n in ("moe_pack_int4", "moe_pack_int8", "moe_fp8_block_to_int4", "moe_quant_act_int8",
+              "moe_router_topk", "moe_layer_forward", "moe_layer_forward_host", "moe_layer_create",
+              "moe_layer_destroy", "moe_block_forward", "moe_layer_debug", "moe_layer_forward_static",
+              "moe_layer_static_status", "moe_last_error"):
         assert n in names
 
 
