@@ -54,6 +54,7 @@ namespace moe {
 namespace dec {
 
 constexpr int kMaxContrib = 128;                       // reduce-block arrivals listed per CTA
+constexpr int kTabEntries = kMaxK + 1;                 // union entries of one token (pointers kept in shared memory)
 
 // Thread 0 records phase stamp k of this CTA when tracing is on.
 __device__ __forceinline__ void stamp(const LayerArgs &a, int k) {
@@ -105,6 +106,7 @@ struct DecodeSmem {
     int ubeg[kSmallT * kMaxK + 2];    // union entry -> first grouped row
     int sh_uexp[1];                   // one-entry view of the shared expert
     int sh_ubeg[2];
+    DevExpert uexd[kTabEntries];      // one token: the union entries' expert pointers
     int nu;                           // routed union entries
     int nblk;                         // reduce blocks this CTA completed
     unsigned int epoch;               // the launch's epoch (DecodeState)
@@ -123,10 +125,13 @@ __device__ __forceinline__ int units_of_warp(int p0, int p1, int warp) {
 }
 
 // Requests unit j of this warp (group p0 + warp + 8*(j / UPG) of the union
-// view, matrix j % UPG) into R.  ex_u/ex cache the current expert's pointers.
+// view, matrix j % UPG) into R.  ex_u/ex cache the current expert's pointers,
+// read from tab[entry] when the CTA holds them in shared memory, else from
+// the global expert table.
 template <int KIND, int CPL>
 __device__ __forceinline__ void request(UnitRegs<KIND, CPL> &R, const LayerArgs &a, const int *uexp, int gpe,
-                                        int p0, int n_my, int j, int &ex_u, DevExpert &ex) {
+                                        int p0, int n_my, int j, int &ex_u, DevExpert &ex,
+                                        const DevExpert *tab = nullptr) {
     constexpr int UPG = KIND == kGateUp ? 2 : 1, RPG = UnitShape<KIND, CPL>::kRows;
     if (j >= n_my) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -135,7 +140,7 @@ __device__ __forceinline__ void request(UnitRegs<KIND, CPL> &R, const LayerArgs 
     const int p = p0 + warp + 8 * (j / UPG), u = p / gpe;
     if (u != ex_u) {
         ex_u = u;
-        ex = a.experts[uexp[u]];
+        ex = tab ? tab[u] : a.experts[uexp[u]];
     }
     const int o = (p - u * gpe) * RPG;
     const uint8_t *mat;
@@ -153,11 +158,12 @@ __device__ __forceinline__ void request(UnitRegs<KIND, CPL> &R, const LayerArgs 
 // Requests the first two units of the warp's share of groups [p0, p1).
 template <int KIND, int CPL>
 __device__ __forceinline__ void prime(UnitRegs<KIND, CPL> &A, UnitRegs<KIND, CPL> &B, const LayerArgs &a,
-                                      const int *uexp, int gpe, int p0, int p1, int &ex_u, DevExpert &ex) {
+                                      const int *uexp, int gpe, int p0, int p1, int &ex_u, DevExpert &ex,
+                                      const DevExpert *tab = nullptr) {
     const int n_my = units_of_warp<KIND>(p0, p1, threadIdx.x >> 5);
     ex_u = -1;
-    request<KIND, CPL>(A, a, uexp, gpe, p0, n_my, 0, ex_u, ex);
-    request<KIND, CPL>(B, a, uexp, gpe, p0, n_my, 1, ex_u, ex);
+    request<KIND, CPL>(A, a, uexp, gpe, p0, n_my, 0, ex_u, ex, tab);
+    request<KIND, CPL>(B, a, uexp, gpe, p0, n_my, 1, ex_u, ex, tab);
 }
 
 // Streams row groups [p0, p1) of a union view (gate/up: a gate row with the
@@ -166,10 +172,13 @@ __device__ __forceinline__ void prime(UnitRegs<KIND, CPL> &A, UnitRegs<KIND, CPL
 // activations (gate/up: the quantised tokens; down: h requantised from L2)
 // in the two-plane layout, then each warp multiplies its units while the
 // next one is in flight.  Must be called by all threads with the same range.
+// At one token, hset (when not null) receives the h values as data (each
+// value its own flag) and the down staging reads them from there.
 template <int KIND, int CPL, int MCH>
 __device__ __forceinline__ void stream_phase(const LayerArgs &a, DecodeSmem &sm, int8_t *xs, const int *uexp,
                                              const int *ubeg, int p0, int p1, UnitRegs<KIND, CPL> &A,
-                                             UnitRegs<KIND, CPL> &B, int &ex_u, DevExpert &ex, float *hset) {
+                                             UnitRegs<KIND, CPL> &B, int &ex_u, DevExpert &ex, float *hset,
+                                             const DevExpert *tab = nullptr) {
     constexpr int UPG = KIND == kGateUp ? 2 : 1, RPG = UnitShape<KIND, CPL>::kRows;
     // at one token every gate/up entry multiplies the same row (token 0),
     // staged once in xs / sm.sx[0] / sm.xsum[0] by the caller
@@ -182,6 +191,48 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, DecodeSmem &sm,
     const int nch = (kdim >> 1) >> 4;
     const int gpe = rows_out / RPG;
     const int n_my = units_of_warp<KIND>(p0, p1, warp);
+
+    if constexpr (kFixedX) {
+        // one token: one row per entry and nothing staged per entry, so
+        // each warp runs straight through the entries of its units, with no
+        // block barrier between entries (a group is a gate row and the same
+        // up row)
+        int held_g = 0;
+        float held_gs = 0.f;
+        auto process1 = [&](const UnitRegs<KIND, CPL> &R, int jj) {
+            const int p = p0 + warp + 8 * (jj / UPG), ue = p / gpe, o0 = p - ue * gpe;
+            int acc[1] = {0};
+            dot_rows<CPL, 1>(acc, R.w[0], xs, kdim, 1, nch, lane);
+            const int mine = lane_sum<1>(acc, 1, lane);
+            if (jj % UPG == 0) {
+                held_g = mine;
+                held_gs = R.s[0];
+            } else if (lane == 0) {
+                const int r0 = ubeg[ue];
+                const int gi = held_g - 8 * sm.xsum[0], ui = mine - 8 * sm.xsum[0];
+                const float gf = __fmul_rn(__fmul_rn((float)gi, sm.sx[0]), held_gs);
+                const float uf = __fmul_rn(__fmul_rn((float)ui, sm.sx[0]), R.s[0]);
+                const float hv = __fmul_rn(silu_f(gf), uf);
+                if (hset) {  // published as data: the down CTAs poll it
+                    const uint32_t bits = __float_as_uint(hv);
+                    st_relaxed_u32(hset + (size_t)r0 * a.I + o0, bits == kHEmpty ? 0x7FFFFFFFu : bits);
+                } else {
+                    a.h[(size_t)r0 * a.I + o0] = hv;
+                }
+                if (a.dbg.gate_acc) a.dbg.gate_acc[(size_t)sm.rows[r0] * a.I + o0] = gi;
+                if (a.dbg.up_acc) a.dbg.up_acc[(size_t)sm.rows[r0] * a.I + o0] = ui;
+            }
+        };
+        for (int j = 0; j < n_my;) {
+            process1(A, j);
+            request<KIND, CPL>(A, a, uexp, gpe, p0, n_my, j + 2, ex_u, ex, tab);
+            if (++j >= n_my) break;
+            process1(B, j);
+            request<KIND, CPL>(B, a, uexp, gpe, p0, n_my, j + 2, ex_u, ex, tab);
+            ++j;
+        }
+        return;
+    }
 
     int hsum = 0;          // lane m: code sum of the requantised h row m (down)
     int held_g = 0;        // lane m: gate sum waiting for its up row
@@ -309,12 +360,7 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, DecodeSmem &sm,
                     const float gf = __fmul_rn(__fmul_rn((float)gi, sm.sx[lane]), held_gs);
                     const float uf = __fmul_rn(__fmul_rn((float)ui, sm.sx[lane]), R.s[0]);
                     const float hv = __fmul_rn(silu_f(gf), uf);
-                    if (MCH == 1 && hset) {  // published as data: the down CTAs poll it
-                        const uint32_t bits = __float_as_uint(hv);
-                        st_relaxed_u32(hset + (size_t)(r0 + lane) * a.I + o0, bits == kHEmpty ? 0x7FFFFFFFu : bits);
-                    } else {
-                        a.h[(size_t)(r0 + lane) * a.I + o0] = hv;
-                    }
+                    a.h[(size_t)(r0 + lane) * a.I + o0] = hv;
                     if (a.dbg.gate_acc) a.dbg.gate_acc[(size_t)sm.ent[lane] * a.I + o0] = gi;
                     if (a.dbg.up_acc) a.dbg.up_acc[(size_t)sm.ent[lane] * a.I + o0] = ui;
                 }
@@ -341,11 +387,11 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, DecodeSmem &sm,
         auto run = [&](auto mm, UnitRegs<KIND, CPL> &X, UnitRegs<KIND, CPL> &Y) -> bool {
             while (in_seg(j)) {
                 process(mm, X, j);
-                request<KIND, CPL>(X, a, uexp, gpe, p0, n_my, j + 2, ex_u, ex);
+                request<KIND, CPL>(X, a, uexp, gpe, p0, n_my, j + 2, ex_u, ex, tab);
                 ++j;
                 if (!in_seg(j)) return true;
                 process(mm, Y, j);
-                request<KIND, CPL>(Y, a, uexp, gpe, p0, n_my, j + 2, ex_u, ex);
+                request<KIND, CPL>(Y, a, uexp, gpe, p0, n_my, j + 2, ex_u, ex, tab);
                 ++j;
             }
             return false;
@@ -606,6 +652,13 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
     const int n_kept = build_union(sm, T, K, S, E, a.n_shared);
     stamp(a, 5);
     const int n_r = sm.nu, n_u = n_r + a.n_shared;
+    // one token: the union entries' expert pointers go to shared memory, so
+    // that no warp's first request of an entry waits on a global load of them
+    const DevExpert *const tab = MCH == 1 ? sm.uexd : nullptr;
+    if (MCH == 1) {
+        if (tid < n_u) sm.uexd[tid] = a.experts[sm.uexp[tid]];
+        __syncthreads();
+    }
     if (b == 0) {  // the tables for the debug entry point and other readers
         for (int i = tid; i < n_sel; i += blockDim.x) {
             a.idx[i] = sm.idx[i];
@@ -656,8 +709,8 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
         dp0 = sm.slice[2];
         dp1 = sm.slice[3];
     }
-    prime<kGateUp, CPLG>(A, B, a, sm.uexp, I, rp0, rp1, ex_u, ex);
-    stream_phase<kGateUp, CPLG, MCH>(a, sm, xs, sm.uexp, sm.ubeg, rp0, rp1, A, B, ex_u, ex, hset);
+    prime<kGateUp, CPLG>(A, B, a, sm.uexp, I, rp0, rp1, ex_u, ex, tab);
+    stream_phase<kGateUp, CPLG, MCH>(a, sm, xs, sm.uexp, sm.ubeg, rp0, rp1, A, B, ex_u, ex, hset, tab);
     stamp(a, 6);
 
     // ---- phase 3.  More tokens: the CTA arrives, requests its first down
@@ -667,7 +720,7 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
     // until every value is there.
     UnitRegs<kDown, CPLD> A2, B2;
     if (hset) {
-        prime<kDown, CPLD>(A2, B2, a, sm.uexp, gpd, dp0, dp1, ex_u, ex);
+        prime<kDown, CPLD>(A2, B2, a, sm.uexp, gpd, dp0, dp1, ex_u, ex, tab);
     } else {
         cta_arrive(&sy->gu_cnt);
         prime<kDown, CPLD>(A2, B2, a, sm.uexp, gpd, dp0, dp1, ex_u, ex);
@@ -676,7 +729,7 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(LayerArgs a) {
         if (b == 0 && tid == 0) st_relaxed_u32(&a.dstate->epoch, sm.epoch + 1u);
     }
     stamp(a, 7);
-    stream_phase<kDown, CPLD, MCH>(a, sm, xs, sm.uexp, sm.ubeg, dp0, dp1, A2, B2, ex_u, ex, hset);
+    stream_phase<kDown, CPLD, MCH>(a, sm, xs, sm.uexp, sm.ubeg, dp0, dp1, A2, B2, ex_u, ex, hset, tab);
     stamp(a, 8);
     // the next kernel in the stream may launch once every CTA is here: its
     // prologue (weight requests) overlaps this grid's reduce and exit
