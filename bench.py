@@ -60,11 +60,13 @@ HOT_KERNEL_DECODE8 = "gateup_kernel<12,1,8> (int8 gate/up rows, SiLU*up, max abs
 HOT_KERNEL_PREFILL = ("umma_gemm_kernel<0, 1> (tcgen05 f16-exact gate/up GEMM, tokens x 256 weight rows per MMA, "
                       "packed weights by TMA, SiLU*up, max abs h)")
 # DRAM bytes (read + write) per launch of the dominant kernel from one ncu
-# capture of the current kernel source, or None.  Keyed by workload.
+# capture of the current kernel source, or None.  Keyed by workload; a
+# capture covers the workload's plain configuration only (int4 experts, plain
+# top-K, one layer per step), so the variants report None.
 TRAFFIC = {
-    # decode_layer_kernel on the full decode batch-1 workload (launch-list
-    # capture with the DRAM byte counters, 14 launches): 176.72 MB read +
-    # 0.30 MB written per launch
+    # decode_layer_kernel at decode batch 1 (DRAM byte counters of 3 launches,
+    # one resident GLM-shaped layer set, caches flushed before each):
+    # 176.72 MB read + 0.30 MB written per launch
     "glm_moe_layer_decode_b1": 177.02e6,
     # umma_gemm_kernel<0, 1> (gate/up, packed weights by TMA) at prefill 2048,
     # full capture of the profiling layout (16 physical experts aliased over
@@ -205,6 +207,14 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(loaded) if loaded else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows),
                 "samples_loaded": len(loaded)}
+
+
+def traffic_for(workload, top_p, wbits, stack, light):
+    """The captured DRAM bytes of the workload's dominant kernel when the run
+    is the configuration the capture covered, else None."""
+    if stack or light or wbits != 4 or 0.0 < top_p < 1.0:
+        return None
+    return TRAFFIC.get(workload)
 
 
 def measured_peak(kind="hbm_gbs"):
@@ -430,13 +440,14 @@ def run_ours(args, workload, rank, world, local, n_layers=None, steps=None, warm
     else:  # back-to-back launches of the one kernel: the gaps between them count
         probe_avg_ms, launches_timed = ms_per_step, K
     grouped = T > 16
+    traffic = traffic_for(workload, top_p, wbits, stack, args.light)
     if single:
         # one kernel is the whole layer: its algorithmic bytes are the step's
         peak, peak_kind = measured_peak("hbm_gbs")
         achieved = step_bytes_layer / (probe_avg_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "kernel": HOT_KERNEL_SINGLE, "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_kind": peak_kind + " HBM copy bandwidth",
-                "traffic": TRAFFIC.get(workload), "algorithmic_bytes_per_launch": step_bytes_layer,
+                "traffic": traffic, "algorithmic_bytes_per_launch": step_bytes_layer,
                 "avg_launch_ms": probe_avg_ms, "launches_timed": launches_timed}
     elif args.probe != "gateup":
         roof = {"bound": "hbm", "kernel": args.probe, "achieved": None, "peak": None, "unit": "GB/s",
@@ -447,7 +458,7 @@ def run_ours(args, workload, rank, world, local, n_layers=None, steps=None, warm
         roof = {"bound": "hbm", "kernel": HOT_KERNEL_DECODE if wbits == 4 else HOT_KERNEL_DECODE8,
                 "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_kind": peak_kind + " HBM copy bandwidth",
-                "traffic": TRAFFIC.get(workload), "algorithmic_bytes_per_launch": gu_bytes,
+                "traffic": traffic, "algorithmic_bytes_per_launch": gu_bytes,
                 "avg_launch_ms": probe_avg_ms, "launches_timed": launches_timed}
     else:
         # int8 ops of the gate/up GEMM: every routed (token, expert) pair and
@@ -462,7 +473,7 @@ def run_ours(args, workload, rank, world, local, n_layers=None, steps=None, warm
                 "unit": "TFLOP/s", "frac": achieved / peak,
                 "peak_kind": peak_kind + " dense bf16 (burst); sm_103a has no int8 tcgen05 kind, so the "
                              "densest tensor rate for these operands is the 16-bit one",
-                "traffic": TRAFFIC.get(workload), "algorithmic_ops_per_launch": ops,
+                "traffic": traffic, "algorithmic_ops_per_launch": ops,
                 "avg_launch_ms": probe_avg_ms, "launches_timed": launches_timed}
 
     # end to end through the C ABI: pinned host x -> device, forward, out -> pinned host
