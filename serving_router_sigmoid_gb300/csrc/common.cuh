@@ -13,7 +13,11 @@ constexpr int kMaxE = 512;        // routed experts per layer
 constexpr int kMaxK = 16;         // experts per token
 constexpr int kSmallT = 16;       // token count served by the fused small-batch router
 constexpr int kMaxDim = 8192;     // D and I upper bound (GEMV chunks per lane <= 8)
-constexpr int kRouterSplitK = 4;  // partial logit buffers of the large-batch router (K split)
+constexpr int kRouterSplitK = 9;  // partial logit buffers of the large-batch router (K split), at most
+// K ranges of the large-batch router at T tokens: 9 from 128 tokens on (the
+// 128 x 128 tiles alone would leave most SMs idle), else 4 (which keeps the
+// partial buffers of a small batch small)
+inline constexpr int router_splits(long long T) { return T >= 128 ? kRouterSplitK : 4; }
 
 // Device error word bits (moe_layer_device_status).
 constexpr int kErrNoSelection = 1;   // a token had no finite selection score left

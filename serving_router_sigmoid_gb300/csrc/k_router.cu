@@ -255,70 +255,92 @@ __global__ void __launch_bounds__(256) router_tile_kernel(const float *__restric
 
 // ------------------------------------------------ large-batch router (2 kernels)
 
-// Logits of a large batch as a register-tiled fp32 GEMM: CTA tile 64 tokens x
-// 64 experts, K in chunks of 32 through shared memory (stored k-major so a
-// thread reads 4 tokens and 4 experts as two float4), 256 threads each
-// accumulating 4 tokens x 4 experts with one fmaf chain per output in
-// ascending d.  The next chunk is loaded into registers while the current
-// one is multiplied.  K is split into gridDim.z contiguous ranges of whole
-// chunks (4 CTAs per tile: T = 2048 otherwise fills only 128 SMs, one CTA
-// each); range z writes its partial logits to logits + z T E and the select
-// kernel adds the partials in z order.  D % 32 == 0.
-constexpr int kRLT = 64, kRLE = 64, kRLK = 32;
-__global__ void __launch_bounds__(256) router_logits_kernel(const float *__restrict__ x, const float *__restrict__ Wr,
-                                                            int T, int D, int E, float *__restrict__ logits) {
+// Logits of a large batch as a register-tiled fp32 GEMM: CTA tile 128 tokens
+// x 128 experts, K in chunks of 16 through a 4-stage cp.async ring (rows kept
+// d-contiguous, so no transpose on the way in), 256 threads each
+// accumulating 8 tokens x 8 experts (rows ty + 16 i, columns tx + 16 j, which
+// keeps the shared-memory reads conflict-free) with one fmaf chain per output
+// in ascending d: per 4 d, 16 16-byte shared loads feed 256 fmaf.  One CTA
+// per SM.  K is split into gridDim.z contiguous ranges of whole chunks (at T
+// = 2048 the 32 tiles x 9 ranges make two waves of the 152 SMs); range z
+// writes its partial logits to logits + z T E and the select kernel adds the
+// partials in z order.  D % 16 == 0; rows past T or E read zeros.
+constexpr int kRLM = 128, kRLK = 16, kRLStages = 4, kRLPitch = kRLK + 4;  // floats per staged row
+constexpr size_t kRLStageFloats = 2 * (size_t)kRLM * kRLPitch;
+constexpr size_t kRLSmemBytes = kRLStages * kRLStageFloats * sizeof(float);
+
+__device__ __forceinline__ void rl_cp_async16(float *smem, const float *gmem, bool valid) {
+    // src-size 0 fills the 16 bytes with zeros (gmem stays a valid address)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(smem)),
+                 "l"(gmem), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+
+__global__ void __launch_bounds__(256, 1) router_logits_kernel(const float *__restrict__ x, const float *__restrict__ Wr,
+                                                               int T, int D, int E, float *__restrict__ logits) {
+    extern __shared__ __align__(16) float rls[];  // [kRLStages][2][kRLM][kRLPitch]
     const int nch = D / kRLK, z = blockIdx.z, nz = gridDim.z;
-    const int kb = (int)((long long)z * nch / nz) * kRLK, ke = (int)((long long)(z + 1) * nch / nz) * kRLK;
+    const int cb = (int)((long long)z * nch / nz), ce = (int)((long long)(z + 1) * nch / nz), n_c = ce - cb;
     logits += (size_t)z * T * E;
-    __shared__ __align__(16) float xs[kRLK][kRLT + 4];
-    __shared__ __align__(16) float ws[kRLK][kRLE + 4];
-    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-    const int t0 = blockIdx.x * kRLT, e0 = blockIdx.y * kRLE;
-    // loader: 64 rows x 32 floats per operand = 512 float4, two per thread
-    const int lr = tid >> 3, lc = (tid & 7) * 4;  // rows lr and lr + 32, float columns lc..lc+3
-    float acc[4][4];
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    const int m0 = blockIdx.x * kRLM, n0 = blockIdx.y * kRLM;
+    // copy q = tid + 256 i of a stage: operand q / 512 (x, Wr), row (q / 4) % 128, 16-byte segment q % 4
+    auto load_stage = [&](int stage, int chunk) {
+        float *st = rls + (size_t)stage * kRLStageFloats;
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-    auto ld = [&](const float *base, int row0, int nrows, int rstride, int r, int k0) {
-        const int row = row0 + r;
-        return row < nrows ? __ldg(reinterpret_cast<const float4 *>(base + (size_t)row * rstride + k0 + lc))
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
-    };
-    float4 xa = ld(x, t0, T, D, lr, kb), xb = ld(x, t0, T, D, lr + 32, kb);
-    float4 wa = ld(Wr, e0, E, D, lr, kb), wb = ld(Wr, e0, E, D, lr + 32, kb);
-    for (int k0 = kb; k0 < ke; k0 += kRLK) {
-        __syncthreads();
-        xs[lc + 0][lr] = xa.x; xs[lc + 1][lr] = xa.y; xs[lc + 2][lr] = xa.z; xs[lc + 3][lr] = xa.w;
-        xs[lc + 0][lr + 32] = xb.x; xs[lc + 1][lr + 32] = xb.y; xs[lc + 2][lr + 32] = xb.z; xs[lc + 3][lr + 32] = xb.w;
-        ws[lc + 0][lr] = wa.x; ws[lc + 1][lr] = wa.y; ws[lc + 2][lr] = wa.z; ws[lc + 3][lr] = wa.w;
-        ws[lc + 0][lr + 32] = wb.x; ws[lc + 1][lr + 32] = wb.y; ws[lc + 2][lr + 32] = wb.z; ws[lc + 3][lr + 32] = wb.w;
-        __syncthreads();
-        if (k0 + kRLK < ke) {  // the next chunk travels while this one is multiplied
-            xa = ld(x, t0, T, D, lr, k0 + kRLK);
-            xb = ld(x, t0, T, D, lr + 32, k0 + kRLK);
-            wa = ld(Wr, e0, E, D, lr, k0 + kRLK);
-            wb = ld(Wr, e0, E, D, lr + 32, k0 + kRLK);
+        for (int i = 0; i < 4; ++i) {
+            const int q = tid + 256 * i, op = q >> 9, row = (q >> 2) & (kRLM - 1), seg = q & 3;
+            const int g = (op == 0 ? m0 : n0) + row, lim = op == 0 ? T : E;
+            const float *src = (op == 0 ? x : Wr) + (size_t)(g < lim ? g : lim - 1) * D + chunk * kRLK + seg * 4;
+            rl_cp_async16(st + (size_t)op * kRLM * kRLPitch + row * kRLPitch + seg * 4, src, g < lim);
         }
+    };
+    float acc[8][8];
 #pragma unroll
-        for (int k = 0; k < kRLK; ++k) {
-            const float4 xv = *reinterpret_cast<const float4 *>(&xs[k][ty * 4]);
-            const float4 wv = *reinterpret_cast<const float4 *>(&ws[k][tx * 4]);
-            const float xr[4] = {xv.x, xv.y, xv.z, xv.w}, wr[4] = {wv.x, wv.y, wv.z, wv.w};
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xr[i], wr[j], acc[i][j]);
+    for (int s = 0; s < kRLStages - 1; ++s) {
+        if (s < n_c) load_stage(s, cb + s);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    for (int c = 0; c < n_c; ++c) {
+        // chunk c has landed (every later group may still be in flight), and
+        // every thread is done with chunk c - 1, whose stage is refilled now
+        asm volatile("cp.async.wait_group %0;" ::"n"(kRLStages - 2) : "memory");
+        __syncthreads();
+        if (c + kRLStages - 1 < n_c) load_stage((c + kRLStages - 1) % kRLStages, cb + c + kRLStages - 1);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        const float *As = rls + (size_t)(c % kRLStages) * kRLStageFloats, *Bs = As + kRLM * kRLPitch;
+#pragma unroll
+        for (int kk = 0; kk < kRLK; kk += 4) {
+            float4 av[8], bv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) av[i] = *reinterpret_cast<const float4 *>(As + (ty + 16 * i) * kRLPitch + kk);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) bv[j] = *reinterpret_cast<const float4 *>(Bs + (tx + 16 * j) * kRLPitch + kk);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    float v = acc[i][j];
+                    v = fmaf(av[i].x, bv[j].x, v);
+                    v = fmaf(av[i].y, bv[j].y, v);
+                    v = fmaf(av[i].z, bv[j].z, v);
+                    v = fmaf(av[i].w, bv[j].w, v);
+                    acc[i][j] = v;
+                }
         }
     }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int t = t0 + ty * 4 + i;
+    for (int i = 0; i < 8; ++i) {
+        const int t = m0 + ty + 16 * i;
         if (t >= T) continue;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int e = e0 + tx * 4 + j;
+        for (int j = 0; j < 8; ++j) {
+            const int e = n0 + tx + 16 * j;
             if (e < E) logits[(size_t)t * E + e] = acc[i][j];
         }
     }
@@ -478,10 +500,13 @@ static cudaError_t launch_select_t(const float *logits, int nz, const float *bia
 cudaError_t launch_router_gemm(const float *x, const float *Wr, const float *bias, int T, int D, int E, int K,
                                float scale, float top_p, float *logits, int32_t *idx, float *w, int32_t *err,
                                cudaStream_t s) {
-    const int nz = D / kRLK < kRouterSplitK ? D / kRLK : kRouterSplitK;
-    router_logits_kernel<<<dim3((T + kRLT - 1) / kRLT, (E + kRLE - 1) / kRLE, nz), 256, 0, s>>>(x, Wr, T, D, E,
-                                                                                                logits);
-    cudaError_t ce = cudaGetLastError();
+    const int nz = D / kRLK < router_splits(T) ? D / kRLK : router_splits(T);
+    cudaError_t ce = cudaFuncSetAttribute(router_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)kRLSmemBytes);
+    if (ce != cudaSuccess) return ce;
+    router_logits_kernel<<<dim3((T + kRLM - 1) / kRLM, (E + kRLM - 1) / kRLM, nz), 256, kRLSmemBytes, s>>>(
+        x, Wr, T, D, E, logits);
+    ce = cudaGetLastError();
     if (ce != cudaSuccess) return ce;
     switch (epl_for(E)) {
         case 1: return launch_select_t<1>(logits, nz, bias, T, E, K, scale, top_p, idx, w, err, s);

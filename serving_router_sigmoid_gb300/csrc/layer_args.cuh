@@ -20,7 +20,7 @@ struct LayerArgs {
     int8_t *xq;          // [Tmax, D] int8, even/odd permuted 8-groups
     float *sx;           // [Tmax]
     int32_t *xsum;       // [Tmax] sum of xq over the row
-    float *logits;       // [kRouterSplitK, max(kSmallT, Tmax), E] (partials of the large-batch router)
+    float *logits;       // [router_splits(Tmax), max(kSmallT, Tmax), E] (partials of the large-batch router)
     int32_t *idx;        // [Tmax, K]
     float *wts;          // [Tmax, K]
     int32_t *rows;       // [Tmax * S] entry ids (t*S + slot) grouped by union expert

@@ -98,8 +98,8 @@ size_t layout(const MoeLayerDesc &d, Handle *h) {
     const size_t o_xq = take(T * D);
     const size_t o_sx = take(4 * T);
     const size_t o_xsum = take(4 * T);
-    const size_t o_logits = take(4 * moe::kRouterSplitK * (T > (size_t)moe::kSmallT ? T : (size_t)moe::kSmallT) *
-                                 E);
+    const size_t o_logits =
+        take(4 * moe::router_splits((long long)T) * (T > (size_t)moe::kSmallT ? T : (size_t)moe::kSmallT) * E);
     const size_t o_idx = take(4 * T * K);
     const size_t o_wts = take(4 * T * K);
     const size_t o_rows = take(4 * T * S);
