@@ -25,9 +25,10 @@
 // the hardware e4m3x2 -> f16x2 conversion (exact: every E4M3 value is an f16
 // value), then f16 -> f32 (exact).  The packer's division is replaced, where
 // that provably gives the same code, by a product with the row's reciprocal
-// (nibble_fast); a chunk with a quotient near a tie is redone exactly.  Rows
-// that are not a multiple of 16 codes, longer than 8192 or unaligned take a
-// plain per-element path with the packer's arithmetic.
+// (nibble2_fast, two codes per packed f32x2 instruction); a chunk with a
+// quotient near a tie is redone exactly.  Rows that are not a multiple of 16
+// codes, longer than 8192 or unaligned take a plain per-element path with the
+// packer's arithmetic.
 #include "layer_args.cuh"
 
 namespace moe {
@@ -55,8 +56,30 @@ __device__ __forceinline__ uint32_t nibble_of(float w, float s) {
     return (uint32_t)(min(7, max(-8, v)) + 8);
 }
 
-// The same code without the division, where that provably gives the same
-// result.  With inv = fl(1/s) and g = fl(sc * inv), y = fl(v * g) differs
+// Two fp32 lanes in one 64-bit register pair (.x low), and the packed
+// two-lane IEEE operations of sm_100 and later: each lane is rounded to
+// nearest exactly as the scalar operation would round it.
+__device__ __forceinline__ unsigned long long f32x2_of(float lo, float hi) {
+    return ((unsigned long long)__float_as_uint(hi) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ unsigned long long mul_f32x2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long add_f32x2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long sub_f32x2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// The packer's code without the division, where that provably gives the
+// same result.  With inv = fl(1/s) and g = fl(sc * inv), y = fl(v * g) differs
 // from the packer's quotient fl(fl(v * sc) / s) by at most five roundings of
 // relative size 2^-24 of a quotient whose magnitude is at most 7 (|w| <= amax,
 // s >= amax/7 rounded): less than 2^-18.  So when y lies farther than 2^-17
@@ -66,29 +89,27 @@ __device__ __forceinline__ uint32_t nibble_of(float w, float s) {
 // sum (|nearest(y)| <= 7, so no borrow or carry leaves the nibble).  `near`
 // is set when y lies within 2^-17 of a half-integer: the caller then forms
 // the quotient exactly as the packer does.
-__device__ __forceinline__ uint32_t nibble_fast(float v, float g, bool &near) {
-    constexpr float kM = 12582920.f;  // 1.5 * 2^23 + 8
-    const float y = __fmul_rn(v, g);
-    const float z = __fadd_rn(y, kM);
-    const float r = __fsub_rn(y, __fsub_rn(z, kM));  // y - nearest(y), exact
-    near |= fabsf(r) >= 0.5f - 7.62939453125e-06f;
-    return __float_as_uint(z) & 15u;
+// Here for the two codes of v at once (v.x's nibble in bits 0..3, v.y's in
+// bits 4..7); g2 and m2 hold g and M in both lanes.
+__device__ __forceinline__ uint32_t nibble2_fast(float2 v, unsigned long long g2, unsigned long long m2, bool &near) {
+    const unsigned long long y = mul_f32x2(f32x2_of(v.x, v.y), g2);
+    const unsigned long long z = add_f32x2(y, m2);
+    const unsigned long long r = sub_f32x2(y, sub_f32x2(z, m2));  // y - nearest(y), exact
+    const float r0 = __uint_as_float((uint32_t)r), r1 = __uint_as_float((uint32_t)(r >> 32));
+    near |= fmaxf(fabsf(r0), fabsf(r1)) >= 0.5f - 7.62939453125e-06f;
+    return ((uint32_t)z & 15u) | (((uint32_t)(z >> 32) & 15u) << 4);
 }
 
-// Packed bytes of one 16-code chunk (4 words, element 2j low nibble).
+// Packed bytes of one 16-code chunk (4 words, element 2j low nibble): per
+// word, its four codes' nibbles in 16 bits.
 __device__ __forceinline__ uint2 pack_chunk_fast(uint4 c, float g, bool &near) {
-    uint32_t out[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const uint32_t w0 = h ? c.z : c.x, w1 = h ? c.w : c.y;
-        const float2 a = e4m3x2_to_f32x2(w0 & 0xFFFFu), b = e4m3x2_to_f32x2(w0 >> 16);
-        const float2 d = e4m3x2_to_f32x2(w1 & 0xFFFFu), e = e4m3x2_to_f32x2(w1 >> 16);
-        out[h] = nibble_fast(a.x, g, near) | (nibble_fast(a.y, g, near) << 4) | (nibble_fast(b.x, g, near) << 8) |
-                 (nibble_fast(b.y, g, near) << 12) | (nibble_fast(d.x, g, near) << 16) |
-                 (nibble_fast(d.y, g, near) << 20) | (nibble_fast(e.x, g, near) << 24) |
-                 (nibble_fast(e.y, g, near) << 28);
-    }
-    return make_uint2(out[0], out[1]);
+    constexpr float kM = 12582920.f;  // 1.5 * 2^23 + 8 (nibble2_fast)
+    const unsigned long long g2 = f32x2_of(g, g), m2 = f32x2_of(kM, kM);
+    auto word = [&](uint32_t w) {
+        return nibble2_fast(e4m3x2_to_f32x2(w & 0xFFFFu), g2, m2, near) |
+               (nibble2_fast(e4m3x2_to_f32x2(w >> 16), g2, m2, near) << 8);
+    };
+    return make_uint2(word(c.x) | (word(c.y) << 16), word(c.z) | (word(c.w) << 16));
 }
 
 // The packer's arithmetic for a whole chunk (rare: a quotient near a tie).
