@@ -14,20 +14,23 @@ namespace moe {
 
 // out[t] = (resid[t] +) sum_k w[t,k] * y[t,k] + y[t,shared], slots in order
 // (slots adaptive top-p dropped are skipped).
-// Every slot's value is loaded before the first add (K <= kMaxK).
+// Every slot's value is loaded before the first add (K <= KB: the register
+// arrays hold KB routed slots, so a layer with a small K keeps the
+// occupancy high enough for the loads in flight this HBM-bound step needs).
+template <int KB>
 __global__ void __launch_bounds__(256) reduce_kernel(LayerArgs a) {
     const int t = blockIdx.y;
     const int o = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
     if (o >= a.D) return;
     const int K = a.K, S = a.S, D = a.D;
     const float *pt = a.part + (size_t)t * S * D + o;
-    float4 y[kMaxK + 1];
-    float wk[kMaxK];
-    bool kept[kMaxK];  // a slot top-p dropped has no expert output
+    float4 y[KB + 1];
+    float wk[KB];
+    bool kept[KB];  // a slot top-p dropped has no expert output
 #pragma unroll
-    for (int k = 0; k <= kMaxK; ++k) {
+    for (int k = 0; k <= KB; ++k) {
         if (k < S) y[k] = *reinterpret_cast<const float4 *>(pt + (size_t)k * D);
-        if (k < K && k < kMaxK) {
+        if (k < K && k < KB) {
             wk[k] = a.wts[t * K + k];
             kept[k] = a.idx[t * K + k] != kDroppedSel;
         }
@@ -36,7 +39,7 @@ __global__ void __launch_bounds__(256) reduce_kernel(LayerArgs a) {
     if (a.resid) r = *reinterpret_cast<const float4 *>(a.resid + (size_t)t * D + o);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int k = 0; k < kMaxK; ++k) {
+    for (int k = 0; k < KB; ++k) {
         if (k < K && kept[k]) {
             acc.x = __fadd_rn(acc.x, __fmul_rn(wk[k], y[k].x));
             acc.y = __fadd_rn(acc.y, __fmul_rn(wk[k], y[k].y));
@@ -46,7 +49,7 @@ __global__ void __launch_bounds__(256) reduce_kernel(LayerArgs a) {
     }
     if (a.n_shared) {
 #pragma unroll
-        for (int k = 0; k <= kMaxK; ++k) {
+        for (int k = 0; k <= KB; ++k) {
             if (k == K) {
                 acc.x = __fadd_rn(acc.x, y[k].x);
                 acc.y = __fadd_rn(acc.y, y[k].y);
@@ -190,7 +193,12 @@ cudaError_t launch_down(const LayerArgs &a, int mch, int grid, bool fused, cudaS
 
 cudaError_t launch_reduce(const LayerArgs &a, cudaStream_t s) {
     dim3 grid((a.D / 4 + 255) / 256, a.T);
-    reduce_kernel<<<grid, 256, 0, s>>>(a);
+    if (a.K <= 4)
+        reduce_kernel<4><<<grid, 256, 0, s>>>(a);
+    else if (a.K <= 8)
+        reduce_kernel<8><<<grid, 256, 0, s>>>(a);
+    else
+        reduce_kernel<kMaxK><<<grid, 256, 0, s>>>(a);
     return cudaGetLastError();
 }
 
