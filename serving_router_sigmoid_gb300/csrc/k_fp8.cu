@@ -89,27 +89,37 @@ __device__ __forceinline__ unsigned long long sub_f32x2(unsigned long long a, un
 // sum (|nearest(y)| <= 7, so no borrow or carry leaves the nibble).  `near`
 // is set when y lies within 2^-17 of a half-integer: the caller then forms
 // the quotient exactly as the packer does.
-// Here for the two codes of v at once (v.x's nibble in bits 0..3, v.y's in
-// bits 4..7); g2 and m2 hold g and M in both lanes.
-__device__ __forceinline__ uint32_t nibble2_fast(float2 v, unsigned long long g2, unsigned long long m2, bool &near) {
+// Here for the two codes of v at once: returns the two sums z (lane x in
+// the low word), whose low bytes are 8 + nearest(y) (0..15: the nibbles);
+// rmax collects max |y - nearest(y)|.  g2 and m2 hold g and M in both lanes.
+__device__ __forceinline__ unsigned long long nibble2_fast(float2 v, unsigned long long g2, unsigned long long m2,
+                                                           float &rmax) {
     const unsigned long long y = mul_f32x2(f32x2_of(v.x, v.y), g2);
     const unsigned long long z = add_f32x2(y, m2);
     const unsigned long long r = sub_f32x2(y, sub_f32x2(z, m2));  // y - nearest(y), exact
-    const float r0 = __uint_as_float((uint32_t)r), r1 = __uint_as_float((uint32_t)(r >> 32));
-    near |= fmaxf(fabsf(r0), fabsf(r1)) >= 0.5f - 7.62939453125e-06f;
-    return ((uint32_t)z & 15u) | (((uint32_t)(z >> 32) & 15u) << 4);
+    rmax = fmaxf(rmax, fmaxf(fabsf(__uint_as_float((uint32_t)r)), fabsf(__uint_as_float((uint32_t)(r >> 32)))));
+    return z;
 }
 
-// Packed bytes of one 16-code chunk (4 words, element 2j low nibble): per
-// word, its four codes' nibbles in 16 bits.
+// Packed bytes of one 16-code chunk (4 words, element 2j low nibble).  Per
+// word, the four sums' low bytes are gathered into one word [n0 n1 n2 n3]
+// (byte permutes); q | q >> 4 then holds n0 | n1 << 4 in byte 0 and
+// n2 | n3 << 4 in byte 2, and a last permute joins two words' bytes 0 and 2.
+// near is set when a quotient lies within 2^-17 of a half-integer.
 __device__ __forceinline__ uint2 pack_chunk_fast(uint4 c, float g, bool &near) {
     constexpr float kM = 12582920.f;  // 1.5 * 2^23 + 8 (nibble2_fast)
     const unsigned long long g2 = f32x2_of(g, g), m2 = f32x2_of(kM, kM);
+    float rmax = 0.f;
     auto word = [&](uint32_t w) {
-        return nibble2_fast(e4m3x2_to_f32x2(w & 0xFFFFu), g2, m2, near) |
-               (nibble2_fast(e4m3x2_to_f32x2(w >> 16), g2, m2, near) << 8);
+        const unsigned long long za = nibble2_fast(e4m3x2_to_f32x2(w & 0xFFFFu), g2, m2, rmax);
+        const unsigned long long zb = nibble2_fast(e4m3x2_to_f32x2(w >> 16), g2, m2, rmax);
+        const uint32_t q = __byte_perm(__byte_perm((uint32_t)za, (uint32_t)(za >> 32), 0x0040),
+                                       __byte_perm((uint32_t)zb, (uint32_t)(zb >> 32), 0x0040), 0x5410);
+        return q | (q >> 4);
     };
-    return make_uint2(word(c.x) | (word(c.y) << 16), word(c.z) | (word(c.w) << 16));
+    const uint32_t t0 = word(c.x), t1 = word(c.y), t2 = word(c.z), t3 = word(c.w);
+    near = rmax >= 0.5f - 7.62939453125e-06f;
+    return make_uint2(__byte_perm(t0, t1, 0x6420), __byte_perm(t2, t3, 0x6420));
 }
 
 // The packer's arithmetic for a whole chunk (rare: a quotient near a tie).

@@ -387,16 +387,29 @@ __global__ void __launch_bounds__(1024) permute_large_kernel(LayerArgs a) {
     const int L = (((n + 31) / 32) + 31) & ~31;  // per-warp slice, a multiple of 32
     const int beg = warp * L, end = min(n, beg + L);
     const unsigned lt = (1u << lane) - 1u;
-    for (int g = beg; g < end; g += 32) {
-        const int i = g + lane;
-        const bool v = i < end;
-        int e = v ? a.idx[i] : -1;
-        const bool kept = v && e != kDroppedSel;  // a selection top-p dropped takes no row
-        if (kept && (e < 0 || e >= E)) { e = 0; atomicOr(a.err, kErrRouteCount); }
-        if (!kept) e = -1;
-        const unsigned m = __match_any_sync(0xffffffffu, e);
-        if (kept && __popc(m & lt) == 0) hist[warp * E + e] += __popc(m);
-        __syncwarp();
+    // the warp's selections kPB steps of 32 at a time, all loads of a batch
+    // issued before the first is used; e = -1 for none or a dropped one
+    constexpr int kPB = 16;
+    auto load_batch = [&](int g0, int (&ev)[kPB]) {
+#pragma unroll
+        for (int j = 0; j < kPB; ++j) {
+            const int i = g0 + 32 * j + lane;
+            ev[j] = i < end ? __ldg(a.idx + i) : kDroppedSel;
+        }
+    };
+    for (int g0 = beg; g0 < end; g0 += 32 * kPB) {
+        int ev[kPB];
+        load_batch(g0, ev);
+#pragma unroll
+        for (int j = 0; j < kPB; ++j) {
+            int e = ev[j];
+            const bool kept = e != kDroppedSel;  // a selection top-p dropped takes no row
+            if (kept && (e < 0 || e >= E)) { e = 0; atomicOr(a.err, kErrRouteCount); }
+            if (!kept) e = -1;
+            const unsigned m = __match_any_sync(0xffffffffu, e);
+            if (kept && __popc(m & lt) == 0) hist[warp * E + e] += __popc(m);
+            __syncwarp();
+        }
     }
     __syncthreads();
     for (int e = tid; e < E; e += blockDim.x) {
@@ -431,19 +444,23 @@ __global__ void __launch_bounds__(1024) permute_large_kernel(LayerArgs a) {
     }
     for (int i = tid; i < 32 * E; i += blockDim.x) hist[i] += base[i % E];
     __syncthreads();
-    for (int g = beg; g < end; g += 32) {
-        const int i = g + lane;
-        const bool v = i < end;
-        int e = v ? a.idx[i] : -1;
-        const bool kept = v && e != kDroppedSel;
-        if (kept && (e < 0 || e >= E)) e = 0;
-        if (!kept) e = -1;
-        const unsigned m = __match_any_sync(0xffffffffu, e);
-        const int rank = __popc(m & lt);
-        if (kept) a.rows[hist[warp * E + e] + rank] = (i / K) * S + (i % K);
-        __syncwarp();
-        if (kept && rank == 0) hist[warp * E + e] += __popc(m);
-        __syncwarp();
+    for (int g0 = beg; g0 < end; g0 += 32 * kPB) {
+        int ev[kPB];
+        load_batch(g0, ev);
+#pragma unroll
+        for (int j = 0; j < kPB; ++j) {
+            const int i = g0 + 32 * j + lane;
+            int e = ev[j];
+            const bool kept = e != kDroppedSel;
+            if (kept && (e < 0 || e >= E)) e = 0;
+            if (!kept) e = -1;
+            const unsigned m = __match_any_sync(0xffffffffu, e);
+            const int rank = __popc(m & lt);
+            if (kept) a.rows[hist[warp * E + e] + rank] = (i / K) * S + (i % K);
+            __syncwarp();
+            if (kept && rank == 0) hist[warp * E + e] += __popc(m);
+            __syncwarp();
+        }
     }
     if (a.n_shared)
         for (int t = tid; t < T; t += blockDim.x) a.rows[n_kept + t] = t * S + K;
