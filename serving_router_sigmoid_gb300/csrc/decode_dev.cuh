@@ -250,9 +250,7 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, DecodeSmem &sm,
         }
         if (threadIdx.x < M) sm.ent[threadIdx.x] = sm.rows[r0 + threadIdx.x];
         __syncthreads();
-        if (kFixedX) {
-            // one token: the tile, its scale and code sum were staged once
-        } else if (KIND == kGateUp) {
+        if (KIND == kGateUp) {  // (one token took the path above)
             if (threadIdx.x < M) {
                 const int t = sm.ent[threadIdx.x] / S;
                 sm.xsum[threadIdx.x] = __ldcg(a.xsum + t);

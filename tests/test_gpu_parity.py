@@ -193,6 +193,7 @@ SMALL_CASES = [
     dict(D=1056, I=96, E=40, K=5, n_shared=0, T=9),    # ragged chunk counts, no shared expert
     dict(D=512, I=1024, E=8, K=8, n_shared=1, T=3),    # K = E
     dict(D=512, I=256, E=300, K=16, n_shared=1, T=2),  # E > 256, K = 16
+    dict(D=512, I=256, E=300, K=16, n_shared=1, T=20),  # K = 16 above the decode sizes: partial router tiles
     dict(D=1056, I=96, E=40, K=5, n_shared=0, T=24),   # batch > 16 on shapes the grouped tiles skip
     dict(D=512, I=256, E=8, K=2, n_shared=1, T=300),   # several token blocks per expert
 ]
