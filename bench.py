@@ -513,7 +513,9 @@ def run_ours(args, workload, rank, world, local, n_layers=None, steps=None, warm
         e_ms = max_over_ranks(e_ms, world, dev)
         e2e = {"value": T * Ke * world / (e_ms / 1e3), "unit": UNIT, "steps": Ke,
                "h2d_bytes_per_step": T * cfg.D * 4, "d2h_bytes_per_step": T * cfg.D * 4,
-               "api": "moe_block_forward" if stack else "moe_layer_forward_host", "graph": False}
+               "api": "moe_block_forward" if stack else "moe_layer_forward_host", "graph": False,
+               "d2h": ("copy" if stack or T > 16 else
+                       "the kernel's stores into the page-locked output (no copy after the forward)")}
 
     cpu = None
     if rank == 0 and with_cpu and not args.no_cpu_baseline:

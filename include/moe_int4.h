@@ -215,9 +215,12 @@ int moe_layer_forward(void *handle, const float *x, int n_tokens, float *out,
  * out).
  *   x_host   host [n_tokens, D] fp32;  out_host host [n_tokens, D] fp32 out
  *   Page-locked host memory lets the copies run asynchronously; with
- *   pageable memory CUDA performs them synchronously.  The staging rows are
- *   part of the handle (one forward at a time per handle, as for
- *   moe_layer_forward); 0 <= n_tokens <= max_tokens.
+ *   pageable memory CUDA performs them synchronously.  At decode sizes
+ *   (n_tokens <= 16) a page-locked, device-addressable, 16-byte aligned
+ *   out_host receives the output rows directly from the kernel's stores, and
+ *   no copy back is enqueued.  The staging rows are part of the handle (one
+ *   forward at a time per handle, as for moe_layer_forward);
+ *   0 <= n_tokens <= max_tokens.
  * Errors: INVALID_ARG, SHAPE, CUDA.
  */
 int moe_layer_forward_host(void *handle, const float *x_host, int n_tokens, float *out_host,

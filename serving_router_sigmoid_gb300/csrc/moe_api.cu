@@ -524,10 +524,22 @@ int moe_layer_forward_host(void *handle, const float *x_host, int n_tokens, floa
     int rc = check_forward(h, h->xnorm, n_tokens, h->xout);
     if (rc) return rc;
     const size_t bytes = sizeof(float) * (size_t)n_tokens * h->d.D;
+    // decode sizes: a page-locked out_host that the device can address takes
+    // the output rows straight from the kernel's stores (no copy after the
+    // forward); otherwise the rows are staged in the handle and copied back
+    float *out_dev = nullptr;
+    if (n_tokens <= moe::kSmallT) {
+        cudaPointerAttributes pa;
+        if (cudaPointerGetAttributes(&pa, out_host) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
+            pa.devicePointer && aligned16(pa.devicePointer))
+            out_dev = static_cast<float *>(pa.devicePointer);
+        else
+            (void)cudaGetLastError();  // a pageable pointer is not an error here
+    }
     cudaError_t ce = cudaMemcpyAsync(h->xnorm, x_host, bytes, cudaMemcpyHostToDevice, stream);
     if (ce != cudaSuccess) return cuda_fail(ce, "copy of x to the device");
-    rc = run_layer(h, h->xnorm, n_tokens, h->xout, nullptr, moe::DebugPtrs{}, stream);
-    if (rc) return rc;
+    rc = run_layer(h, h->xnorm, n_tokens, out_dev ? out_dev : h->xout, nullptr, moe::DebugPtrs{}, stream);
+    if (rc || out_dev) return rc;
     ce = cudaMemcpyAsync(out_host, h->xout, bytes, cudaMemcpyDeviceToHost, stream);
     if (ce != cudaSuccess) return cuda_fail(ce, "copy of out to the host");
     return MOE_OK;
