@@ -298,44 +298,78 @@ __global__ void __launch_bounds__(256) grouped_gemm_kernel(LayerArgs a) {
 
 // Requantise every grouped h row to int8 (the activation quantiser of [A] §12
 // with the row max|h| of the gate/up pass) in the even/odd lane layout, with
-// the row code sum and scale.  One CTA per grouped row.
+// the row code sum and scale.  kRQ grouped rows per CTA, every row's loads of
+// a pass issued before the first is used (a CTA per row left each thread one
+// row's loads in flight).
+constexpr int kRQ = 4;
 __global__ void __launch_bounds__(256) requant_h_kernel(LayerArgs a) {
-    __shared__ int red_i[32];
-    const int r = blockIdx.x;
+    __shared__ int red_i[kRQ][8];
     // grouped rows of this batch: T*S, fewer when adaptive top-p dropped selections
-    if (r >= a.meta->ubeg[a.meta->n_union]) return;
-    const int I = a.I;
-    float s, inv;
-    act_scale(__uint_as_float(a.hamax[r]), s, inv);
-    const int ent = a.rows[r];
-    int sum = 0;
+    const int n_rows = a.meta->ubeg[a.meta->n_union];
+    const int I = a.I, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r0 = blockIdx.x * kRQ;
+    if (r0 >= n_rows) return;
+    float sc[kRQ], inv[kRQ];
+    int sum[kRQ], ent[kRQ];
+#pragma unroll
+    for (int j = 0; j < kRQ; ++j) {
+        const bool ok = r0 + j < n_rows;
+        act_scale(ok ? __uint_as_float(a.hamax[r0 + j]) : 0.f, sc[j], inv[j]);
+        ent[j] = ok ? a.rows[r0 + j] : 0;
+        sum[j] = 0;
+    }
     for (int gi = threadIdx.x; gi < (I >> 3); gi += blockDim.x) {
-        const float *hp = a.h + (size_t)r * I + 8 * gi;
-        const float4 v0 = *reinterpret_cast<const float4 *>(hp), v1 = *reinterpret_cast<const float4 *>(hp + 4);
-        const int q0 = quant_i8(v0.x, inv), q1 = quant_i8(v0.y, inv), q2 = quant_i8(v0.z, inv),
-                  q3 = quant_i8(v0.w, inv), q4 = quant_i8(v1.x, inv), q5 = quant_i8(v1.y, inv),
-                  q6 = quant_i8(v1.z, inv), q7 = quant_i8(v1.w, inv);
-        sum += q0 + q1 + q2 + q3 + q4 + q5 + q6 + q7;
-        const uint32_t ev = (q0 & 255) | ((q2 & 255) << 8) | ((q4 & 255) << 16) | ((uint32_t)(q6 & 255) << 24);
-        const uint32_t od = (q1 & 255) | ((q3 & 255) << 8) | ((q5 & 255) << 16) | ((uint32_t)(q7 & 255) << 24);
-        *reinterpret_cast<uint2 *>(a.hq + (size_t)r * I + 8 * gi) = make_uint2(ev, od);
-        if (a.xf) {  // the tcgen05 GEMM's operand: the same codes as f16 integers, same order
-            auto h2 = [](int lo, int hi) {
-                return (uint32_t)__half_as_ushort(__int2half_rn(lo)) | ((uint32_t)__half_as_ushort(__int2half_rn(hi)) << 16);
-            };
-            *reinterpret_cast<uint4 *>(a.xf + (size_t)r * I + 8 * gi) = make_uint4(h2(q0, q2), h2(q4, q6), h2(q1, q3), h2(q5, q7));
+        float4 v0[kRQ], v1[kRQ];
+#pragma unroll
+        for (int j = 0; j < kRQ; ++j) {
+            if (r0 + j < n_rows) {
+                const float *hp = a.h + (size_t)(r0 + j) * I + 8 * gi;
+                v0[j] = *reinterpret_cast<const float4 *>(hp);
+                v1[j] = *reinterpret_cast<const float4 *>(hp + 4);
+            }
         }
-        if (a.dbg.hq) {
-            const uint32_t n0 = (q0 & 255) | ((q1 & 255) << 8) | ((q2 & 255) << 16) | ((uint32_t)(q3 & 255) << 24);
-            const uint32_t n1 = (q4 & 255) | ((q5 & 255) << 8) | ((q6 & 255) << 16) | ((uint32_t)(q7 & 255) << 24);
-            *reinterpret_cast<uint2 *>(a.dbg.hq + (size_t)ent * I + 8 * gi) = make_uint2(n0, n1);
+#pragma unroll
+        for (int j = 0; j < kRQ; ++j) {
+            if (r0 + j >= n_rows) continue;
+            const int r = r0 + j;
+            const float iv = inv[j];
+            const int q0 = quant_i8(v0[j].x, iv), q1 = quant_i8(v0[j].y, iv), q2 = quant_i8(v0[j].z, iv),
+                      q3 = quant_i8(v0[j].w, iv), q4 = quant_i8(v1[j].x, iv), q5 = quant_i8(v1[j].y, iv),
+                      q6 = quant_i8(v1[j].z, iv), q7 = quant_i8(v1[j].w, iv);
+            sum[j] += q0 + q1 + q2 + q3 + q4 + q5 + q6 + q7;
+            const uint32_t ev = (q0 & 255) | ((q2 & 255) << 8) | ((q4 & 255) << 16) | ((uint32_t)(q6 & 255) << 24);
+            const uint32_t od = (q1 & 255) | ((q3 & 255) << 8) | ((q5 & 255) << 16) | ((uint32_t)(q7 & 255) << 24);
+            *reinterpret_cast<uint2 *>(a.hq + (size_t)r * I + 8 * gi) = make_uint2(ev, od);
+            if (a.xf) {  // the tcgen05 GEMM's operand: the same codes as f16 integers, same order
+                auto h2 = [](int lo, int hi) {
+                    return (uint32_t)__half_as_ushort(__int2half_rn(lo)) | ((uint32_t)__half_as_ushort(__int2half_rn(hi)) << 16);
+                };
+                *reinterpret_cast<uint4 *>(a.xf + (size_t)r * I + 8 * gi) =
+                    make_uint4(h2(q0, q2), h2(q4, q6), h2(q1, q3), h2(q5, q7));
+            }
+            if (a.dbg.hq) {
+                const uint32_t n0 = (q0 & 255) | ((q1 & 255) << 8) | ((q2 & 255) << 16) | ((uint32_t)(q3 & 255) << 24);
+                const uint32_t n1 = (q4 & 255) | ((q5 & 255) << 8) | ((q6 & 255) << 16) | ((uint32_t)(q7 & 255) << 24);
+                *reinterpret_cast<uint2 *>(a.dbg.hq + (size_t)ent[j] * I + 8 * gi) = make_uint2(n0, n1);
+            }
         }
     }
-    sum = block_sum_i(sum, red_i);
-    if (threadIdx.x == 0) {
-        a.hsum[r] = sum;
-        a.shq[r] = s;
-        if (a.dbg.sh) a.dbg.sh[ent] = s;
+    // the rows' code sums: warp sums, then thread j adds row j's
+#pragma unroll
+    for (int j = 0; j < kRQ; ++j) {
+        const int w = warp_sum_i(sum[j]);
+        if (lane == 0) red_i[j][warp] = w;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kRQ; ++j) {
+        if ((int)threadIdx.x == j && r0 + j < n_rows) {
+            int t = 0;
+            for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red_i[j][w];
+            a.hsum[r0 + j] = t;
+            a.shq[r0 + j] = sc[j];
+            if (a.dbg.sh) a.dbg.sh[ent[j]] = sc[j];
+        }
     }
 }
 
@@ -363,7 +397,7 @@ cudaError_t launch_grouped_gateup(const LayerArgs &a, int num_sms, cudaStream_t 
 }
 
 cudaError_t launch_requant_h(const LayerArgs &a, cudaStream_t s) {
-    requant_h_kernel<<<a.T * a.S, 256, 0, s>>>(a);
+    requant_h_kernel<<<(a.T * a.S + kRQ - 1) / kRQ, 256, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -189,6 +189,15 @@ __device__ __forceinline__ bool mb_wait(uint64_t *b, uint32_t parity, volatile i
     }
 }
 
+// One 32-byte store of 8 fp32 values (32-byte aligned p): a thread writes a
+// whole sector of its row, so the epilogue's scattered row stores take half
+// the instructions of 16-byte ones.
+__device__ __forceinline__ void st_global_v8(float *p, const float *v) {
+    asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(v[0]), "f"(v[1]),
+                 "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+                 : "memory");
+}
+
 // Named barrier 1 over the 128 epilogue threads; returns the OR of p over
 // them, so a decision to leave the loop is the same in every thread.
 __device__ __forceinline__ bool epi_bar_or(bool p) {
@@ -616,9 +625,9 @@ __global__ void __launch_bounds__(Cfg<WTMA>::kThreads, 1)
                         if (a.dbg.gate_acc) a.dbg.gate_acc[(size_t)e * a.I + o0 + jj] = gi;
                         if (a.dbg.up_acc) a.dbg.up_acc[(size_t)e * a.I + o0 + jj] = ui;
                     }
-                    float4 *hp = reinterpret_cast<float4 *>(a.h + (size_t)r * a.I + o0);
+                    float *hp = a.h + (size_t)r * a.I + o0;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) hp[q] = make_float4(hv[4 * q], hv[4 * q + 1], hv[4 * q + 2], hv[4 * q + 3]);
+                    for (int q = 0; q < 2; ++q) st_global_v8(hp + 8 * q, hv + 8 * q);
                 }
             } else {
                 for (int c = 0; c < 8; ++c) {
@@ -634,9 +643,9 @@ __global__ void __launch_bounds__(Cfg<WTMA>::kThreads, 1)
                         yv[jj] = __fmul_rn(__fmul_rn((float)di, ts), sm.wsc[buf][32 * c + jj]);
                         if (a.dbg.down_acc) a.dbg.down_acc[(size_t)e * a.D + o0 + jj] = di;
                     }
-                    float4 *yp = reinterpret_cast<float4 *>(a.part + (size_t)e * a.D + o0);
+                    float *yp = a.part + (size_t)e * a.D + o0;
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) yp[q] = make_float4(yv[4 * q], yv[4 * q + 1], yv[4 * q + 2], yv[4 * q + 3]);
+                    for (int q = 0; q < 4; ++q) st_global_v8(yp + 8 * q, yv + 8 * q);
                 }
             }
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -654,26 +663,37 @@ __global__ void __launch_bounds__(Cfg<WTMA>::kThreads, 1)
 }
 
 // The activation operand of the gate/up GEMM: grouped row r = the int8 codes
-// of its token (even/odd order kept) as f16 integers (exact).
+// of its token (even/odd order kept) as f16 integers (exact).  kAR grouped
+// rows per CTA, each pass's loads of every row issued before the first is
+// converted.
+constexpr int kAR = 4;
 __global__ void __launch_bounds__(256) act_rows_f16_kernel(const int8_t *__restrict__ xq,
                                                            const int32_t *__restrict__ rows, const RouteMeta *meta,
                                                            int S, int D, __half *__restrict__ xf) {
-    const int r = blockIdx.x;
     // grouped rows of this batch: T*S, fewer when adaptive top-p dropped selections
-    if (r >= meta->ubeg[meta->n_union]) return;
-    const int tok = rows[r] / S;
-    const int8_t *src = xq + (size_t)tok * D;
-    __half *dst = xf + (size_t)r * D;
-    for (int g = threadIdx.x; g < (D >> 3); g += blockDim.x) {
-        const uint2 v = __ldg(reinterpret_cast<const uint2 *>(src + 8 * g));
-        uint32_t o[4];
+    const int n_rows = meta->ubeg[meta->n_union];
+    const int r0 = blockIdx.x * kAR;
+    if (r0 >= n_rows) return;
+    int tok[kAR];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const uint32_t word = k < 2 ? v.x : v.y, sh = 16 * (k & 1);
-            const int lo = (int)(int8_t)((word >> sh) & 0xFFu), hi = (int)(int8_t)((word >> (sh + 8)) & 0xFFu);
-            o[k] = (uint32_t)__half_as_ushort(__int2half_rn(lo)) | ((uint32_t)__half_as_ushort(__int2half_rn(hi)) << 16);
+    for (int j = 0; j < kAR; ++j) tok[j] = r0 + j < n_rows ? rows[r0 + j] / S : 0;
+    for (int g = threadIdx.x; g < (D >> 3); g += blockDim.x) {
+        uint2 v[kAR];
+#pragma unroll
+        for (int j = 0; j < kAR; ++j)
+            if (r0 + j < n_rows) v[j] = __ldg(reinterpret_cast<const uint2 *>(xq + (size_t)tok[j] * D + 8 * g));
+#pragma unroll
+        for (int j = 0; j < kAR; ++j) {
+            if (r0 + j >= n_rows) continue;
+            uint32_t o[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t word = k < 2 ? v[j].x : v[j].y, sh = 16 * (k & 1);
+                const int lo = (int)(int8_t)((word >> sh) & 0xFFu), hi = (int)(int8_t)((word >> (sh + 8)) & 0xFFu);
+                o[k] = (uint32_t)__half_as_ushort(__int2half_rn(lo)) | ((uint32_t)__half_as_ushort(__int2half_rn(hi)) << 16);
+            }
+            *reinterpret_cast<uint4 *>(xf + (size_t)(r0 + j) * D + 8 * g) = make_uint4(o[0], o[1], o[2], o[3]);
         }
-        *reinterpret_cast<uint4 *>(dst + 8 * g) = make_uint4(o[0], o[1], o[2], o[3]);
     }
 }
 
@@ -737,7 +757,8 @@ cudaError_t umma_encode_maps(void *xf, int rows, int D, int I, UmmaMaps *maps) {
 }
 
 cudaError_t launch_act_rows_f16(const LayerArgs &a, cudaStream_t s) {
-    act_rows_f16_kernel<<<a.T * a.S, 256, 0, s>>>(a.xq, a.rows, a.meta, a.S, a.D, reinterpret_cast<__half *>(a.xf));
+    act_rows_f16_kernel<<<(a.T * a.S + kAR - 1) / kAR, 256, 0, s>>>(a.xq, a.rows, a.meta, a.S, a.D,
+                                                                   reinterpret_cast<__half *>(a.xf));
     return cudaGetLastError();
 }
 
