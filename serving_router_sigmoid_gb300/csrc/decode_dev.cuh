@@ -364,20 +364,30 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, DecodeSmem &sm,
                 }
             } else {
 #pragma unroll
+                // the unit's RPG rows are consecutive outputs: at one token,
+                // with 4 of them (16-byte aligned: o0 is a multiple of 4),
+                // one 16-byte store (wider batches keep their registers)
+                constexpr bool kY4 = MCH == 1 && RPG == 4;
+                float yv[RPG];
+#pragma unroll
                 for (int rr = 0; rr < RPG; ++rr) {
                     int acc[MM];
 #pragma unroll
                     for (int m = 0; m < MM; ++m) acc[m] = 0;
                     dot_rows<CPL, MM>(acc, R.w[rr], xs, kdim, M, nch, lane);
                     const int mine = lane_sum<MM>(acc, M, lane);
+                    yv[rr] = 0.f;
                     if (lane < M) {
                         const int o = o0 + rr;
                         const int di = mine - 8 * hsum;
-                        const float y = __fmul_rn(__fmul_rn((float)di, sm.sx[lane]), R.s[rr]);
-                        a.part[(size_t)sm.ent[lane] * a.D + o] = y;
+                        yv[rr] = __fmul_rn(__fmul_rn((float)di, sm.sx[lane]), R.s[rr]);
+                        if (!kY4) a.part[(size_t)sm.ent[lane] * a.D + o] = yv[rr];
                         if (a.dbg.down_acc) a.dbg.down_acc[(size_t)sm.ent[lane] * a.D + o] = di;
                     }
                 }
+                if (kY4 && lane < M)
+                    *reinterpret_cast<float4 *>(a.part + (size_t)sm.ent[lane] * a.D + o0) =
+                        make_float4(yv[0], yv[RPG > 1 ? 1 : 0], yv[RPG > 2 ? 2 : 0], yv[RPG > 3 ? 3 : 0]);
             }
         };
         // X holds unit j, Y unit j + 1; each processed set is refilled with
