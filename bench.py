@@ -66,13 +66,13 @@ HOT_KERNEL_PREFILL = ("umma_gemm_kernel<0, 1> (tcgen05 f16-exact gate/up GEMM, t
 TRAFFIC = {
     # decode_layer_kernel at decode batch 1 (DRAM byte counters of 3 launches,
     # one resident GLM-shaped layer set, caches flushed before each):
-    # 176.72 MB read + 0.30 MB written per launch
-    "glm_moe_layer_decode_b1": 177.02e6,
+    # 176.72 MB read + 0.37 MB written per launch
+    "glm_moe_layer_decode_b1": 177.09e6,
     # umma_gemm_kernel<0, 1> (gate/up, packed weights by TMA) at prefill 2048,
     # full capture of the profiling layout (16 physical experts aliased over
     # the 257 table entries; the routing, tiles and bytes per tile are the
-    # full layer's): 2.507 GB read + 0.133 GB written per launch
-    "glm_moe_layer_prefill_2048": 2.640e9,
+    # full layer's): 2.550 GB read + 0.134 GB written per launch
+    "glm_moe_layer_prefill_2048": 2.684e9,
 }
 
 
