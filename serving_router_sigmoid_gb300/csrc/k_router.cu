@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(256) router_tile_kernel(const float *__restric
 // ------------------------------------------------ large-batch router (2 kernels)
 
 // Logits of a large batch as a register-tiled fp32 GEMM: CTA tile 128 tokens
-// x 128 experts, K in chunks of 16 through a 4-stage cp.async ring (rows kept
+// x 128 experts, K in chunks of 32 through a 4-stage cp.async ring (rows kept
 // d-contiguous, so no transpose on the way in), 256 threads each
 // accumulating 8 tokens x 8 experts (rows ty + 16 i, columns tx + 16 j, which
 // keeps the shared-memory reads conflict-free) with one fmaf chain per output
@@ -264,8 +264,8 @@ __global__ void __launch_bounds__(256) router_tile_kernel(const float *__restric
 // per SM.  K is split into gridDim.z contiguous ranges of whole chunks (at T
 // = 2048 the 32 tiles x 9 ranges make two waves of the 152 SMs); range z
 // writes its partial logits to logits + z T E and the select kernel adds the
-// partials in z order.  D % 16 == 0; rows past T or E read zeros.
-constexpr int kRLM = 128, kRLK = 16, kRLStages = 4, kRLPitch = kRLK + 4;  // floats per staged row
+// partials in z order.  D % 32 == 0; rows past T or E read zeros.
+constexpr int kRLM = 128, kRLK = 32, kRLStages = 4, kRLPitch = kRLK + 4;  // floats per staged row
 constexpr size_t kRLStageFloats = 2 * (size_t)kRLM * kRLPitch;
 constexpr size_t kRLSmemBytes = kRLStages * kRLStageFloats * sizeof(float);
 
@@ -288,8 +288,9 @@ __global__ void __launch_bounds__(256, 1) router_logits_kernel(const float *__re
     auto load_stage = [&](int stage, int chunk) {
         float *st = rls + (size_t)stage * kRLStageFloats;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int q = tid + 256 * i, op = q >> 9, row = (q >> 2) & (kRLM - 1), seg = q & 3;
+        for (int i = 0; i < kRLK / 4; ++i) {
+            const int q = tid + 256 * i, op = q / (kRLM * (kRLK / 4)), row = (q / (kRLK / 4)) % kRLM,
+                      seg = q % (kRLK / 4);
             const int g = (op == 0 ? m0 : n0) + row, lim = op == 0 ? T : E;
             const float *src = (op == 0 ? x : Wr) + (size_t)(g < lim ? g : lim - 1) * D + chunk * kRLK + seg * 4;
             rl_cp_async16(st + (size_t)op * kRLM * kRLPitch + row * kRLPitch + seg * 4, src, g < lim);
