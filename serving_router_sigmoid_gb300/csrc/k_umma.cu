@@ -712,7 +712,7 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link
-// against the driver library).
+// against libcuda).
 cudaError_t encode_fn(EncodeTiledFn *out) {
     static EncodeTiledFn fn = nullptr;
     if (!fn) {
